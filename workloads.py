@@ -1,0 +1,125 @@
+"""Seeded synthetic inputs for the Q8_0 linear layer (shared by tests and the benchmark).
+
+This module only draws random numbers and shapes them; it holds none of the method's
+arithmetic (no quantization, no scales, no dot products), so it can feed both the CUDA
+library and the CPU oracle without coupling them.
+
+Recipe (numpy PCG64 via default_rng):
+  * weights  W = standard_normal((N, K), float32) * 0.02
+  * activations x = standard_normal((M, K), float32); for the outlier workload a fixed
+    set of round(0.01*K) channels (K indices, the same for every row) is multiplied by
+    20 in float32; then x is rounded to bfloat16 (nearest-even) unless the workload is
+    float32.
+  * one generator per (workload, projection) for weights, and one per (workload,
+    projection, M) for activations, seeded as listed in SEEDS below.
+"""
+from dataclasses import dataclass, field
+from typing import List, Tuple
+
+import numpy as np
+
+QK = 32
+
+
+def bf16_bits_from_f32(x32: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns, round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(x32, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = u + 0x7FFF + ((u >> 16) & 1)
+    return ((u >> 16) & 0xFFFF).astype(np.uint16)
+
+
+def f32_from_bf16_bits(b: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def weights(rng: np.random.Generator, N: int, K: int, std: float = 0.02) -> np.ndarray:
+    return (rng.standard_normal((N, K), dtype=np.float32) * np.float32(std)).astype(np.float32)
+
+
+def activations(rng: np.random.Generator, M: int, K: int, bf16: bool = True,
+                outlier_frac: float = 0.0, outlier_gain: float = 20.0):
+    """Returns (x, outlier_channels): x is uint16 bf16 bits when bf16 else float32."""
+    x = rng.standard_normal((M, K), dtype=np.float32)
+    idx = np.zeros(0, np.int64)
+    if outlier_frac > 0.0:
+        cnt = int(round(outlier_frac * K))
+        idx = np.sort(rng.choice(K, size=cnt, replace=False)).astype(np.int64)
+        x[:, idx] *= np.float32(outlier_gain)
+    if bf16:
+        return bf16_bits_from_f32(x), idx
+    return x, idx
+
+
+@dataclass
+class Linear:
+    """One projection shape: y[M,N] = x[M,K] . W[N,K]^T."""
+    name: str
+    K: int
+    N: int
+
+
+@dataclass
+class Workload:
+    name: str
+    seed: int
+    projections: List[Linear]
+    Ms: List[int]
+    bf16: bool = True
+    outlier_frac: float = 0.0
+    notes: str = ""
+    extra: dict = field(default_factory=dict)
+
+    def weight_rng(self, p: int) -> np.random.Generator:
+        return np.random.default_rng([self.seed, 1000 + p])
+
+    def act_rng(self, p: int, mi: int) -> np.random.Generator:
+        return np.random.default_rng([self.seed, 2000 + 100 * mi + p])
+
+    def make_weights(self, p: int) -> np.ndarray:
+        pr = self.projections[p]
+        return weights(self.weight_rng(p), pr.N, pr.K)
+
+    def make_act(self, p: int, mi: int):
+        pr = self.projections[p]
+        return activations(self.act_rng(p, mi), self.Ms[mi], pr.K, bf16=self.bf16,
+                           outlier_frac=self.outlier_frac)
+
+    def cases(self) -> List[Tuple[int, int]]:
+        """(projection index, M index) pairs, M outermost."""
+        return [(p, mi) for mi in range(len(self.Ms)) for p in range(len(self.projections))]
+
+
+HIDDEN = 5120
+FFN_27B = 17408
+
+WORKLOADS = {
+    # tiny Q8_0 linear, float32 activations
+    "tiny": Workload("tiny", 0, [Linear("tiny", 512, 256)], [16], bf16=False),
+    # decode: FFN up-projection of a dense ~9B-class layer, M = 1 and batched decode
+    "decode": Workload("decode", 1, [Linear("up", 4096, 12288)], [1, 4, 16, 64]),
+    # prefill, 9B-class up and down projections
+    "prefill9b": Workload("prefill9b", 2, [Linear("up", 4096, 12288), Linear("down", 12288, 4096)],
+                          [2048]),
+    # prefill, 27B-class shapes, 1% of activation channels scaled x20
+    "prefill27b": Workload("prefill27b", 3, [Linear("up", HIDDEN, FFN_27B),
+                                             Linear("down", FFN_27B, HIDDEN)], [8192],
+                           outlier_frac=0.01),
+    # every linear of a synthetic hybrid layer with hidden size 5120
+    "sweep": Workload("sweep", 4, [Linear("q", HIDDEN, HIDDEN), Linear("k", HIDDEN, HIDDEN),
+                                   Linear("v", HIDDEN, HIDDEN), Linear("o", HIDDEN, HIDDEN),
+                                   Linear("gate", HIDDEN, FFN_27B), Linear("up", HIDDEN, FFN_27B),
+                                   Linear("down", FFN_27B, HIDDEN),
+                                   Linear("gdn_in", HIDDEN, 10240)],
+                      [1, 4, 16, 128, 512, 2048, 8192]),
+}
+
+
+def algorithmic_bytes(M: int, N: int, K: int, x_bytes: int = 2) -> int:
+    """Bytes a Q8_0 linear must move at least once: codes + binary16 scales of W,
+    the activations, and the float32 output."""
+    return N * K + 2 * N * (K // QK) + x_bytes * M * K + 4 * M * N
+
+
+def algorithmic_ops(M: int, N: int, K: int) -> int:
+    """int8-equivalent multiply-add operations (2 per MAC); block rescales excluded."""
+    return 2 * M * N * K
