@@ -1,0 +1,147 @@
+/*
+ * q8.h -- C ABI of libq8: the Q8_0 block-quantized linear layer on GB300 (sm_103a).
+ *
+ * The operation.  The post "CUDA inference engine for running Qwen3.5/3.6 hybrid models
+ * on mining cards (CMP 100-210)" (news.hada.io topic 29953) runs the linear layers of its
+ * dense GDN + attention models as an int8 GEMM over Q8_0 weights (list of un-throttled
+ * paths: the DP4A int8 GEMM; "Limitations" list: Q8_0 is the only supported type).
+ * This library computes that layer with this Q8_0 definition:
+ *   - K is cut into blocks of 32 consecutive elements (K must be a multiple of 32);
+ *   - per block: amax = max |v|, d = amax / 127 in IEEE binary32, codes
+ *     q = round(v / d) (one IEEE binary32 division, ties away from zero, clamped to
+ *     [-127, 127]); an all-zero block (or one whose d underflows to 0) gets d = 0 and
+ *     codes 0;
+ *   - weight scales are stored as IEEE binary16 (round to nearest even), activation
+ *     scales as binary32;
+ *   - y[m,n] = sum_b Wd[n,b] * xd[m,b] * isum[m,n,b], with the exact integer block dot
+ *     isum[m,n,b] = sum_{j<32} xq[m,32b+j] * Wq[n,32b+j]  (|isum| <= 516128).
+ * Codes, scales and block sums are exact; y is a binary32 sum whose order is not fixed.
+ *
+ * Layouts (row-major, K contiguous, nn.Linear orientation y = x W^T):
+ *   W  float   [N, K]          Wq int8  [N, K]      Wd uint16 [N, K/32]  (binary16 bits)
+ *   x  bf16/f32 [M, K]         xq int8  [M, K]      xd float  [M, K/32]
+ *   y  float   [M, N]          isum int32 [M, N, K/32]
+ *
+ * Conventions for every entry point:
+ *   - all array pointers are DEVICE pointers owned by the caller; the library never
+ *     frees or keeps them; every array pointer must be 16-byte aligned; the pointer of an
+ *     empty array (zero elements) may be NULL;
+ *   - calls are asynchronous on `stream` (0 = the legacy default stream); inputs must
+ *     stay valid and outputs untouched until the stream passes the call;
+ *   - arguments are checked on the host before anything is launched; on any error
+ *     nothing is launched and the status says why; Q8_ERR_CUDA reports a failed CUDA
+ *     runtime call (its text: q8_last_cuda_error());
+ *   - the current CUDA device must be a compute capability 10.3 GPU (GB300);
+ *   - inputs must be finite (NaN / Inf are outside the domain and not checked).
+ */
+#ifndef Q8_H
+#define Q8_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum q8_status {
+    Q8_OK = 0,
+    Q8_ERR_NULL = 1,     /* a required pointer is NULL                                 */
+    Q8_ERR_SHAPE = 2,    /* M, N or K < 0, K not a multiple of 32, or a size overflows  */
+    Q8_ERR_ALIGN = 3,    /* an array pointer is not 16-byte aligned                     */
+    Q8_ERR_DTYPE = 4,    /* unknown activation type or path selector                    */
+    Q8_ERR_NOMEM = 5,    /* workspace too small, or the library could not allocate one  */
+    Q8_ERR_CUDA = 6,     /* a CUDA runtime call failed                                  */
+    Q8_ERR_DEVICE = 7,   /* the current device is not compute capability 10.3           */
+    Q8_ERR_CAPTURE = 8   /* the call would allocate while its stream is being captured  */
+} q8_status;
+
+typedef enum q8_dtype {
+    Q8_F32 = 0,          /* IEEE binary32 activations                                   */
+    Q8_BF16 = 1          /* bfloat16 activations (uint16 bit patterns)                  */
+} q8_dtype;
+
+/* Which kernel family computes the product.  AUTO picks by M (decode kernel for small
+ * M, tensor-core GEMM otherwise); the explicit choices exist for tests and benchmarks. */
+typedef enum q8_path {
+    Q8_PATH_AUTO = 0,
+    Q8_PATH_DECODE = 1,  /* weight-streaming kernel (int8 dot products, fused act-quant) */
+    Q8_PATH_TENSOR = 2   /* tcgen05 tensor-core GEMM with per-block rescale             */
+} q8_path;
+
+/*
+ * q8_quantize_weights -- Q8_0 weight quantizer (one-off, per weight matrix).
+ *   W  [N,K] float in;  Wq [N,K] int8 out;  Wd [N,K/32] binary16 bits out.
+ *   N, K >= 0 (zero sizes launch nothing), K % 32 == 0.
+ */
+q8_status q8_quantize_weights(const float* W, int8_t* Wq, uint16_t* Wd, int64_t N, int64_t K,
+                              cudaStream_t stream);
+
+/*
+ * q8_quantize_act -- Q8_0 activation quantizer.
+ *   x [M,K] of type xtype in;  xq [M,K] int8 out;  xd [M,K/32] float out.
+ */
+q8_status q8_quantize_act(const void* x, q8_dtype xtype, int8_t* xq, float* xd, int64_t M,
+                          int64_t K, cudaStream_t stream);
+
+/*
+ * q8_linear -- y = Q8_0 linear layer of bf16 activations x:  y[M,N] = x[M,K] . W^T through
+ * the codes above (activations are quantized per call, inside the library).
+ *   x [M,K] bf16 in;  Wq, Wd from q8_quantize_weights;  y [M,N] float out (overwritten).
+ * Scratch memory (quantized activations, at most 2*M*K + 4*M*(K/32) bytes plus 2*N*K for
+ * the tensor-core path) is owned by the library, one buffer per (device, stream); it
+ * grows on demand with cudaMalloc, which is not allowed while the stream is captured:
+ * make the first call with the largest shape before capturing (else Q8_ERR_CAPTURE).
+ * q8_release() frees it.
+ */
+q8_status q8_linear(const void* x, const int8_t* Wq, const uint16_t* Wd, float* y, int64_t M,
+                    int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * q8_linear_ex -- q8_linear with the activation type, the kernel family and the scratch
+ * memory chosen by the caller.  workspace may be NULL only if workspace_bytes is 0 and
+ * q8_linear_workspace_size() returns 0 for the chosen path; never allocates.
+ */
+q8_status q8_linear_ex(const void* x, q8_dtype xtype, const int8_t* Wq, const uint16_t* Wd,
+                       float* y, int64_t M, int64_t N, int64_t K, q8_path path,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of scratch q8_linear_ex needs for this shape and path (0 if none). */
+size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path);
+
+/*
+ * q8_block_sums -- the exact int32 block dot products isum[M,N,K/32] of given codes,
+ * computed by the same kernel code as q8_linear on the chosen path (TENSOR: the tcgen05
+ * MMAs whose binary32 TMEM results the rescale reads; DECODE: the dp4a kernel).  Meant
+ * for checking; scratch as for q8_linear (library-owned).
+ */
+q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64_t M, int64_t N,
+                        int64_t K, q8_path path, cudaStream_t stream);
+
+/*
+ * q8_device_error -- synchronizes the current device, then returns (and clears) the
+ * library's device error word: bit 0 = a bounded device-side wait gave up (the results
+ * of that call are undefined), bit 1 = a kernel met launch parameters it cannot handle.
+ * 0 means no error.  Returns Q8_ERR_CUDA through *status if the sync itself failed.
+ */
+uint32_t q8_device_error(q8_status* status);
+
+/* Human-readable text of a status code (static storage). */
+const char* q8_status_string(q8_status status);
+
+/* Text of the last CUDA error seen by the calling thread in this library (static/TLS). */
+const char* q8_last_cuda_error(void);
+
+/* Frees library-owned scratch memory on every device.  Not thread-safe against calls in
+ * flight: call it when no q8_linear / q8_block_sums call is running. */
+void q8_release(void);
+
+/* Library version, e.g. "0.1.0". */
+const char* q8_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q8_H */

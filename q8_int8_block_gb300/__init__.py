@@ -1,0 +1,210 @@
+"""Python binding of libq8 (include/q8.h): the Q8_0 block-quantized linear layer on GB300.
+
+Argument marshalling only: every step of the layer runs in the CUDA library.  Tensors
+are torch tensors on the current CUDA device (torch provides device memory and streams);
+each function passes raw pointers, sizes and the current stream to the C ABI and raises
+Q8Error on a non-OK status.  There is no CPU fallback: if libq8.so is missing, importing
+this package fails.
+
+    Wq, Wd = q8_quantize_weights(W)              # W float32 [N,K] -> int8 [N,K], fp16 bits [N,K/32]
+    xq, xd = q8_quantize_act(x)                  # x bf16/float32 [M,K] -> int8 [M,K], float32 [M,K/32]
+    y = q8_linear(x, Wq, Wd)                     # x bf16 [M,K] -> float32 [M,N]
+    y = q8_linear_ex(x, Wq, Wd, path="tensor", workspace=ws)
+    isum = q8_block_sums(xq, Wq, path="decode")  # int32 [M,N,K/32]
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = ["Q8Error", "q8_quantize_weights", "q8_quantize_act", "q8_linear", "q8_linear_ex",
+           "q8_linear_workspace_size", "q8_block_sums", "q8_device_error", "q8_release",
+           "q8_version", "lib_path", "QK", "PATHS"]
+
+QK = 32
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libq8.so")
+
+STATUS = {0: "Q8_OK", 1: "Q8_ERR_NULL", 2: "Q8_ERR_SHAPE", 3: "Q8_ERR_ALIGN", 4: "Q8_ERR_DTYPE",
+          5: "Q8_ERR_NOMEM", 6: "Q8_ERR_CUDA", 7: "Q8_ERR_DEVICE", 8: "Q8_ERR_CAPTURE"}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+PATHS = {"auto": 0, "decode": 1, "tensor": 2}
+
+
+class Q8Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = _L.q8_status_string(status).decode()
+        if status == 6:
+            msg += ": " + _L.q8_last_cuda_error().decode()
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({msg})")
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"libq8.so is not built ({_LIB_PATH}); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(_LIB_PATH)
+    p, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    sigs = {
+        "q8_quantize_weights": [p, p, p, i64, i64, p],
+        "q8_quantize_act": [p, i32, p, p, i64, i64, p],
+        "q8_linear": [p, p, p, p, i64, i64, i64, p],
+        "q8_linear_ex": [p, i32, p, p, p, i64, i64, i64, i32, p, sz, p],
+        "q8_block_sums": [p, p, p, i64, i64, i64, i32, p],
+    }
+    for name, args in sigs.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = i32
+    L.q8_linear_workspace_size.argtypes = [i64, i64, i64, i32]
+    L.q8_linear_workspace_size.restype = sz
+    L.q8_device_error.argtypes = [ctypes.POINTER(i32)]
+    L.q8_device_error.restype = ctypes.c_uint32
+    L.q8_status_string.argtypes = [i32]
+    L.q8_status_string.restype = ctypes.c_char_p
+    L.q8_last_cuda_error.argtypes = []
+    L.q8_last_cuda_error.restype = ctypes.c_char_p
+    L.q8_release.argtypes = []
+    L.q8_release.restype = None
+    L.q8_version.argtypes = []
+    L.q8_version.restype = ctypes.c_char_p
+    return L
+
+
+_L = _load()
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    return _L
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise Q8Error(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, shape, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: must be a contiguous CUDA tensor")
+
+
+def q8_quantize_weights(W, Wq=None, Wd=None, stream=None):
+    """W float32 [N,K] -> (Wq int8 [N,K], Wd int16-stored binary16 bits [N,K/32])."""
+    N, K = W.shape
+    _need(W, torch.float32, (N, K), "W")
+    if Wq is None:
+        Wq = torch.empty((N, K), dtype=torch.int8, device=W.device)
+    if Wd is None:
+        Wd = torch.empty((N, K // QK), dtype=torch.int16, device=W.device)
+    _need(Wq, torch.int8, (N, K), "Wq")
+    _need(Wd, torch.int16, (N, K // QK), "Wd")
+    _check(_L.q8_quantize_weights(_ptr(W), _ptr(Wq), _ptr(Wd), N, K, _stream(stream)),
+           "q8_quantize_weights")
+    return Wq, Wd
+
+
+def q8_quantize_act(x, xq=None, xd=None, stream=None):
+    """x bf16 or float32 [M,K] -> (xq int8 [M,K], xd float32 [M,K/32])."""
+    M, K = x.shape
+    if x.dtype not in DTYPES:
+        raise TypeError(f"x: expected bfloat16 or float32, got {x.dtype}")
+    _need(x, x.dtype, (M, K), "x")
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if xd is None:
+        xd = torch.empty((M, K // QK), dtype=torch.float32, device=x.device)
+    _need(xq, torch.int8, (M, K), "xq")
+    _need(xd, torch.float32, (M, K // QK), "xd")
+    _check(_L.q8_quantize_act(_ptr(x), DTYPES[x.dtype], _ptr(xq), _ptr(xd), M, K, _stream(stream)),
+           "q8_quantize_act")
+    return xq, xd
+
+
+def _lin_check(x, Wq, Wd, y):
+    M, K = x.shape
+    N = Wq.shape[0]
+    _need(Wq, torch.int8, (N, K), "Wq")
+    _need(Wd, torch.int16, (N, K // QK), "Wd")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _need(y, torch.float32, (M, N), "y")
+    return M, N, K, y
+
+
+def q8_linear(x, Wq, Wd, y=None, stream=None):
+    """y float32 [M,N] = Q8_0 linear of bf16 x [M,K] (library-owned scratch)."""
+    _need(x, torch.bfloat16, tuple(x.shape), "x")
+    M, N, K, y = _lin_check(x, Wq, Wd, y)
+    _check(_L.q8_linear(_ptr(x), _ptr(Wq), _ptr(Wd), _ptr(y), M, N, K, _stream(stream)),
+           "q8_linear")
+    return y
+
+
+def q8_linear_workspace_size(M, N, K, path="auto") -> int:
+    return int(_L.q8_linear_workspace_size(M, N, K, PATHS[path]))
+
+
+def q8_linear_ex(x, Wq, Wd, y=None, path="auto", workspace=None, stream=None):
+    """q8_linear with activation type (bf16/float32), kernel family and caller scratch.
+    workspace: a uint8 CUDA tensor of at least q8_linear_workspace_size() bytes, or None
+    (then one is allocated here with torch)."""
+    if x.dtype not in DTYPES:
+        raise TypeError(f"x: expected bfloat16 or float32, got {x.dtype}")
+    _need(x, x.dtype, tuple(x.shape), "x")
+    M, N, K, y = _lin_check(x, Wq, Wd, y)
+    need = q8_linear_workspace_size(M, N, K, path)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_L.q8_linear_ex(_ptr(x), DTYPES[x.dtype], _ptr(Wq), _ptr(Wd), _ptr(y), M, N, K,
+                           PATHS[path], _ptr(workspace), nbytes, _stream(stream)), "q8_linear_ex")
+    return y
+
+
+def q8_block_sums(xq, Wq, isum=None, path="auto", stream=None):
+    """Exact int32 block sums isum [M,N,K/32] of int8 codes, by the kernel of `path`."""
+    M, K = xq.shape
+    N = Wq.shape[0]
+    _need(xq, torch.int8, (M, K), "xq")
+    _need(Wq, torch.int8, (N, K), "Wq")
+    if isum is None:
+        isum = torch.empty((M, N, K // QK), dtype=torch.int32, device=xq.device)
+    _need(isum, torch.int32, (M, N, K // QK), "isum")
+    _check(_L.q8_block_sums(_ptr(xq), _ptr(Wq), _ptr(isum), M, N, K, PATHS[path], _stream(stream)),
+           "q8_block_sums")
+    return isum
+
+
+def q8_device_error() -> int:
+    """Synchronizes the device and returns (and clears) the device error word (0 = none)."""
+    st = ctypes.c_int(0)
+    word = _L.q8_device_error(ctypes.byref(st))
+    _check(st.value, "q8_device_error")
+    return int(word)
+
+
+def q8_release():
+    _L.q8_release()
+
+
+def q8_version() -> str:
+    return _L.q8_version().decode()

@@ -1,0 +1,313 @@
+// q8_api.cu -- the C ABI of libq8 (declared in include/q8.h): host-side argument
+// checks, device checks, scratch management and dispatch to the kernels.
+//
+// Nothing is launched unless every check passes.  Every launch is asynchronous on the
+// caller's stream; the library holds no lock while kernels run.
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/q8.h"
+#include "q8_internal.h"
+
+namespace q8 {
+namespace {
+
+// The library's device error word (one per device that loads the library).  Kernels
+// get its address as a parameter and atomically OR error bits into it.
+__device__ uint32_t g_err_word;
+
+thread_local char g_last_cuda_error[256] = "no error";
+
+q8_status cuda_fail(cudaError_t e) {
+  std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return Q8_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+// Checks the current device and fills its info on first use.
+q8_status current_device(DeviceInfo* out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return Q8_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.device < 0) {
+    int major = 0, minor = 0, sms = 0, smem = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+            cudaSuccess)
+      return cuda_fail(e);
+    if (major != 10 || minor != 3) return Q8_ERR_DEVICE;
+    void* addr = nullptr;
+    if ((e = cudaGetSymbolAddress(&addr, g_err_word)) != cudaSuccess) return cuda_fail(e);
+    d.sm_count = sms;
+    d.max_smem_optin = smem;
+    d.err_word = static_cast<uint32_t*>(addr);
+    d.device = dev;
+  }
+  *out = d;
+  return Q8_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// M, N, K in [0, 2^31), K % 32 == 0, and byte sizes that fit comfortably in 64 bits.
+q8_status check_shape(int64_t M, int64_t N, int64_t K) {
+  const int64_t lim = static_cast<int64_t>(0x7FFFFFFF);
+  if (M < 0 || N < 0 || K < 0 || M > lim || N > lim || K > lim) return Q8_ERR_SHAPE;
+  if (K % kQK != 0) return Q8_ERR_SHAPE;
+  // every array the library touches is below 2^48 bytes
+  const double big = 281474976710656.0;
+  if (static_cast<double>(M) * K * 4 > big || static_cast<double>(N) * K * 4 > big ||
+      static_cast<double>(M) * N * 4 > big)
+    return Q8_ERR_SHAPE;
+  return Q8_OK;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// Resolves AUTO; returns Q8_ERR_SHAPE if the requested path cannot run this shape.
+q8_status resolve_path(int64_t M, int64_t K, q8_path req, const DeviceInfo& dev, q8_path* out) {
+  const bool decode_ok = decode_smem_bytes(M < 1 ? 1 : M, K, dev) != 0 && M <= kDecodeMaxM;
+  if (req == Q8_PATH_AUTO) {
+    *out = decode_ok ? Q8_PATH_DECODE : Q8_PATH_TENSOR;
+    return Q8_OK;
+  }
+  if (req == Q8_PATH_DECODE) {
+    if (!decode_ok) return Q8_ERR_SHAPE;
+    *out = req;
+    return Q8_OK;
+  }
+  if (req == Q8_PATH_TENSOR) {
+    *out = req;
+    return Q8_OK;
+  }
+  return Q8_ERR_DTYPE;
+}
+
+// Scratch of the tensor path: A16 [M,K] f16 codes, xd [M,K/32] f32, B16 [N,K] f16 codes.
+size_t tensor_ws_bytes(int64_t M, int64_t N, int64_t K) {
+  return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(M) * (K / kQK) * 4) +
+         align256(static_cast<size_t>(N) * K * 2);
+}
+
+// Library-owned scratch for (current device, stream), grown on demand.
+q8_status library_workspace(const DeviceInfo& dev, cudaStream_t stream, size_t bytes, void** out) {
+  *out = nullptr;
+  if (bytes == 0) return Q8_OK;
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace& w = g_ws[{dev.device, stream}];
+  if (w.bytes >= bytes) {
+    *out = w.ptr;
+    return Q8_OK;
+  }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (cap != cudaStreamCaptureStatusNone) return Q8_ERR_CAPTURE;
+  void* p = nullptr;
+  e = cudaMallocAsync(&p, bytes, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? Q8_ERR_NOMEM : cuda_fail(e);
+  }
+  if (w.ptr != nullptr) cudaFreeAsync(w.ptr, stream);  // stream-ordered: after prior users
+  w.ptr = p;
+  w.bytes = bytes;
+  *out = p;
+  return Q8_OK;
+}
+
+q8_status launch_status(cudaError_t e) { return e == cudaSuccess ? Q8_OK : cuda_fail(e); }
+
+q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uint16_t* Wd,
+                      float* y, int64_t M, int64_t N, int64_t K, q8_path path, void* ws,
+                      size_t ws_bytes, bool library_ws, cudaStream_t stream) {
+  if (xtype != Q8_F32 && xtype != Q8_BF16) return Q8_ERR_DTYPE;
+  if (path != Q8_PATH_AUTO && path != Q8_PATH_DECODE && path != Q8_PATH_TENSOR) return Q8_ERR_DTYPE;
+  q8_status st = check_shape(M, N, K);
+  if (st != Q8_OK) return st;
+  // pointers of empty arrays may be NULL
+  if ((M * K > 0 && x == nullptr) || (N * K > 0 && (Wq == nullptr || Wd == nullptr)) ||
+      (M * N > 0 && y == nullptr))
+    return Q8_ERR_NULL;
+  if (!aligned16(x) || !aligned16(Wq) || !aligned16(Wd) || !aligned16(y)) return Q8_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != Q8_OK) return st;
+  q8_path p;
+  if ((st = resolve_path(M, K, path, dev, &p)) != Q8_OK) return st;
+  if (M == 0 || N == 0) return Q8_OK;
+  if (K == 0) return launch_status(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 4, stream));
+  if (p == Q8_PATH_DECODE)
+    return launch_status(launch_decode(x, static_cast<int>(xtype), nullptr, Wq, Wd, y, nullptr, M,
+                                       N, K, dev, stream));
+  const size_t need = tensor_ws_bytes(M, N, K);
+  if (library_ws) {
+    if ((st = library_workspace(dev, stream, need, &ws)) != Q8_OK) return st;
+  } else {
+    if (ws == nullptr) return Q8_ERR_NULL;
+    if (!aligned16(ws)) return Q8_ERR_ALIGN;
+    if (ws_bytes < need) return Q8_ERR_NOMEM;
+  }
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  uint16_t* A16 = reinterpret_cast<uint16_t*>(w8);
+  float* xd = reinterpret_cast<float*>(w8 + align256(static_cast<size_t>(M) * K * 2));
+  uint16_t* B16 = reinterpret_cast<uint16_t*>(w8 + align256(static_cast<size_t>(M) * K * 2) +
+                                              align256(static_cast<size_t>(M) * (K / kQK) * 4));
+  cudaError_t e = launch_quantize(x, static_cast<int>(xtype), A16, true, xd, false, M, K, dev, stream);
+  if (e == cudaSuccess) e = launch_codes_to_f16(Wq, B16, N * K, dev, stream);
+  if (e == cudaSuccess) e = launch_gemm_tc(A16, B16, xd, Wd, y, nullptr, M, N, K, dev, stream);
+  return launch_status(e);
+}
+
+}  // namespace
+}  // namespace q8
+
+using namespace q8;
+
+extern "C" {
+
+q8_status q8_quantize_weights(const float* W, int8_t* Wq, uint16_t* Wd, int64_t N, int64_t K,
+                              cudaStream_t stream) {
+  q8_status st = check_shape(0, N, K);
+  if (st != Q8_OK) return st;
+  if (N * K > 0 && (W == nullptr || Wq == nullptr || Wd == nullptr)) return Q8_ERR_NULL;
+  if (!aligned16(W) || !aligned16(Wq) || !aligned16(Wd)) return Q8_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != Q8_OK) return st;
+  return launch_status(launch_quantize(W, 0, Wq, false, Wd, true, N, K, dev, stream));
+}
+
+q8_status q8_quantize_act(const void* x, q8_dtype xtype, int8_t* xq, float* xd, int64_t M,
+                          int64_t K, cudaStream_t stream) {
+  if (xtype != Q8_F32 && xtype != Q8_BF16) return Q8_ERR_DTYPE;
+  q8_status st = check_shape(M, 0, K);
+  if (st != Q8_OK) return st;
+  if (M * K > 0 && (x == nullptr || xq == nullptr || xd == nullptr)) return Q8_ERR_NULL;
+  if (!aligned16(x) || !aligned16(xq) || !aligned16(xd)) return Q8_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != Q8_OK) return st;
+  return launch_status(
+      launch_quantize(x, static_cast<int>(xtype), xq, false, xd, false, M, K, dev, stream));
+}
+
+q8_status q8_linear(const void* x, const int8_t* Wq, const uint16_t* Wd, float* y, int64_t M,
+                    int64_t N, int64_t K, cudaStream_t stream) {
+  return linear_impl(x, Q8_BF16, Wq, Wd, y, M, N, K, Q8_PATH_AUTO, nullptr, 0, true, stream);
+}
+
+q8_status q8_linear_ex(const void* x, q8_dtype xtype, const int8_t* Wq, const uint16_t* Wd,
+                       float* y, int64_t M, int64_t N, int64_t K, q8_path path, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+  return linear_impl(x, xtype, Wq, Wd, y, M, N, K, path, workspace, workspace_bytes, false, stream);
+}
+
+size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path) {
+  if (check_shape(M, N, K) != Q8_OK) return 0;
+  DeviceInfo dev;
+  if (current_device(&dev) != Q8_OK) return 0;
+  q8_path p;
+  if (resolve_path(M, K, path, dev, &p) != Q8_OK) return 0;
+  if (p == Q8_PATH_DECODE || M == 0 || N == 0 || K == 0) return 0;
+  return tensor_ws_bytes(M, N, K);
+}
+
+q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64_t M, int64_t N,
+                        int64_t K, q8_path path, cudaStream_t stream) {
+  if (path != Q8_PATH_AUTO && path != Q8_PATH_DECODE && path != Q8_PATH_TENSOR) return Q8_ERR_DTYPE;
+  q8_status st = check_shape(M, N, K);
+  if (st != Q8_OK) return st;
+  if ((M * K > 0 && xq == nullptr) || (N * K > 0 && Wq == nullptr) || (M * N * K > 0 && isum == nullptr))
+    return Q8_ERR_NULL;
+  if (!aligned16(xq) || !aligned16(Wq) || !aligned16(isum)) return Q8_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != Q8_OK) return st;
+  q8_path p;
+  if ((st = resolve_path(M, K, path, dev, &p)) != Q8_OK) return st;
+  if (M == 0 || N == 0 || K == 0) return Q8_OK;
+  if (p == Q8_PATH_DECODE)
+    return launch_status(
+        launch_decode(nullptr, 0, xq, Wq, nullptr, nullptr, isum, M, N, K, dev, stream));
+  const size_t need = align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(N) * K * 2);
+  void* ws = nullptr;
+  if ((st = library_workspace(dev, stream, need, &ws)) != Q8_OK) return st;
+  uint16_t* A16 = static_cast<uint16_t*>(ws);
+  uint16_t* B16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) +
+                                              align256(static_cast<size_t>(M) * K * 2));
+  cudaError_t e = launch_codes_to_f16(xq, A16, M * K, dev, stream);
+  if (e == cudaSuccess) e = launch_codes_to_f16(Wq, B16, N * K, dev, stream);
+  if (e == cudaSuccess)
+    e = launch_gemm_tc(A16, B16, nullptr, nullptr, nullptr, isum, M, N, K, dev, stream);
+  return launch_status(e);
+}
+
+uint32_t q8_device_error(q8_status* status) {
+  if (status) *status = Q8_OK;
+  DeviceInfo dev;
+  q8_status st = current_device(&dev);
+  if (st != Q8_OK) {
+    if (status) *status = st;
+    return 0;
+  }
+  cudaError_t e = cudaDeviceSynchronize();
+  uint32_t word = 0;
+  const uint32_t zero = 0;
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&word, g_err_word, sizeof word);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_err_word, &zero, sizeof zero);
+  if (e != cudaSuccess) {
+    cuda_fail(e);
+    if (status) *status = Q8_ERR_CUDA;
+  }
+  return word;
+}
+
+const char* q8_status_string(q8_status s) {
+  switch (s) {
+    case Q8_OK: return "ok";
+    case Q8_ERR_NULL: return "a required pointer is NULL";
+    case Q8_ERR_SHAPE: return "bad shape (negative size, K not a multiple of 32, too large, or not supported by the chosen path)";
+    case Q8_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case Q8_ERR_DTYPE: return "unknown activation type or path";
+    case Q8_ERR_NOMEM: return "workspace too small or allocation failed";
+    case Q8_ERR_CUDA: return "CUDA runtime error (see q8_last_cuda_error)";
+    case Q8_ERR_DEVICE: return "current device is not compute capability 10.3";
+    case Q8_ERR_CAPTURE: return "the call would allocate scratch while its stream is captured";
+  }
+  return "unknown status";
+}
+
+const char* q8_last_cuda_error(void) { return g_last_cuda_error; }
+
+void q8_release(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int cur = -1;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_ws) {
+    if (kv.second.ptr != nullptr) {
+      cudaSetDevice(kv.first.first);
+      cudaFree(kv.second.ptr);
+    }
+  }
+  g_ws.clear();
+  if (cur >= 0) cudaSetDevice(cur);
+}
+
+const char* q8_version(void) { return "0.1.0"; }
+
+}  // extern "C"

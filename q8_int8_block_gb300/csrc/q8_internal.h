@@ -1,0 +1,50 @@
+// q8_internal.h -- launchers shared between the translation units of libq8 (not part of
+// the public ABI; include/q8.h is).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace q8 {
+
+constexpr int kQK = 32;  // elements per Q8_0 block
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int max_smem_optin = 0;
+  uint32_t* err_word = nullptr;  // device address of the library's error word
+};
+
+// ---- q8_quant.cu ------------------------------------------------------------------
+// Quantizes `rows` rows of K values (xtype 0 = f32, 1 = bf16 bits) into codes and scales.
+//   codes_f16 == false: int8 codes;  true: binary16 codes (exact small integers).
+//   scale_f16 == false: binary32 scales;  true: binary16 scale bits.
+cudaError_t launch_quantize(const void* x, int xtype, void* codes, bool codes_f16, void* scales,
+                            bool scale_f16, int64_t rows, int64_t K, const DeviceInfo& dev,
+                            cudaStream_t stream);
+
+// int8 codes -> binary16 codes (n a multiple of 16).
+cudaError_t launch_codes_to_f16(const int8_t* q, uint16_t* out, int64_t n, const DeviceInfo& dev,
+                                cudaStream_t stream);
+
+// ---- q8_decode.cu -----------------------------------------------------------------
+// Largest M the decode kernel takes.
+constexpr int kDecodeMaxM = 8;
+// Shared memory the decode kernel needs for M tokens of K (0 if it cannot run).
+size_t decode_smem_bytes(int64_t M, int64_t K, const DeviceInfo& dev);
+// y = linear(x) (fused activation quantization) or, when isum != nullptr, the raw
+// block sums of given codes xq (x ignored; xd ignored).
+cudaError_t launch_decode(const void* x, int xtype, const int8_t* xq_in, const int8_t* Wq,
+                          const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
+                          int64_t K, const DeviceInfo& dev, cudaStream_t stream);
+
+// ---- q8_gemm.cu -------------------------------------------------------------------
+// Tensor-core GEMM on binary16 codes: A16 [M,K] activation codes, B16 [N,K] weight codes,
+// xd [M,K/32] f32, Wd [N,K/32] binary16 bits.  Writes y [M,N] (rescaled sum) or, when
+// isum != nullptr, the raw block sums isum [M,N,K/32].
+cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float* xd,
+                           const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
+                           int64_t K, const DeviceInfo& dev, cudaStream_t stream);
+
+}  // namespace q8
