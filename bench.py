@@ -194,29 +194,55 @@ def l2_bytes(torch):
         return 129 * 1024 * 1024
 
 
-def time_graph_steps(torch, step_fns, steps, warmup):
+# Named workloads: (workload, projection index, M index) of workloads.WORKLOADS.
+CASES = {
+    "decode_m1": ("decode", 0, 0), "decode_m4": ("decode", 0, 1), "decode_m16": ("decode", 0, 2),
+    "decode_m64": ("decode", 0, 3), "tiny": ("tiny", 0, 0),
+    "prefill9b_up": ("prefill9b", 0, 0), "prefill9b_down": ("prefill9b", 1, 0),
+    "prefill27b_up": ("prefill27b", 0, 0), "prefill27b_down": ("prefill27b", 1, 0),
+}
+TRAFFIC_PROFILES = {  # committed ncu summaries that record DRAM bytes per launch
+    "decode_m1": ("decode_kernel_m1_k4096_n12288.md", ["q8_decode.cu", "q8_ptx.cuh", "q8_quant_dev.cuh"]),
+    "prefill9b_up": ("gemm_tc_kernel_m2048_k4096_n12288.md", ["q8_gemm.cu", "q8_ptx.cuh"]),
+}
+
+
+def time_graph_steps(torch, q8, step_fns, steps, warmup, instrument=True):
     """Captures one CUDA graph holding len(step_fns) steps, runs `warmup` steps, then times
-    exactly `steps` steps (whole replays, plus a prefix replay of a partial graph).
-    Returns (total seconds, seconds per step) measured with CUDA events."""
+    exactly `steps` steps: whole replays plus a replay of a graph holding the remainder.
+    Returns (seconds for the timed steps, mean seconds of the main kernel), all from CUDA
+    events on the launching stream.  With `instrument`, the library records event nodes
+    around each step's main kernel and the mean is over the last len(step_fns) launches;
+    without it (one kernel per step, consecutive launches overlapping through programmatic
+    dependent launch, which event nodes between them would serialize), the main kernel's
+    time per launch is the timed region's time per step."""
     R = len(step_fns)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(R)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(R)]
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        for f in step_fns:  # eager once (allocations, attributes) before capture
+        for f in step_fns:  # eager once (function attributes, workspace) before capture
             f()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    full = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(full):
-        for f in step_fns:
-            f()
-    rem = steps % R
-    part = None
-    if rem:
-        part = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(part):
-            for f in step_fns[:rem]:
+    if instrument:
+        q8.q8_set_timing_events(starts, stops)
+    try:
+        full = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(full):
+            for f in step_fns:
                 f()
+        rem = steps % R
+        part = None
+        if rem and instrument:
+            q8.q8_set_timing_events(starts, stops)
+            part = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(part):
+                for f in step_fns[:rem]:
+                    f()
+    finally:
+        q8.q8_set_timing_events()
     for _ in range((warmup + R - 1) // R):
         full.replay()
     torch.cuda.synchronize()
@@ -233,7 +259,126 @@ def time_graph_steps(torch, step_fns, steps, warmup):
     torch.cuda.synchronize()
     barrier()
     total = ev0.elapsed_time(ev1) / 1e3
-    return total, total / steps
+    if instrument:
+        kern = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, stops)) / 1e3
+    else:
+        kern = total / steps
+    return total, kern
+
+
+def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=False):
+    wname, p, mi = CASES[name]
+    wl = workloads.WORKLOADS[wname]
+    W = wl.make_weights(p)
+    x_np, _ = wl.make_act(p, mi)
+    M, K = x_np.shape
+    N = W.shape[0]
+    Wq0, Wd0 = q8.q8_quantize_weights(torch.from_numpy(W).to(dev))
+    del W
+    wbytes = N * K + 2 * N * (K // 32)
+    copies = max(2, -(-(2 * l2_bytes(torch)) // wbytes))
+    Wqs = [Wq0] + [Wq0.clone() for _ in range(copies - 1)]
+    Wds = [Wd0] + [Wd0.clone() for _ in range(copies - 1)]
+    xdt = torch.bfloat16 if wl.bf16 else torch.float32
+    xsize = 2 if wl.bf16 else 4
+    if wl.bf16:
+        x = torch.from_numpy(x_np.view(np.int16).copy()).to(dev).view(torch.bfloat16)
+    else:
+        x = torch.from_numpy(x_np).to(dev)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    wsz = q8.q8_linear_workspace_size(M, N, K)
+    ws = torch.empty(max(wsz, 1), dtype=torch.uint8, device=dev) if wsz else None
+    path = "decode" if wsz == 0 else "tensor"
+    fns = [lambda i=i: q8.q8_linear_ex(x, Wqs[i], Wds[i], y=y, workspace=ws) for i in range(copies)]
+    bytes_step = workloads.algorithmic_bytes(M, N, K, x_bytes=xsize)
+    ops_step = workloads.algorithmic_ops(M, N, K)
+    t_hbm = bytes_step / (pk["hbm_gbs"] * 1e9)
+    t_tc = ops_step / (pk["bf16_tflops"] * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    inst = path != "decode"  # multi-kernel steps: time the GEMM itself with event nodes
+    if clocks:
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            total, kern = time_graph_steps(torch, q8, fns, steps, warmup, instrument=inst)
+        clk_summary = clk.summary()
+    else:
+        total, kern = time_graph_steps(torch, q8, fns, steps, warmup, instrument=inst)
+        clk_summary = None
+    t_max = max_over_ranks(total)
+    if bound == "hbm":
+        unit = "GB/s"
+        value = sum_over_ranks(bytes_step * steps) / t_max / 1e9
+        roof = {"bound": "hbm", "achieved": round(bytes_step / kern / 1e9, 2), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(bytes_step / kern / 1e9 / pk["hbm_gbs"], 4),
+                "algorithmic_bytes_per_launch": bytes_step,
+                "peak_source": f"hbm_gbs of the {pk_src} peaks"}
+    else:
+        unit = "TOPS"
+        value = sum_over_ranks(ops_step * steps) / t_max / 1e12
+        roof = {"bound": "tensor", "achieved": round(ops_step / kern / 1e12, 2),
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(ops_step / kern / 1e12 / pk["bf16_tflops"], 4),
+                "algorithmic_flops_per_launch": ops_step,
+                "peak_source": f"bf16_tflops (burst) of the {pk_src} peaks: the kernel runs on "
+                               "the dense kind::f16 tensor pipe (int8 codes as binary16)"}
+    roof["kernel"] = "q8::decode_kernel" if path == "decode" else "q8::gemm_tc_kernel"
+    roof["kernel_us"] = round(kern * 1e6, 3)
+    roof["kernel_time"] = ("time per step of the timed region (one kernel per step; "
+                           "consecutive launches overlap by programmatic dependent launch)"
+                           if not inst else "mean of event-node pairs around the GEMM launches")
+    prof = TRAFFIC_PROFILES.get(name)
+    roof["traffic"] = profiled_traffic(*prof) if prof else None
+    out = {"name": name, "M": M, "K": K, "N": N, "path": path, "unit": unit, "value": value,
+           "t_max": t_max, "roofline": roof, "copies": copies, "wbytes": wbytes,
+           "launches_per_step": 1 if path == "decode" else 3, "clocks": clk_summary,
+           "bytes_step": bytes_step, "xsize": xsize, "bf16": wl.bf16}
+    if e2e:
+        out["e2e"] = e2e_measure(torch, q8, dev, x_np, wl.bf16, Wqs, Wds, M, N, K, steps, warmup,
+                                 bytes_step, ops_step, bound)
+        out["Wq0"], out["Wd0"], out["x_np"] = Wq0, Wd0, x_np
+    return out
+
+
+def e2e_measure(torch, q8, dev, x_np, bf16, Wqs, Wds, M, N, K, steps, warmup, bytes_step, ops_step,
+                bound):
+    """End to end through the public call q8_linear / q8_linear_ex: per step the H2D copy of x
+    from pinned memory, the call, and the D2H copy of y into pinned memory."""
+    copies = len(Wqs)
+    n = max(1, min(steps, 2000 if bound == "hbm" else 50))
+    if bf16:
+        xh = torch.from_numpy(x_np.view(np.int16).copy()).pin_memory()
+        xd = torch.empty((M, K), dtype=torch.int16, device=dev)
+        call = lambda i: q8.q8_linear(xd.view(torch.bfloat16), Wqs[i % copies], Wds[i % copies], y=yd)
+    else:
+        xh = torch.from_numpy(x_np.copy()).pin_memory()
+        xd = torch.empty((M, K), dtype=torch.float32, device=dev)
+        call = lambda i: q8.q8_linear_ex(xd, Wqs[i % copies], Wds[i % copies], y=yd)
+    yh = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    yd = torch.empty((M, N), dtype=torch.float32, device=dev)
+    for i in range(3):
+        xd.copy_(xh, non_blocking=True)
+        call(i)
+        yh.copy_(yd, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t = time.perf_counter()
+    e0.record()
+    for i in range(n):
+        xd.copy_(xh, non_blocking=True)
+        call(i)
+        yh.copy_(yd, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    t = time.perf_counter() - t
+    barrier()
+    t = max_over_ranks(max(t, e0.elapsed_time(e1) / 1e3))
+    if bound == "hbm":
+        v, u = sum_over_ranks(bytes_step * n) / t / 1e9, "GB/s"
+    else:
+        v, u = sum_over_ranks(ops_step * n) / t / 1e12, "TOPS"
+    return {"value": round(v, 3), "unit": u, "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
+            "d2h_bytes_per_step": M * N * 4, "steps": n,
+            "api": "q8_int8_block_gb300.q8_linear (C ABI q8_linear), host-timed"}
 
 
 def gpu_arm(args):
@@ -247,141 +392,49 @@ def gpu_arm(args):
 
     pk, pk_src = peaks()
     dev = torch.device("cuda", local)
-    wl = workloads.WORKLOADS["decode"]
-    pr = wl.projections[0]
-    M, K, N = 1, pr.K, pr.N
-    W = wl.make_weights(0)
-    x_np, _ = wl.make_act(0, 0)  # M = 1
-    Wq0, Wd0 = q8.q8_quantize_weights(torch.from_numpy(W).to(dev))
-    wbytes = N * K + 2 * N * (K // 32)
-    copies = max(2, -(-(2 * l2_bytes(torch) + wbytes) // wbytes))
-    Wqs = [Wq0] + [Wq0.clone() for _ in range(copies - 1)]
-    Wds = [Wd0] + [Wd0.clone() for _ in range(copies - 1)]
-    x = torch.from_numpy(x_np.view(np.int16).copy()).to(dev).view(torch.bfloat16)
-    y = torch.empty((M, N), dtype=torch.float32, device=dev)
-    fns = [lambda i=i: q8.q8_linear(x, Wqs[i], Wds[i], y=y) for i in range(copies)]
-    bytes_step = workloads.algorithmic_bytes(M, N, K)
-
-    with ClockSampler(local) as clk:
-        total, per_step = time_graph_steps(torch, fns, args.steps, args.warmup)
-    clocks = clk.summary()
-    t_max = max_over_ranks(total)
-    value = sum_over_ranks(bytes_step * args.steps) / t_max / 1e9
-    achieved = bytes_step / per_step / 1e9
-    traffic = profiled_traffic("decode_kernel_m1_k4096_n12288.md", ["q8_decode.cu", "q8_ptx.cuh",
-                                                                     "q8_quant_dev.cuh"])
-
-    # end to end through the public API: H2D of x from pinned memory, the call, D2H of y
-    e2e_steps = min(args.steps, 2000)
-    xh = torch.from_numpy(x_np.view(np.int16).copy()).pin_memory()
-    yh = torch.empty((M, N), dtype=torch.float32).pin_memory()
-    xd = torch.empty((M, K), dtype=torch.int16, device=dev)
-    for i in range(max(3, args.warmup // 100)):
-        xd.copy_(xh, non_blocking=True)
-        q8.q8_linear(xd.view(torch.bfloat16), Wqs[i % copies], Wds[i % copies], y=y)
-        yh.copy_(y, non_blocking=True)
-    torch.cuda.synchronize()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_host = time.perf_counter()
-    e0.record()
-    for i in range(e2e_steps):
-        xd.copy_(xh, non_blocking=True)
-        q8.q8_linear(xd.view(torch.bfloat16), Wqs[i % copies], Wds[i % copies], y=y)
-        yh.copy_(y, non_blocking=True)
-    e1.record()
-    torch.cuda.synchronize()
-    t_host = time.perf_counter() - t_host
-    barrier()
-    e2e_t = max_over_ranks(max(e0.elapsed_time(e1) / 1e3, t_host))
-    e2e_value = sum_over_ranks(bytes_step * e2e_steps) / e2e_t / 1e9
-
+    r = run_case(torch, q8, dev, args.workload, args.steps, args.warmup, pk, pk_src, clocks=True,
+                 e2e=True)
     extra = {}
-    if not args.no_extra:
-        extra = extra_measurements(torch, q8, dev, pk, args)
-
+    if not args.no_extra and args.workload == "decode_m1":
+        for name, st in (("decode_m4", 20000), ("decode_m16", 20000), ("decode_m64", 20000),
+                         ("prefill9b_up", 200), ("prefill9b_down", 200)):
+            e = run_case(torch, q8, dev, name, st, max(3, st // 50), pk, pk_src)
+            extra[name] = {"value": round(e["value"], 3), "unit": e["unit"], "path": e["path"],
+                           "us_per_step": round(e["t_max"] / st * 1e6, 3),
+                           "roofline": e["roofline"], "steps": st}
     err = q8.q8_device_error()
+    wname = CASES[args.workload][0]
+    desc = {"decode": "decode GEMV, FFN up-projection of a dense ~9B-class layer",
+            "tiny": "tiny Q8_0 linear (float32 activations)",
+            "prefill9b": "prefill GEMM, 9B-class projection",
+            "prefill27b": "prefill GEMM, 27B-class projection, 1% activation channels x20"}[wname]
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_max / args.steps * 1e3, 6),
+        "metric": METRIC, "value": round(r["value"], 3), "unit": r["unit"], "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(r["t_max"] / args.steps * 1e3, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
-        "data": "synthetic (seeded N(0,0.02) weights quantized to Q8_0, N(0,1) bf16 activations)",
-        "config": {"workload": "decode GEMV, FFN up-projection of a dense ~9B-class layer",
-                   "M": M, "K": K, "N": N, "weights": "Q8_0 (int8 codes + binary16 scale per 32)",
-                   "activations": "bf16, quantized per call inside the kernel",
-                   "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: {copies} rotating weight copies "
-                         f"({copies * wbytes / 1e6:.0f} MB > 2 x L2)",
-                   "timing": "CUDA graph replays, CUDA events"},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                     "traffic": traffic, "kernel": "q8::decode_kernel<1,false,true>",
-                     "algorithmic_bytes_per_launch": bytes_step,
-                     "peak_source": f"hbm_gbs of {pk_src} peaks"},
-        "clocks": clocks,
-        "e2e": {"value": round(e2e_value, 3), "unit": "GB/s",
-                "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 4,
-                "steps": e2e_steps, "api": "q8_int8_block_gb300.q8_linear (C ABI q8_linear)"},
-        "gpu_launches": args.steps,
+        "data": "synthetic (seeded N(0,0.02) weights quantized to Q8_0, N(0,1) activations)",
+        "config": {"workload": f"{desc}: {args.workload}", "M": r["M"], "K": r["K"], "N": r["N"],
+                   "weights": "Q8_0 (int8 codes + binary16 scale per 32 along K)",
+                   "activations": ("bf16" if r["bf16"] else "float32") +
+                                  ", quantized per call inside the library",
+                   "kernel_path": r["path"], "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {r['copies']} rotating weight copies "
+                         f"({r['copies'] * r['wbytes'] / 1e6:.0f} MB > 2 x L2)",
+                   "timing": "CUDA graph replays, CUDA events; main kernel timed by event nodes "
+                             "around each launch"},
+        "roofline": r["roofline"],
+        "clocks": r["clocks"],
+        "e2e": r["e2e"],
+        "gpu_launches": args.steps * r["launches_per_step"],
         "device_error_word": err,
     }
     if extra:
         line["extra"] = extra
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(Wq0, Wd0, x_np, M, N, K, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(r["Wq0"], r["Wd0"], r["x_np"], r["bf16"], r["M"], r["N"],
+                                            r["K"], r["xsize"], args.cpu_seconds)
     return rank, line
-
-
-def extra_measurements(torch, q8, dev, pk, args):
-    """Secondary lines: batched decode and the prefill GEMM (not part of the headline)."""
-    out = {}
-    # batched decode, same weights, M = 4, 16, 64
-    wl = workloads.WORKLOADS["decode"]
-    pr = wl.projections[0]
-    W = wl.make_weights(0)
-    Wq, Wd = q8.q8_quantize_weights(torch.from_numpy(W).to(dev))
-    K, N = pr.K, pr.N
-    wbytes = N * K + 2 * N * (K // 32)
-    copies = max(2, -(-(2 * l2_bytes(torch) + wbytes) // wbytes))
-    Wqs = [Wq] + [Wq.clone() for _ in range(copies - 1)]
-    Wds = [Wd] + [Wd.clone() for _ in range(copies - 1)]
-    for mi, M in enumerate(wl.Ms):
-        if M == 1:
-            continue
-        x_np, _ = wl.make_act(0, mi)
-        x = torch.from_numpy(x_np.view(np.int16).copy()).to(dev).view(torch.bfloat16)
-        y = torch.empty((M, N), dtype=torch.float32, device=dev)
-        fns = [lambda i=i: q8.q8_linear(x, Wqs[i], Wds[i], y=y) for i in range(copies)]
-        steps = 2000
-        _, per = time_graph_steps(torch, fns, steps, 60)
-        b = workloads.algorithmic_bytes(M, N, K)
-        ops = workloads.algorithmic_ops(M, N, K)
-        out[f"decode_M{M}"] = {"GB/s": round(b / per / 1e9, 2), "TOPS": round(ops / per / 1e12, 3),
-                               "us_per_step": round(per * 1e6, 3),
-                               "hbm_frac": round(b / per / 1e9 / pk["hbm_gbs"], 4)}
-    del Wqs, Wds
-    # prefill: 9B-class up and down projections, M = 2048
-    wl = workloads.WORKLOADS["prefill9b"]
-    for p, pr in enumerate(wl.projections):
-        W = wl.make_weights(p)
-        Wq, Wd = q8.q8_quantize_weights(torch.from_numpy(W).to(dev))
-        x_np, _ = wl.make_act(p, 0)
-        M = x_np.shape[0]
-        x = torch.from_numpy(x_np.view(np.int16).copy()).to(dev).view(torch.bfloat16)
-        y = torch.empty((M, pr.N), dtype=torch.float32, device=dev)
-        fns = [lambda: q8.q8_linear(x, Wq, Wd, y=y)]
-        steps = 50
-        _, per = time_graph_steps(torch, fns, steps, 5)
-        ops = workloads.algorithmic_ops(M, pr.N, pr.K)
-        tops = ops / per / 1e12
-        out[f"prefill9b_{pr.name}_M{M}"] = {
-            "TOPS": round(tops, 2), "us_per_step": round(per * 1e6, 2),
-            "K": pr.K, "N": pr.N,
-            "tensor_frac_of_f16_peak": round(tops / pk["bf16_tflops"], 4),
-            "note": "int8-equivalent ops 2MNK on the kind::f16 pipe (binary16 codes); peak = "
-                    "dense bf16/f16 burst rate; per step = activation quantize + weight code "
-                    "widening + GEMM"}
-    return out
 
 
 # ----------------------------------------------------------------------------------- #
@@ -392,23 +445,31 @@ def _oracle_cores():
     return os.cpu_count() or 1
 
 
-def cpu_baseline(Wq_t, Wd_t, x_np, M, N, K, seconds):
+def cpu_baseline(Wq_t, Wd_t, x_np, bf16, M, N, K, xsize, seconds):
     from oracle import oracle as O
     Wq = Wq_t.cpu().numpy()
     Wd = Wd_t.cpu().numpy().view(np.uint16)
     cores = _oracle_cores()
-    O.linear(x_np, Wq, Wd, bf16=True, nthreads=cores)  # warm
+    rows = N
+    t0 = time.perf_counter()
+    O.linear(x_np, Wq, Wd, bf16=bf16, nthreads=cores)
+    t_full = time.perf_counter() - t0
+    if t_full > seconds:  # large layers: a contiguous slice of the output rows
+        rows = max(64, int(N * seconds / t_full / 2))
     passes, t0 = 0, time.perf_counter()
     while True:
-        O.linear(x_np, Wq, Wd, bf16=True, nthreads=cores)
+        O.linear(x_np, Wq[:rows], Wd[:rows], bf16=bf16, nthreads=cores)
         passes += 1
         dt = time.perf_counter() - t0
         if dt >= seconds or passes >= 100000:
             break
-    b = workloads.algorithmic_bytes(M, N, K) * passes
-    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{passes} full passes of the M={M} K={K} N={N} layer (activation "
-                      f"quantization + all {N} outputs) in {dt:.1f} s"}
+    b = workloads.algorithmic_bytes(M, rows, K, x_bytes=xsize) * passes
+    ops = workloads.algorithmic_ops(M, rows, K) * passes
+    tensor = workloads.algorithmic_ops(M, N, K) / 1.9e15 > workloads.algorithmic_bytes(M, N, K) / 6.8e12
+    val, unit = (ops / dt / 1e12, "TOPS") if tensor else (b / dt / 1e9, "GB/s")
+    return {"value": round(val, 6), "unit": unit, "cores": cores, "kind": "oracle",
+            "sample": f"{passes} passes of the M={M} K={K} layer over {rows} of {N} output rows "
+                      f"(activation quantization + those outputs) in {dt:.1f} s"}
 
 
 def reference_arm(args):
@@ -416,43 +477,48 @@ def reference_arm(args):
     if rank != 0:
         return 0, None  # the oracle is timed once, on rank 0
     from oracle import oracle as O
-    wl = workloads.WORKLOADS["decode"]
-    pr = wl.projections[0]
-    M, K, N = 1, pr.K, pr.N
-    W = wl.make_weights(0)
-    x_np, _ = wl.make_act(0, 0)
+    wname, p, mi = CASES[args.workload]
+    wl = workloads.WORKLOADS[wname]
+    W = wl.make_weights(p)
+    x_np, _ = wl.make_act(p, mi)
+    M, K = x_np.shape
+    N = W.shape[0]
+    xsize = 2 if wl.bf16 else 4
     Wq, Wd = O.quantize_weights(W)
+    del W
     cores = _oracle_cores()
+    # time a slice first, to size each step so that all steps fit in about a minute
+    probe = min(N, 256)
     t0 = time.perf_counter()
-    O.linear(x_np, Wq, Wd, bf16=True, nthreads=cores)
-    t_full = time.perf_counter() - t0
-    # each step: the layer on a contiguous slice of output rows, sized so that all steps
-    # fit in about a minute
+    O.linear(x_np, Wq[:probe], Wd[:probe], bf16=wl.bf16, nthreads=cores)
+    t_row = (time.perf_counter() - t0) / probe
     budget = 60.0
-    rows = int(max(64, min(N, N * budget / max(1, args.steps + args.warmup) / max(t_full, 1e-6))))
+    rows = int(max(16, min(N, budget / max(1, args.steps + args.warmup) / max(t_row, 1e-9))))
     starts = [(i * rows) % (N - rows + 1) for i in range(args.steps + args.warmup)]
     for i in range(args.warmup):
         s = starts[i]
-        O.linear(x_np, Wq[s:s + rows], Wd[s:s + rows], bf16=True, nthreads=cores)
+        O.linear(x_np, Wq[s:s + rows], Wd[s:s + rows], bf16=wl.bf16, nthreads=cores)
     t0 = time.perf_counter()
     for i in range(args.warmup, args.warmup + args.steps):
         s = starts[i]
-        O.linear(x_np, Wq[s:s + rows], Wd[s:s + rows], bf16=True, nthreads=cores)
+        O.linear(x_np, Wq[s:s + rows], Wd[s:s + rows], bf16=wl.bf16, nthreads=cores)
     dt = time.perf_counter() - t0
-    b = workloads.algorithmic_bytes(M, rows, K) * args.steps
-    value = b / dt / 1e9
+    b = workloads.algorithmic_bytes(M, rows, K, x_bytes=xsize) * args.steps
+    ops = workloads.algorithmic_ops(M, rows, K) * args.steps
+    tensor = workloads.algorithmic_ops(M, N, K) / 1.9e15 > workloads.algorithmic_bytes(M, N, K) / 6.8e12
+    value, unit = (ops / dt / 1e12, "TOPS") if tensor else (b / dt / 1e9, "GB/s")
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8",
-        "data": "synthetic (seeded N(0,0.02) weights quantized to Q8_0, N(0,1) bf16 activations)",
-        "config": {"workload": "decode GEMV, FFN up-projection of a dense ~9B-class layer",
-                   "M": M, "K": K, "N": N, "parallelism": "CPU oracle, rank 0 only"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"each step: {rows} of {N} output rows (activation quantization + "
-                                   f"those rows), rotating over the matrix"},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+        "data": "synthetic (seeded N(0,0.02) weights quantized to Q8_0, N(0,1) activations)",
+        "config": {"workload": f"{args.workload}", "M": M, "K": K, "N": N,
+                   "parallelism": "CPU oracle, rank 0 only"},
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: the layer over {rows} of {N} output rows "
+                                   f"(activation quantization + those outputs), rotating over W"},
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     return rank, line
@@ -464,6 +530,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100000)
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", choices=sorted(CASES), default="decode_m1",
+                    help="which configured shape to time (default: decode GEMV, M=1)")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -127,6 +127,19 @@ q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64
  */
 uint32_t q8_device_error(q8_status* status);
 
+/*
+ * q8_set_timing_events -- timing hook for benchmarks.  With count > 0, each later
+ * q8_linear / q8_linear_ex call records starts[i] on its stream right before the launch
+ * of its main kernel (the decode kernel, or the tensor-core GEMM) and stops[i] right after
+ * it, i = 0, 1, ..., count-1, count, ... taken modulo count (i restarts at 0 on every call
+ * of this function).  Under stream capture the records become graph event nodes
+ * (cudaEventRecordExternal).  The arrays are copied; the events must outlive their use.
+ * count == 0 (or NULL arrays) switches the hook off.  Process-wide; calls that race with
+ * this one may or may not see the change.  Returns Q8_ERR_NULL if count > 0 and an array
+ * is NULL.
+ */
+q8_status q8_set_timing_events(cudaEvent_t* starts, cudaEvent_t* stops, int count);
+
 /* Human-readable text of a status code (static storage). */
 const char* q8_status_string(q8_status status);
 

@@ -19,6 +19,7 @@ import torch
 
 __all__ = ["Q8Error", "q8_quantize_weights", "q8_quantize_act", "q8_linear", "q8_linear_ex",
            "q8_linear_workspace_size", "q8_block_sums", "q8_device_error", "q8_release",
+           "q8_set_timing_events",
            "q8_version", "lib_path", "QK", "PATHS"]
 
 QK = 32
@@ -57,6 +58,8 @@ def _load():
         f = getattr(L, name)
         f.argtypes = args
         f.restype = i32
+    L.q8_set_timing_events.argtypes = [p, p, i32]
+    L.q8_set_timing_events.restype = i32
     L.q8_linear_workspace_size.argtypes = [i64, i64, i64, i32]
     L.q8_linear_workspace_size.restype = sz
     L.q8_device_error.argtypes = [ctypes.POINTER(i32)]
@@ -200,6 +203,23 @@ def q8_device_error() -> int:
     word = _L.q8_device_error(ctypes.byref(st))
     _check(st.value, "q8_device_error")
     return int(word)
+
+
+def q8_set_timing_events(starts=None, stops=None):
+    """Timing hook: events (torch.cuda.Event(enable_timing=True)) recorded around the main
+    kernel of each later q8_linear / q8_linear_ex call, cycling through the list; under
+    graph capture they become event nodes.  No arguments: switch off."""
+    if not starts:
+        _check(_L.q8_set_timing_events(None, None, 0), "q8_set_timing_events")
+        return
+    assert len(starts) == len(stops)
+    for e in list(starts) + list(stops):  # make sure the CUDA events exist
+        if e.cuda_event == 0:
+            e.record()
+    arr = ctypes.c_void_p * len(starts)
+    a = arr(*[e.cuda_event for e in starts])
+    b = arr(*[e.cuda_event for e in stops])
+    _check(_L.q8_set_timing_events(a, b, len(starts)), "q8_set_timing_events")
 
 
 def q8_release():

@@ -8,6 +8,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "../../include/q8.h"
 #include "q8_internal.h"
@@ -136,6 +137,41 @@ q8_status library_workspace(const DeviceInfo& dev, cudaStream_t stream, size_t b
 
 q8_status launch_status(cudaError_t e) { return e == cudaSuccess ? Q8_OK : cuda_fail(e); }
 
+// ---- timing hook (q8_set_timing_events) ----------------------------------------------
+std::mutex g_timing_mu;
+std::vector<cudaEvent_t> g_t_start, g_t_stop;
+size_t g_t_next = 0;
+
+// Picks the event pair for the next main-kernel launch (false if the hook is off).
+bool timing_pair(cudaEvent_t* a, cudaEvent_t* b) {
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  if (g_t_start.empty()) return false;
+  const size_t i = g_t_next++ % g_t_start.size();
+  *a = g_t_start[i];
+  *b = g_t_stop[i];
+  return true;
+}
+
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t stream) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return e;
+  if (cap == cudaStreamCaptureStatusActive)
+    return cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal);
+  return cudaEventRecord(ev, stream);
+}
+
+// Runs `launch` (the main kernel of a call) between the hook's events, if the hook is on.
+template <typename F>
+cudaError_t timed_launch(cudaStream_t stream, F&& launch) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  const bool on = timing_pair(&a, &b);
+  cudaError_t e = on ? record_event(a, stream) : cudaSuccess;
+  if (e == cudaSuccess) e = launch();
+  if (e == cudaSuccess && on) e = record_event(b, stream);
+  return e;
+}
+
 q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uint16_t* Wd,
                       float* y, int64_t M, int64_t N, int64_t K, q8_path path, void* ws,
                       size_t ws_bytes, bool library_ws, cudaStream_t stream) {
@@ -155,8 +191,10 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
   if (M == 0 || N == 0) return Q8_OK;
   if (K == 0) return launch_status(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 4, stream));
   if (p == Q8_PATH_DECODE)
-    return launch_status(launch_decode(x, static_cast<int>(xtype), nullptr, Wq, Wd, y, nullptr, M,
-                                       N, K, dev, stream));
+    return launch_status(timed_launch(stream, [&] {
+      return launch_decode(x, static_cast<int>(xtype), nullptr, Wq, Wd, y, nullptr, M, N, K, dev,
+                           stream);
+    }));
   const size_t need = tensor_ws_bytes(M, N, K);
   if (library_ws) {
     if ((st = library_workspace(dev, stream, need, &ws)) != Q8_OK) return st;
@@ -172,7 +210,10 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
                                               align256(static_cast<size_t>(M) * (K / kQK) * 4));
   cudaError_t e = launch_quantize(x, static_cast<int>(xtype), A16, true, xd, false, M, K, dev, stream);
   if (e == cudaSuccess) e = launch_codes_to_f16(Wq, B16, N * K, dev, stream);
-  if (e == cudaSuccess) e = launch_gemm_tc(A16, B16, xd, Wd, y, nullptr, M, N, K, dev, stream);
+  if (e == cudaSuccess)
+    e = timed_launch(stream, [&] {
+      return launch_gemm_tc(A16, B16, xd, Wd, y, nullptr, M, N, K, dev, stream);
+    });
   return launch_status(e);
 }
 
@@ -293,6 +334,18 @@ const char* q8_status_string(q8_status s) {
 }
 
 const char* q8_last_cuda_error(void) { return g_last_cuda_error; }
+
+q8_status q8_set_timing_events(cudaEvent_t* starts, cudaEvent_t* stops, int count) {
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  g_t_start.clear();
+  g_t_stop.clear();
+  g_t_next = 0;
+  if (count <= 0) return Q8_OK;
+  if (starts == nullptr || stops == nullptr) return Q8_ERR_NULL;
+  g_t_start.assign(starts, starts + count);
+  g_t_stop.assign(stops, stops + count);
+  return Q8_OK;
+}
 
 void q8_release(void) {
   std::lock_guard<std::mutex> lock(g_mu);

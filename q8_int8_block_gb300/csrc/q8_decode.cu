@@ -6,21 +6,27 @@
 // (CMP 100-210)" (news.hada.io topic 29953, list of un-throttled paths: the DP4A int8
 // GEMM), at decode batch sizes (M <= 8), where the layer is bound by reading the weights.
 //
-// Design (one CTA per SM, persistent):
-//   * CTA c owns the contiguous rows [r0, r1) of W; their codes form one contiguous byte
-//     range, streamed row by row through a ring of shared-memory stages with bulk async
-//     copies (one elected producer thread, one mbarrier per stage).  A row's binary16
-//     scales ride in the same stage when the row of scales is 16-byte sized (K % 256 == 0),
-//     else they are read from global memory.
-//   * While the first rows are in flight, the consumer warps quantize the M activation
-//     rows into shared memory (fused activation quantizer: the same device function as
-//     the standalone quantizer, so codes and scales are identical).
-//   * Each consumer warp takes whole rows: lane l handles the 16-byte pieces l, l+32, ...
-//     of the row, 4 dp4a per piece and token; an xor-shuffle joins the two halves of each
-//     32-element block into the exact int32 block sum, the even lane rescales it by
-//     Wd*xd in binary32, and a warp reduction finishes the row.
-//   * Block-sum mode (for checking) takes int8 codes instead of x and writes the raw
-//     block sums instead of y.
+// Design (one CTA per SM, 1 producer warp + 16 consumer warps):
+//   * CTA c owns the contiguous rows [r0, r1) of W.  Their codes (and, when a row of scales
+//     is a multiple of 16 bytes, their binary16 scales) are contiguous, and stream through a
+//     ring of shared-memory stages of R whole rows (about 16 KB) by bulk asynchronous copies
+//     that one elected thread issues; each stage completes on its own mbarrier.  Copies of
+//     16 KB keep the per-copy overhead of the copy engine small.
+//   * Programmatic dependent launch: the kernel lets the next kernel in the stream start as
+//     soon as it begins, and its producer fills the ring before anything waits for the
+//     previous kernel.  Only the consumers wait (griddepcontrol.wait) before they read x and
+//     write y.  So the weights, which are read before that wait, must not be written by a
+//     kernel that triggers its dependents early (no kernel of this library does).  A CTA is
+//     small enough that the next kernel's CTA can be resident on the same SM and prefetch
+//     its first stages while this one finishes.
+//   * Fused activation quantizer: after the wait, the consumers quantize the M activation
+//     rows into shared memory with the same device function as the standalone quantizer.
+//   * Consumer warp w takes rows w, w + 16, ...: lane l handles the 16-byte pieces
+//     l + 32 i of the row, 4 dp4a per piece and token; an xor-shuffle joins the two halves
+//     of each 32-element block into the exact int32 block sum; the even lane rescales it by
+//     Wd * xd in binary32; a warp reduction finishes the row.
+//   * Block-sum mode (for checking) takes int8 codes instead of x and writes the raw block
+//     sums instead of y.
 #include <cuda_fp16.h>
 
 #include "q8_internal.h"
@@ -30,9 +36,12 @@
 namespace q8 {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxStages = 32;
+constexpr int kStageTarget = 16 * 1024;  // bytes of codes per stage (whole rows)
+constexpr int kRingTarget = 96 * 1024;   // bytes of codes and scales in flight per CTA
+constexpr int kXRegPieces = 8;           // one token with K <= 4096: codes in registers
 
 struct DecodeParams {
   const void* x;       // [M,K] bf16 bits or f32 (fused quantization)
@@ -43,78 +52,95 @@ struct DecodeParams {
   float* y;            // [M,N]
   int32_t* isum;       // [M,N,K/32] (block-sum mode)
   int M, N, K;
-  int stages;
+  int rows_per_stage;  // R
+  int stages;          // S
   uint32_t* err;
 };
 
-__device__ __forceinline__ int4 lds128(const void* p) {
-  return *reinterpret_cast<const int4*>(p);
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-template <int MT, bool kBlockSums, bool kScalesInStage>
+__device__ __forceinline__ int4 lds128(const void* p) { return *reinterpret_cast<const int4*>(p); }
+
+// kXP > 0: one token, K <= 512 * kXP; each lane always covers the same K positions, so it
+// keeps its activation codes and scales in registers instead of reading shared memory.
+template <int MT, bool kBlockSums, bool kScalesInStage, int kXP>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+  pdl_launch_dependents();
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full_bar[kMaxStages];
   __shared__ uint64_t empty_bar[kMaxStages];
   __shared__ int abort_flag;
+  // Stages issued so far.  A consumer waits for its stage's ticket before the parity wait
+  // on the stage's barrier: once stage st is issued, the barrier of its slot has finished
+  // every phase before st's, so the parity names st's phase exactly, whatever the number
+  // of stages and consumers.
+  __shared__ volatile int issued;
 
-  const int K = p.K, N = p.N, M = p.M;
+  const int K = p.K, N = p.N, M = p.M, R = p.rows_per_stage, S = p.stages;
   const int nb = K / kQK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * N / gridDim.x;
   const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * N / gridDim.x;
   const int nrows = static_cast<int>(r1 - r0);
-  const int S = p.stages;
-
-  // shared memory carve-up: [x codes MT*K][x scales MT*nb f32][stages]
+  const int nstages = (nrows + R - 1) / R;
+  const uint32_t code_bytes = static_cast<uint32_t>(R) * K;
+  const uint32_t scale_bytes = kScalesInStage ? static_cast<uint32_t>(R) * nb * 2 : 0u;
+  const uint32_t stage_bytes = code_bytes + scale_bytes;
+  // carve-up: [x codes MT*K][x scales MT*nb f32][ring S*stage_bytes]
   int8_t* xs = reinterpret_cast<int8_t*>(smem);
   float* xds = reinterpret_cast<float*>(smem + MT * K);
-  const uint32_t scale_bytes = kScalesInStage ? static_cast<uint32_t>(nb * 2) : 0u;
-  const uint32_t stage_bytes = static_cast<uint32_t>(K) + scale_bytes;
   uint8_t* ring = smem + ((MT * K + MT * nb * 4 + 127) & ~127);
 
+  if (S > kMaxStages || S < 2) {  // the launcher never does this
+    if (threadIdx.x == 0) report_error(p.err, kErrBadLaunch, nullptr);
+    return;
+  }
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    issued = 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], static_cast<uint32_t>(R));
     }
     fence_barrier_init();
   }
   __syncthreads();
 
   if (warp == 0) {
-    // ---------------- producer: one thread streams the rows through the ring ----------
+    // ---------------- producer: weights only, so it does not wait for the previous kernel
     if (lane == 0) {
-      int issued = 0;
-      for (int j = 0; j < nrows; ++j) {
-        const int s = j % S;
-        if (!mbar_wait(&empty_bar[s], ((j / S) & 1) ^ 1, &abort_flag)) {
+      for (int st = 0; st < nstages; ++st) {
+        const int s = st % S;
+        if (!mbar_wait(&empty_bar[s], ((st / S) & 1) ^ 1, &abort_flag)) {
           report_error(p.err, kErrWaitTimeout, &abort_flag);
           break;
         }
-        uint8_t* st = ring + static_cast<size_t>(s) * stage_bytes;
-        mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
-        bulk_load(st, p.Wq + (r0 + j) * static_cast<int64_t>(K), static_cast<uint32_t>(K),
-                  &full_bar[s]);
+        const int64_t ra = r0 + static_cast<int64_t>(st) * R;
+        const int rows = static_cast<int>((r1 - ra) < R ? (r1 - ra) : R);
+        uint8_t* dst = ring + static_cast<size_t>(s) * stage_bytes;
+        mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(rows) * (K + (kScalesInStage ? nb * 2 : 0)));
+        bulk_load(dst, p.Wq + ra * K, static_cast<uint32_t>(rows) * K, &full_bar[s]);
         if constexpr (kScalesInStage)
-          bulk_load(st + K, p.Wd + (r0 + j) * static_cast<int64_t>(nb), scale_bytes,
-                    &full_bar[s]);
-        ++issued;
+          bulk_load(dst + code_bytes, p.Wd + ra * nb, static_cast<uint32_t>(rows) * nb * 2, &full_bar[s]);
+        issued = st + 1;
       }
-      // Never leave with copies in flight: wait for the last stages issued.
-      for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
-        if (!mbar_wait(&full_bar[j % S], (j / S) & 1, nullptr)) {
+      // never leave with copies in flight
+      const int n_issued = issued;
+      for (int st = (n_issued > S ? n_issued - S : 0); st < n_issued; ++st)
+        if (!mbar_wait(&full_bar[st % S], (st / S) & 1, nullptr)) {
           report_error(p.err, kErrWaitTimeout, nullptr);
           break;
         }
     }
   } else {
-    // ---------------- consumers ----------------------------------------------------------
-    const int cw = warp - 1;                   // consumer warp index
-    const int ct = threadIdx.x - 32;           // consumer thread index
-    constexpr int kCT = 32 * kConsumerWarps;   // consumer threads
-    // 1) activation codes and scales into shared memory
+    // ---------------- consumers ---------------------------------------------------------
+    const int cw = warp - 1;
+    const int ct = threadIdx.x - 32;
+    constexpr int kCT = 32 * kConsumerWarps;
+    pdl_wait();  // x, y: wait for the previous kernel in the stream
     if constexpr (kBlockSums) {
       const int n16 = M * K / 16;
       for (int i = ct; i < n16; i += kCT)
@@ -123,16 +149,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       const int nblk = M * nb;
       const int sub = lane & 3;
       const unsigned gmask = 0xFu << (lane & ~3);
-      // every group of 4 lanes of every warp runs the same number of iterations
       const int iters = (nblk + kCT / 4 - 1) / (kCT / 4);
       for (int it = 0; it < iters; ++it) {
         const int blk = it * (kCT / 4) + (ct >> 2);
-        if (blk < nblk) {
+        if (blk < nblk) {  // the 4 lanes of a group agree on this
           float v[8];
           const int64_t off = static_cast<int64_t>(blk) * kQK + sub * 8;
           if (p.xtype == 1) {
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + off),
-                          v);
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + off), v);
           } else {
             const float4* f = reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + off);
             const float4 a = f[0], b = f[1];
@@ -148,34 +172,78 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory");
 
-    // 2) rows
-    const int npieces = K >> 4;  // 16-byte pieces per row (even, since K % 32 == 0)
+    const int npieces = K >> 4;  // even, since K % 32 == 0
     const int iters = (npieces + 31) >> 5;
+    int4 xr[kXP > 0 ? kXP : 1];
+    float xdr[kXP > 0 ? kXP : 1];
+    if constexpr (kXP > 0) {
+#pragma unroll
+      for (int i = 0; i < kXP; ++i) {
+        const int pc = lane + 32 * i;
+        xr[i] = pc < npieces ? lds128(xs + 16 * pc) : make_int4(0, 0, 0, 0);
+        xdr[i] = pc < npieces ? xds[pc >> 1] : 0.0f;
+      }
+    }
     for (int j = cw; j < nrows; j += kConsumerWarps) {
-      const int s = j % S;
+      const int st = j / R;
+      const int s = st % S;
+      bool ticket = issued > st;
+      if (!ticket) {
+        const long long t0 = clock64();
+        while (!(ticket = issued > st) && !*reinterpret_cast<volatile int*>(&abort_flag) &&
+               clock64() - t0 < kWaitBudgetCycles)
+          __nanosleep(64);
+      }
       // every lane waits (and so observes the copied bytes); the warp leaves together
-      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&full_bar[s], (j / S) & 1, &abort_flag));
+      const bool ok =
+          __all_sync(0xFFFFFFFFu, ticket && mbar_wait(&full_bar[s], (st / S) & 1, &abort_flag));
       if (!ok) {
         if (lane == 0) report_error(p.err, kErrWaitTimeout, &abort_flag);
         break;
       }
-      const uint8_t* st = ring + static_cast<size_t>(s) * stage_bytes;
-      const uint16_t* wd_row = kScalesInStage
-                                   ? reinterpret_cast<const uint16_t*>(st + K)
-                                   : p.Wd + (r0 + j) * static_cast<int64_t>(nb);
+      const uint8_t* stage = ring + static_cast<size_t>(s) * stage_bytes;
+      const int jr = j - st * R;  // row within the stage
+      const uint8_t* wrow = stage + static_cast<size_t>(jr) * K;
       const int64_t n = r0 + j;
+      const uint16_t* wd_row = kScalesInStage
+                                   ? reinterpret_cast<const uint16_t*>(stage + code_bytes) + jr * nb
+                                   : p.Wd + n * nb;
       float acc[MT];
 #pragma unroll
       for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
-#pragma unroll 2
+      if constexpr (kXP > 0) {
+#pragma unroll
+        for (int i = 0; i < kXP; ++i) {
+          const int pc = lane + 32 * i;
+          const bool valid = pc < npieces;  // the same on both lanes of a block
+          int4 w = make_int4(0, 0, 0, 0);
+          float dw = 0.0f;
+          if (valid) {
+            w = lds128(wrow + 16 * pc);
+            if constexpr (!kBlockSums) dw = __half2float(__ushort_as_half(wd_row[pc >> 1]));
+          }
+          int sum = __dp4a(w.x, xr[i].x, 0);
+          sum = __dp4a(w.y, xr[i].y, sum);
+          sum = __dp4a(w.z, xr[i].z, sum);
+          sum = __dp4a(w.w, xr[i].w, sum);
+          sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);  // exact int32 block sum
+          if (valid && !(lane & 1)) {
+            if constexpr (kBlockSums)
+              p.isum[n * nb + (pc >> 1)] = sum;
+            else
+              acc[0] = fmaf(dw * xdr[i], static_cast<float>(sum), acc[0]);
+          }
+        }
+      } else
+#pragma unroll 4
       for (int i = 0; i < iters; ++i) {
         const int pc = lane + (i << 5);
-        const bool valid = pc < npieces;
+        const bool valid = pc < npieces;  // the same on both lanes of a block
         const int blk = pc >> 1;
         int4 w = make_int4(0, 0, 0, 0);
         float dw = 0.0f;
         if (valid) {
-          w = lds128(st + 16 * pc);
+          w = lds128(wrow + 16 * pc);
           if constexpr (!kBlockSums) dw = __half2float(__ushort_as_half(wd_row[blk]));
         }
 #pragma unroll
@@ -189,15 +257,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
             sum = __dp4a(w.w, xv.w, sum);
           }
           sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);  // exact int32 block sum
-          if constexpr (kBlockSums) {
-            if (t < M && valid && !(lane & 1))
+          if (t < M && valid && !(lane & 1)) {
+            if constexpr (kBlockSums)
               p.isum[(static_cast<int64_t>(t) * N + n) * nb + blk] = sum;
-          } else {
-            if (t < M && valid && !(lane & 1))
+            else
               acc[t] = fmaf(dw * xds[t * nb + blk], static_cast<float>(sum), acc[t]);
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);  // the row's bytes are no longer needed
       if constexpr (!kBlockSums) {
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
@@ -207,67 +276,88 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           if (lane == 0 && t < M) p.y[static_cast<int64_t>(t) * N + n] = a;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
   }
   __syncthreads();
 }
 
-template <int MT, bool kBS, bool kSc>
+struct Plan {
+  int R = 0, S = 0;
+  bool scales_in_stage = false;
+  size_t smem = 0;
+};
+
+int mt_for(int64_t M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+
+Plan plan_for(int64_t M, int64_t K, bool block_sums, const DeviceInfo& dev) {
+  Plan pl;
+  if (M < 1 || M > kDecodeMaxM || K < kQK) return pl;
+  const int MT = mt_for(M);
+  const int64_t nb = K / kQK;
+  pl.scales_in_stage = !block_sums && (nb % 8 == 0);
+  pl.R = static_cast<int>(K >= kStageTarget ? 1 : kStageTarget / K);
+  const size_t stage = static_cast<size_t>(pl.R) * (K + (pl.scales_in_stage ? nb * 2 : 0));
+  const size_t fixed = static_cast<size_t>((MT * K + MT * nb * 4 + 127) & ~static_cast<int64_t>(127));
+  const int smin = 2;
+  int want = static_cast<int>((kRingTarget + stage - 1) / stage);
+  if (want < smin) want = smin;
+  if (want > kMaxStages) want = kMaxStages;
+  const size_t budget = static_cast<size_t>(dev.max_smem_optin) - 2048;  // static smem headroom
+  if (fixed + smin * stage > budget) return Plan{};
+  int S = want;
+  while (S > smin && fixed + S * stage > budget) --S;
+  pl.S = S;
+  pl.smem = fixed + S * stage;
+  return pl;
+}
+
+template <int MT, bool kBS, bool kSc, int kXP = 0>
 cudaError_t launch_one(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream) {
-  auto fn = decode_kernel<MT, kBS, kSc>;
+  auto fn = decode_kernel<MT, kBS, kSc, kXP>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  fn<<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 template <int MT>
 cudaError_t launch_mt(const DecodeParams& p, bool bs, bool sc, int grid, size_t smem,
                       cudaStream_t stream) {
-  if (bs) return sc ? launch_one<MT, true, true>(p, grid, smem, stream)
-                    : launch_one<MT, true, false>(p, grid, smem, stream);
+  if constexpr (MT == 1) {
+    if (p.K <= 512 * kXRegPieces) {  // activation codes in registers
+      if (bs) return launch_one<1, true, false, kXRegPieces>(p, grid, smem, stream);
+      return sc ? launch_one<1, false, true, kXRegPieces>(p, grid, smem, stream)
+                : launch_one<1, false, false, kXRegPieces>(p, grid, smem, stream);
+    }
+  }
+  if (bs) return launch_one<MT, true, false>(p, grid, smem, stream);
   return sc ? launch_one<MT, false, true>(p, grid, smem, stream)
             : launch_one<MT, false, false>(p, grid, smem, stream);
-}
-
-int mt_for(int64_t M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
-
-size_t fixed_bytes(int MT, int64_t K) {
-  const int64_t nb = K / kQK;
-  return static_cast<size_t>((MT * K + MT * nb * 4 + 127) & ~static_cast<int64_t>(127));
 }
 
 }  // namespace
 
 size_t decode_smem_bytes(int64_t M, int64_t K, const DeviceInfo& dev) {
-  if (M < 1 || M > kDecodeMaxM || K < kQK) return 0;
-  const int MT = mt_for(M);
-  const size_t stage = static_cast<size_t>(K) + ((K % 256 == 0) ? static_cast<size_t>(K / 16) : 0);
-  const size_t fixed = fixed_bytes(MT, K);
-  const size_t budget = static_cast<size_t>(dev.max_smem_optin) - 2048;  // static smem headroom
-  if (fixed + 2 * stage > budget) return 0;
-  size_t stages = (budget - fixed) / stage;
-  if (stages > kMaxStages) stages = kMaxStages;
-  // enough stages to keep ~96 KB in flight; more only costs shared memory
-  size_t want = (96 * 1024 + stage - 1) / stage;
-  if (want < 2) want = 2;
-  if (stages > want) stages = want;
-  return fixed + stages * stage;
+  return plan_for(M, K, false, dev).smem;
 }
 
 cudaError_t launch_decode(const void* x, int xtype, const int8_t* xq_in, const int8_t* Wq,
                           const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
                           int64_t K, const DeviceInfo& dev, cudaStream_t stream) {
   if (M == 0 || N == 0) return cudaSuccess;
-  const size_t smem = decode_smem_bytes(M, K, dev);
-  if (smem == 0) return cudaErrorInvalidValue;
-  const int MT = mt_for(M);
-  // block-sum mode reads no scales
-  const bool scales_in_stage = (K % 256) == 0 && isum == nullptr;
-  const size_t stage = static_cast<size_t>(K) + (scales_in_stage ? static_cast<size_t>(K / 16) : 0);
+  const bool bs = isum != nullptr;
+  const Plan pl = plan_for(M, K, bs, dev);
+  if (pl.smem == 0) return cudaErrorInvalidValue;
   DecodeParams p;
   p.x = x;
   p.xtype = xtype;
@@ -279,16 +369,15 @@ cudaError_t launch_decode(const void* x, int xtype, const int8_t* xq_in, const i
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  const size_t stages = (smem - fixed_bytes(MT, K)) / stage;
-  p.stages = static_cast<int>(stages < kMaxStages ? stages : kMaxStages);
+  p.rows_per_stage = pl.R;
+  p.stages = pl.S;
   p.err = dev.err_word;
   const int grid = static_cast<int>(N < dev.sm_count ? N : dev.sm_count);
-  const bool bs = isum != nullptr;
-  switch (MT) {
-    case 1: return launch_mt<1>(p, bs, scales_in_stage, grid, smem, stream);
-    case 2: return launch_mt<2>(p, bs, scales_in_stage, grid, smem, stream);
-    case 4: return launch_mt<4>(p, bs, scales_in_stage, grid, smem, stream);
-    default: return launch_mt<8>(p, bs, scales_in_stage, grid, smem, stream);
+  switch (mt_for(M)) {
+    case 1: return launch_mt<1>(p, bs, pl.scales_in_stage, grid, pl.smem, stream);
+    case 2: return launch_mt<2>(p, bs, pl.scales_in_stage, grid, pl.smem, stream);
+    case 4: return launch_mt<4>(p, bs, pl.scales_in_stage, grid, pl.smem, stream);
+    default: return launch_mt<8>(p, bs, pl.scales_in_stage, grid, pl.smem, stream);
   }
 }
 

@@ -93,7 +93,7 @@ def _codes(rng, rows, K):
 
 @pytest.mark.parametrize("path,M,N,K", [
     ("decode", 1, 7, 64), ("decode", 3, 100, 288), ("decode", 8, 33, 4096),
-    ("decode", 5, 257, 4128),
+    ("decode", 5, 257, 4128), ("decode", 1, 700, 17408), ("decode", 6, 1500, 4096),
     ("tensor", 16, 256, 512), ("tensor", 130, 300, 96), ("tensor", 1, 1, 32),
     ("tensor", 257, 513, 160), ("tensor", 3, 40, 4096)])
 def test_block_sums_bit_exact(q8, path, M, N, K):
@@ -111,7 +111,8 @@ def test_block_sums_bit_exact(q8, path, M, N, K):
 
 @pytest.mark.parametrize("path,M,N,K,bf16", [
     ("decode", 1, 300, 4096, True), ("decode", 2, 257, 4128, True), ("decode", 4, 1000, 512, False),
-    ("decode", 8, 64, 17408, True), ("decode", 3, 5, 32, True), ("decode", 7, 129, 96, False),
+    ("decode", 2, 64, 17408, True), ("decode", 3, 5, 32, True), ("decode", 7, 129, 96, False),
+    ("decode", 1, 5120, 17408, True), ("decode", 4, 3000, 12288, True), ("decode", 8, 2000, 4096, True),
     ("tensor", 16, 256, 512, False), ("tensor", 130, 300, 96, True), ("tensor", 257, 513, 1056, True),
     ("tensor", 128, 256, 4096, True), ("tensor", 1, 17, 32, True), ("tensor", 200, 100, 4128, False),
     ("auto", 16, 256, 512, False), ("auto", 1, 256, 512, True)])
