@@ -208,7 +208,7 @@ TRAFFIC_PROFILES = {  # committed ncu summaries that record DRAM bytes per launc
 
 
 def time_graph_steps(torch, q8, step_fns, steps, warmup, instrument=True):
-    """Captures one CUDA graph holding len(step_fns) steps, runs `warmup` steps, then times
+    """Captures one CUDA graph holding whole rotations of step_fns, runs `warmup` steps, then times
     exactly `steps` steps: whole replays plus a replay of a graph holding the remainder.
     Returns (seconds for the timed steps, mean seconds of the main kernel), all from CUDA
     events on the launching stream.  With `instrument`, the library records event nodes
@@ -216,13 +216,17 @@ def time_graph_steps(torch, q8, step_fns, steps, warmup, instrument=True):
     without it (one kernel per step, consecutive launches overlapping through programmatic
     dependent launch, which event nodes between them would serialize), the main kernel's
     time per launch is the timed region's time per step."""
+    # one graph holds a whole number of rotations and at least 48 steps, so the chain of
+    # overlapping launches breaks only at replay boundaries, rarely
+    reps = max(1, -(-min(48, steps) // len(step_fns)))
+    step_fns = list(step_fns) * reps
     R = len(step_fns)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(R)]
     stops = [torch.cuda.Event(enable_timing=True) for _ in range(R)]
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        for f in step_fns:  # eager once (function attributes, workspace) before capture
+        for f in step_fns[:len(step_fns) // reps]:  # eager once (attributes, workspace)
             f()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()

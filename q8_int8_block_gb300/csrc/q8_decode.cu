@@ -9,16 +9,16 @@
 // Design (one CTA per SM, 1 producer warp + 16 consumer warps):
 //   * CTA c owns the contiguous rows [r0, r1) of W.  Their codes (and, when a row of scales
 //     is a multiple of 16 bytes, their binary16 scales) are contiguous, and stream through a
-//     ring of shared-memory stages of R whole rows (about 16 KB) by bulk asynchronous copies
-//     that one elected thread issues; each stage completes on its own mbarrier.  Copies of
-//     16 KB keep the per-copy overhead of the copy engine small.
+//     ring of shared-memory stages of R whole rows (about 24 KB; 192 KB in flight per SM)
+//     by bulk asynchronous copies that one elected thread issues; each stage completes on
+//     its own mbarrier.  Large copies keep the per-copy overhead of the copy engine small
+//     (4 KB copies ran at a third of the bandwidth).
 //   * Programmatic dependent launch: the kernel lets the next kernel in the stream start as
 //     soon as it begins, and its producer fills the ring before anything waits for the
 //     previous kernel.  Only the consumers wait (griddepcontrol.wait) before they read x and
 //     write y.  So the weights, which are read before that wait, must not be written by a
-//     kernel that triggers its dependents early (no kernel of this library does).  A CTA is
-//     small enough that the next kernel's CTA can be resident on the same SM and prefetch
-//     its first stages while this one finishes.
+//     kernel that triggers its dependents early (no kernel of this library does).  The next
+//     kernel's CTAs start streaming their first stages as soon as this kernel's CTAs exit.
 //   * Fused activation quantizer: after the wait, the consumers quantize the M activation
 //     rows into shared memory with the same device function as the standalone quantizer.
 //   * Consumer warp w takes rows w, w + 16, ...: lane l handles the 16-byte pieces
@@ -39,8 +39,11 @@ namespace {
 constexpr int kConsumerWarps = 16;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxStages = 32;
-constexpr int kStageTarget = 16 * 1024;  // bytes of codes per stage (whole rows)
-constexpr int kRingTarget = 96 * 1024;   // bytes of codes and scales in flight per CTA
+// Stage and ring sizes (measured on GB300 for the M=1 decode workload, graph replays with
+// programmatic dependent launch): 24 KB stages in a 192 KB ring beat 16 KB stages in a
+// ring small enough for two CTAs per SM (9.3 us vs 10.5 us per 53.5 MB call).
+constexpr int kStageTarget = 24 * 1024;  // bytes of codes per stage (whole rows)
+constexpr int kRingTarget = 192 * 1024;  // bytes of codes and scales in flight per CTA
 constexpr int kXRegPieces = 8;           // one token with K <= 4096: codes in registers
 
 struct DecodeParams {

@@ -12,15 +12,20 @@
 // accumulator).  Each Q8_0 block gets its own TMEM accumulator (two K=16 MMAs starting
 // from zero), so the value read back is exactly the int32 block sum isum[m,n,b].
 //
-// Design (one CTA per 128 x 256 output tile, 320 threads):
+// Design (one CTA per 128 x 256 output tile, 384 threads = 3 warpgroups; the control
+// warpgroup hands registers to the two drain warpgroups with setmaxnreg):
 //   warp 0     TMA producer: A (activation codes, 128 x 64 binary16) and B (weight codes,
-//              256 x 64 binary16) tiles with 128-byte swizzle into a 4-stage ring;
+//              256 x 64 binary16) tiles with 128-byte swizzle into a 3-stage ring;
 //   warp 1     TMEM owner and MMA issuer: per 32-K block, 2 x tcgen05.mma
 //              (M=128, N=256, K=16) into one of two 256-column TMEM buffers, then
 //              tcgen05.commit to that buffer's "full" barrier;
-//   warps 2-9  rescale drain, two warpgroups of 128 columns each: tcgen05.ld the block
-//              sums of their TMEM lanes, y_acc += (Wd * xd) * isum in binary32
-//              registers, release the TMEM buffer; finally store y.
+//   warps 2-3  scale producer: windows of 16 blocks of Wd (the tile's columns) and xd (its
+//              rows), widened to binary32 into a 2-slot shared-memory ring;
+//   warps 4-11 rescale drain, two warpgroups of 128 columns each: per block, tcgen05.ld
+//              the block sums of their TMEM lanes 16 columns at a time and the column
+//              scales from shared memory, both one chunk ahead, then
+//              y_acc += (xd * Wd) * isum in binary32 registers (packed f32x2 multiply,
+//              scalar fused multiply-add); release the TMEM buffer; finally store y.
 // Block-sum mode (for checking) stores the TMEM block sums as int32 instead.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -36,14 +41,27 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;  // two Q8_0 blocks per pipeline stage (one 128-byte swizzle row)
-constexpr int kStages = 4;
-constexpr int kThreads = 320;
+constexpr int kStages = 3;
+constexpr int kThreads = 384;               // 3 warpgroups
+// Register split (setmaxnreg): the kernel is compiled for kLaunchRegs per thread; the
+// control warpgroup gives registers back, the two drain warpgroups take them.  Per SM
+// sub-partition (one warp of each warpgroup) and in total the split equals the launch.
+constexpr int kLaunchRegs = 168;
+constexpr int kCtrlRegs = 56;
+constexpr int kDrainRegs = 224;
+static_assert(128 * kCtrlRegs + 256 * kDrainRegs == kThreads * kLaunchRegs, "register split");
+static_assert(32 * (kCtrlRegs + 2 * kDrainRegs) <= 16384, "registers per sub-partition");
 constexpr int kDrainWarps = 8;
+constexpr int kScaleThreads = 64;           // warps 2-3 stage the scales
 constexpr uint32_t kStageA = BM * BK * 2;   // 16 KB
 constexpr uint32_t kStageB = BN * BK * 2;   // 32 KB
 constexpr uint32_t kTmemCols = 2 * BN;      // two accumulation buffers
+constexpr int kWin = 16;                    // Q8_0 blocks per window of staged scales
+constexpr int kWinSlots = 2;                // windows in the scale ring
+constexpr uint32_t kWinDw = kWin * BN * 4;  // Wd of the tile's columns, f32   (16 KB)
+constexpr uint32_t kWinDx = kWin * BM * 4;  // xd of the tile's rows, f32      (8 KB)
 constexpr size_t kSmemBytes = 1024 /*align*/ + kStages * (kStageA + kStageB) +
-                              2 /*wg*/ * 2 /*buf*/ * 128 * sizeof(float);
+                              kWinSlots * (kWinDw + kWinDx);
 
 struct GemmParams {
   const float* xd;     // [M, nb]
@@ -54,6 +72,64 @@ struct GemmParams {
   uint32_t* err;
 };
 
+// Fill one window of scales: Wd of the tile's 256 columns and xd of its 128 rows, blocks
+// [16 w, 16 w + 16) (zero past the ends), as f32 [block][column] and [block][row].
+__device__ __forceinline__ void stage_scales(const GemmParams& p, int w, int m0, int n0, int nb,
+                                             float* dws, float* dxs, int t) {
+  const int b0 = w * kWin;
+  const bool vec_w = (nb % 8) == 0;   // 8 binary16 scales of a row are one 16-byte load
+  const bool vec_x = (nb % 4) == 0;
+#pragma unroll 1
+  for (int q = 0; q < BN / kScaleThreads; ++q) {
+    const int col = t + kScaleThreads * q;
+    const int n = n0 + col;
+#pragma unroll
+    for (int h = 0; h < kWin; h += 8) {
+      float f[8];
+      if (n < p.N && vec_w && b0 + h + 8 <= nb) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.Wd + static_cast<int64_t>(n) * nb + b0 + h));
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 g = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+          f[2 * i] = g.x;
+          f[2 * i + 1] = g.y;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          f[i] = (n < p.N && b0 + h + i < nb)
+                     ? __half2float(__ushort_as_half(p.Wd[static_cast<int64_t>(n) * nb + b0 + h + i]))
+                     : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dws[(h + i) * BN + col] = f[i];
+    }
+  }
+#pragma unroll 1
+  for (int q = 0; q < BM / kScaleThreads; ++q) {
+    const int row = t + kScaleThreads * q;
+    const int m = m0 + row;
+#pragma unroll
+    for (int h = 0; h < kWin; h += 4) {
+      float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (m < p.M && vec_x && b0 + h + 4 <= nb) {
+        v = __ldg(reinterpret_cast<const float4*>(p.xd + static_cast<int64_t>(m) * nb + b0 + h));
+      } else if (m < p.M) {
+        const float* src = p.xd + static_cast<int64_t>(m) * nb + b0 + h;
+        if (b0 + h + 0 < nb) v.x = src[0];
+        if (b0 + h + 1 < nb) v.y = src[1];
+        if (b0 + h + 2 < nb) v.z = src[2];
+        if (b0 + h + 3 < nb) v.w = src[3];
+      }
+      dxs[(h + 0) * BM + row] = v.x;
+      dxs[(h + 1) * BM + row] = v.y;
+      dxs[(h + 2) * BM + row] = v.z;
+      dxs[(h + 3) * BM + row] = v.w;
+    }
+  }
+}
+
 template <bool kBlockSums>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -61,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2];
+  __shared__ uint64_t sfull_bar[kWinSlots], sempty_bar[kWinSlots];
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
 
@@ -68,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int M = p.M, N = p.N, K = p.K;
   const int nb = K / kQK;
   const int nk = (K + BK - 1) / BK;
+  const int nwin = (nb + kWin - 1) / kWin;
   const int mtiles = (M + BM - 1) / BM;
   const int m0 = (blockIdx.x % mtiles) * BM;
   const int n0 = (blockIdx.x / mtiles) * BN;
@@ -77,7 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base = smem_raw + (((raw + 1023) & ~1023u) - raw);
   uint8_t* sA = base;
   uint8_t* sB = base + kStages * kStageA;
-  float* sDw = reinterpret_cast<float*>(sB + kStages * kStageB);  // [wg][buf][128]
+  float* sW = reinterpret_cast<float*>(sB + kStages * kStageB);  // [slot][kWin][BN]
+  float* sX = sW + kWinSlots * kWin * BN;                          // [slot][kWin][BM]
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -89,6 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tfull_bar[b], 1);
       mbar_init(&tempty_bar[b], kDrainWarps);
     }
+    for (int b = 0; b < kWinSlots; ++b) {
+      mbar_init(&sfull_bar[b], kScaleThreads);
+      mbar_init(&sempty_bar[b], kDrainWarps);
+    }
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -99,154 +182,200 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_slot;
 
-  if (warp == 0) {
-    // ------------------------------- TMA producer -------------------------------------
-    if (lane == 0) {
-      int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kStages;
-        if (!mbar_wait(&empty_bar[s], ((kb / kStages) & 1) ^ 1, &abort_flag)) {
-          report_error(p.err, kErrWaitTimeout, &abort_flag);
-          break;
-        }
-        mbar_arrive_expect_tx(&full_bar[s], kStageA + kStageB);
-        tma_load_2d(sA + s * kStageA, &tmA, &full_bar[s], kb * BK, m0);
-        tma_load_2d(sB + s * kStageB, &tmB, &full_bar[s], kb * BK, n0);
-        ++issued;
-      }
-      for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb)
-        if (!mbar_wait(&full_bar[kb % kStages], (kb / kStages) & 1, nullptr)) {
-          report_error(p.err, kErrWaitTimeout, nullptr);
-          break;
-        }
-    }
-  } else if (warp == 1) {
-    // ------------------------------- MMA issuer ---------------------------------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
-      int last_stage = -1;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kStages;
-        if (!mbar_wait(&full_bar[s], (kb / kStages) & 1, &abort_flag)) {
-          report_error(p.err, kErrWaitTimeout, &abort_flag);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t a0 = smem_u32(sA + s * kStageA);
-        const uint32_t b0 = smem_u32(sB + s * kStageB);
-        const int nblk = (nb - 2 * kb) < 2 ? (nb - 2 * kb) : 2;
-        bool ok = true;
-        for (int j = 0; j < nblk; ++j) {
-          const int blk = 2 * kb + j;
-          const int buf = blk & 1;
-          if (!mbar_wait(&tempty_bar[buf], ((blk >> 1) & 1) ^ 1, &abort_flag)) {
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+    if (warp == 0) {
+      // ------------------------------- TMA producer -----------------------------------
+      if (lane == 0) {
+        int issued = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+          const int s = kb % kStages;
+          if (!mbar_wait(&empty_bar[s], ((kb / kStages) & 1) ^ 1, &abort_flag)) {
             report_error(p.err, kErrWaitTimeout, &abort_flag);
-            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[s], kStageA + kStageB);
+          tma_load_2d(sA + s * kStageA, &tmA, &full_bar[s], kb * BK, m0);
+          tma_load_2d(sB + s * kStageB, &tmB, &full_bar[s], kb * BK, n0);
+          ++issued;
+        }
+        for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb)
+          if (!mbar_wait(&full_bar[kb % kStages], (kb / kStages) & 1, nullptr)) {
+            report_error(p.err, kErrWaitTimeout, nullptr);
+            break;
+          }
+      }
+    } else if (warp == 1) {
+      // ------------------------------- MMA issuer -------------------------------------
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+        int last_stage = -1;
+        for (int kb = 0; kb < nk; ++kb) {
+          const int s = kb % kStages;
+          if (!mbar_wait(&full_bar[s], (kb / kStages) & 1, &abort_flag)) {
+            report_error(p.err, kErrWaitTimeout, &abort_flag);
             break;
           }
           tc_fence_after();
-          const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
+          const uint32_t a0 = smem_u32(sA + s * kStageA);
+          const uint32_t b0 = smem_u32(sB + s * kStageB);
+          const int nblk = (nb - 2 * kb) < 2 ? (nb - 2 * kb) : 2;
+          bool ok = true;
+          for (int j = 0; j < nblk; ++j) {
+            const int blk = 2 * kb + j;
+            const int buf = blk & 1;
+            if (!mbar_wait(&tempty_bar[buf], ((blk >> 1) & 1) ^ 1, &abort_flag)) {
+              report_error(p.err, kErrWaitTimeout, &abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint32_t koff = static_cast<uint32_t>((2 * j + kk) * 32);  // 16 f16 = 32 B
-            mma_f16_ss(d, sdesc_k_sw128(a0 + koff), sdesc_k_sw128(b0 + koff), idesc,
-                       kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 2; ++kk) {
+              const uint32_t koff = static_cast<uint32_t>((2 * j + kk) * 32);  // 16 f16 = 32 B
+              mma_f16_ss(d, sdesc_k_sw128(a0 + koff), sdesc_k_sw128(b0 + koff), idesc,
+                         kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&tfull_bar[buf]);
           }
-          mma_commit(&tfull_bar[buf]);
+          mma_commit(&empty_bar[s]);
+          last_stage = kb;
+          if (!ok) break;
         }
-        mma_commit(&empty_bar[s]);
-        last_stage = kb;
-        if (!ok) break;
+        // do not leave while MMAs are still reading shared memory / writing TMEM
+        if (last_stage >= 0 &&
+            !mbar_wait(&empty_bar[last_stage % kStages], (last_stage / kStages) & 1, nullptr))
+          report_error(p.err, kErrWaitTimeout, nullptr);
       }
-      // do not leave while MMAs are still reading shared memory / writing TMEM
-      if (last_stage >= 0 &&
-          !mbar_wait(&empty_bar[last_stage % kStages], (last_stage / kStages) & 1, nullptr))
-        report_error(p.err, kErrWaitTimeout, nullptr);
+    } else if constexpr (!kBlockSums) {
+      // ------------------------------- scale producer (warps 2-3) ---------------------
+      const int t = threadIdx.x - 64;  // 0..63
+      for (int w = 0; w < nwin; ++w) {
+        const int slot = w % kWinSlots;
+        if (!mbar_wait(&sempty_bar[slot], ((w / kWinSlots) & 1) ^ 1, &abort_flag)) {
+          report_error(p.err, kErrWaitTimeout, &abort_flag);
+          break;
+        }
+        stage_scales(p, w, m0, n0, nb, sW + slot * kWin * BN, sX + slot * kWin * BM, t);
+        mbar_arrive(&sfull_bar[slot]);  // release: the stores above are visible to waiters
+      }
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kDrainRegs));
     // ------------------------------- rescale drain ------------------------------------
-    const int dw_idx = warp - 2;            // 0..7
-    const int wg = dw_idx >> 2;             // column half of the tile
-    const int quad = warp & 3;              // TMEM lane quadrant this warp may access
-    const int row = quad * 32 + lane;       // tile row = TMEM lane
+    // Warp w (4..11) may read TMEM lanes 32*(w%4)..+31 (its quadrant); warpgroup wg owns
+    // tile columns [128 wg, 128 wg + 128).  Each thread owns one row m and 128 columns:
+    // per block b, acc[n] += (xd[m,b] * Wd[n,b]) * isum[m,n,b] in binary32.  Per block:
+    // 8 chunks of 16 columns; the TMEM load and the shared-memory scale load of chunk
+    // c + 1 are in flight while chunk c is computed.
+    const int wg = (warp - 4) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
     const int m = m0 + row;
-    const int wg_tid = (dw_idx & 3) * 32 + lane;  // 0..127 within the warpgroup
-    const int n_load = n0 + wg * 128 + wg_tid;    // the column whose scale this thread stages
     const bool m_ok = m < M;
-    float acc[kBlockSums ? 1 : 128];
+    float2 acc[kBlockSums ? 1 : 64];
     if constexpr (!kBlockSums) {
 #pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
     }
-    float dw_next = (!kBlockSums && n_load < N) ? __half2float(__ushort_as_half(p.Wd[static_cast<int64_t>(n_load) * nb])) : 0.0f;
-    float dx_next = (!kBlockSums && m_ok) ? p.xd[static_cast<int64_t>(m) * nb] : 0.0f;
-    for (int blk = 0; blk < nb; ++blk) {
-      const int buf = blk & 1;
-      float* dws = sDw + (wg * 2 + buf) * 128;
-      float dx = 0.0f;
+    bool failed = false;
+    for (int w = 0; w < nwin && !failed; ++w) {
+      const int slot = w % kWinSlots;
+      const float* dws = sW + slot * kWin * BN + wg * 128;
+      const float* dxs = sX + slot * kWin * BM;
       if constexpr (!kBlockSums) {
-        dws[wg_tid] = dw_next;
-        dx = dx_next;
-      }
-      const bool ok = mbar_wait(&tfull_bar[buf], (blk >> 1) & 1, &abort_flag);
-      // Warpgroup barrier that also ORs the failures: the 128 threads leave together, and
-      // the staged scales are visible to all of them.
-      if (wg_barrier_any(2 + wg, !ok)) {
-        if (lane == 0) report_error(p.err, kErrWaitTimeout, &abort_flag);
-        break;
-      }
-      if constexpr (!kBlockSums) {
-        if (blk + 1 < nb) {
-          dw_next = n_load < N ? __half2float(__ushort_as_half(p.Wd[static_cast<int64_t>(n_load) * nb + blk + 1])) : 0.0f;
-          dx_next = m_ok ? p.xd[static_cast<int64_t>(m) * nb + blk + 1] : 0.0f;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sfull_bar[slot], (w / kWinSlots) & 1, &abort_flag))) {
+          if (lane == 0) report_error(p.err, kErrWaitTimeout, &abort_flag);
+          failed = true;
+          break;
         }
       }
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                             static_cast<uint32_t>(buf * BN + wg * 128);
+      const int nbw = (nb - w * kWin) < kWin ? (nb - w * kWin) : kWin;
+#pragma unroll 1
+      for (int bb = 0; bb < nbw; ++bb) {
+        const int blk = w * kWin + bb;
+        const int buf = blk & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull_bar[buf], (blk >> 1) & 1, &abort_flag))) {
+          if (lane == 0) report_error(p.err, kErrWaitTimeout, &abort_flag);
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                               static_cast<uint32_t>(buf * BN + wg * 128);
+        const float* dwb = dws + bb * BN;
+        float dx = 0.0f;
+        if constexpr (!kBlockSums) dx = dxs[bb * BM + row];
+        const float2 dx2 = make_float2(dx, dx);
+        uint32_t r[2][16];
+        float4 wv[2][4];
+        tmem_ld_32x32b_x16(taddr, r[0]);
+        if constexpr (!kBlockSums) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, r);
-        tmem_ld_wait();
-        if constexpr (kBlockSums) {
-          if (m_ok) {
+          for (int i = 0; i < 4; ++i) wv[0][i] = *reinterpret_cast<const float4*>(dwb + 4 * i);
+        }
+        tmem_ld_wait_regs(r[0]);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int n = n0 + wg * 128 + c * 32 + i;
-              if (n < N)
-                p.isum[(static_cast<int64_t>(m) * N + n) * nb + blk] =
-                    __float2int_rn(__uint_as_float(r[i]));
+        for (int c = 0; c < 8; ++c) {
+          if (c + 1 < 8) {
+            tmem_ld_32x32b_x16(taddr + (c + 1) * 16, r[(c + 1) & 1]);
+            if constexpr (!kBlockSums) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                wv[(c + 1) & 1][i] = *reinterpret_cast<const float4*>(dwb + (c + 1) * 16 + 4 * i);
             }
           }
-        } else {
+          const uint32_t* rc = r[c & 1];
+          if constexpr (kBlockSums) {
+            if (m_ok) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 w4 = *reinterpret_cast<const float4*>(dws + c * 32 + i);
-            acc[c * 32 + i + 0] = fmaf(dx * w4.x, __uint_as_float(r[i + 0]), acc[c * 32 + i + 0]);
-            acc[c * 32 + i + 1] = fmaf(dx * w4.y, __uint_as_float(r[i + 1]), acc[c * 32 + i + 1]);
-            acc[c * 32 + i + 2] = fmaf(dx * w4.z, __uint_as_float(r[i + 2]), acc[c * 32 + i + 2]);
-            acc[c * 32 + i + 3] = fmaf(dx * w4.w, __uint_as_float(r[i + 3]), acc[c * 32 + i + 3]);
+              for (int i = 0; i < 16; ++i) {
+                const int n = n0 + wg * 128 + c * 16 + i;
+                if (n < N)
+                  p.isum[(static_cast<int64_t>(m) * N + n) * nb + blk] =
+                      __float2int_rn(__uint_as_float(rc[i]));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float4 w4 = wv[c & 1][i];
+              const float2 c0 = __fmul2_rn(dx2, make_float2(w4.x, w4.y));
+              const float2 c1 = __fmul2_rn(dx2, make_float2(w4.z, w4.w));
+              const int a = (c * 16 + 4 * i) >> 1;
+              acc[a].x = fmaf(c0.x, __uint_as_float(rc[4 * i]), acc[a].x);
+              acc[a].y = fmaf(c0.y, __uint_as_float(rc[4 * i + 1]), acc[a].y);
+              acc[a + 1].x = fmaf(c1.x, __uint_as_float(rc[4 * i + 2]), acc[a + 1].x);
+              acc[a + 1].y = fmaf(c1.y, __uint_as_float(rc[4 * i + 3]), acc[a + 1].y);
+            }
           }
+          if (c + 1 < 8) tmem_ld_wait_regs(r[(c + 1) & 1]);
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+      if constexpr (!kBlockSums) {
+        __syncwarp();
+        if (lane == 0 && !failed) mbar_arrive(&sempty_bar[slot]);
+      }
     }
     if constexpr (!kBlockSums) {
-      if (m_ok) {
+      if (m_ok && !failed) {
         float* yrow = p.y + static_cast<int64_t>(m) * N;
         const int nbase = n0 + wg * 128;
         if ((N & 3) == 0 && nbase + 128 <= N) {
 #pragma unroll
-          for (int i = 0; i < 128; i += 4)
-            *reinterpret_cast<float4*>(yrow + nbase + i) =
-                make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+          for (int i = 0; i < 64; i += 2)
+            *reinterpret_cast<float4*>(yrow + nbase + 2 * i) =
+                make_float4(acc[i].x, acc[i].y, acc[i + 1].x, acc[i + 1].y);
         } else {
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (nbase + i < N) yrow[nbase + i] = acc[i];
+          for (int i = 0; i < 64; ++i) {
+            if (nbase + 2 * i < N) yrow[nbase + 2 * i] = acc[i].x;
+            if (nbase + 2 * i + 1 < N) yrow[nbase + 2 * i + 1] = acc[i].y;
+          }
         }
       }
     }
@@ -298,8 +427,14 @@ template <bool kBS>
 cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
                         cudaStream_t stream) {
   auto fn = gemm_tc_kernel<kBS>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
+  // setmaxnreg.inc waits until the registers exist: the split above is exact only if the
+  // kernel was compiled for kLaunchRegs per thread.  Refuse to launch otherwise.
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   fn<<<grid, kThreads, kSmemBytes, stream>>>(a, b, p);
   return cudaGetLastError();

@@ -196,6 +196,29 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
+// 32 TMEM lanes x 16 consecutive 32-bit columns (see tmem_ld_32x32b_x32).  No memory
+// clobber: the values reach their users through the registers, and tmem_ld_wait_regs
+// below makes every user wait for the load.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// tcgen05.wait::ld that also "rewrites" the 16 registers of an earlier load, so the
+// compiler cannot schedule any use of them before the wait (without a memory clobber
+// that would also pin unrelated shared-memory loads in place).
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
 // Shared-memory matrix descriptor for tcgen05 (K-major operand, 128-byte swizzle):
 // rows of 128 bytes, 8-row / 1024-byte swizzle atoms stacked every 1024 bytes.
 __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t smem_addr) {
