@@ -128,6 +128,29 @@ q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64
 uint32_t q8_device_error(q8_status* status);
 
 /*
+ * q8_linear_noalloc -- the tensor-core Q8_0 linear layer (same kernels and results as
+ * q8_linear_ex with Q8_PATH_TENSOR) for callers that cannot allocate device memory during
+ * a call: a host framework that owns every device allocation through its own fixed pool,
+ * or a serving loop where cudaMalloc's implicit device synchronization, or running out of
+ * memory in the middle of a step, is not acceptable.  The post has no counterpart of this
+ * entry point; it exists for such callers only.
+ *   x [M,K] of type xtype, Wq/Wd from q8_quantize_weights, y [M,N] float out.
+ * Scratch lives in one static device array of Q8_NOALLOC_SCRATCH_BYTES bytes that every
+ * GPU loading the library holds until the process exits; this call allocates and frees
+ * nothing.  A shape whose scratch (2*M*K + 4*M*(K/32) + 2*N*K bytes, each part rounded up
+ * to 256) exceeds the array is rejected with Q8_ERR_NOMEM before anything runs.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current: make that first call before any stream capture.
+ * All calls on a device share the one array, and its contents stay from the last call
+ * (each call writes all the scratch it reads, so nothing needs clearing): calls that
+ * overlap on the GPU -- on different streams, or from different threads -- race, so
+ * serialize them.
+ */
+#define Q8_NOALLOC_SCRATCH_BYTES (64u << 20)
+q8_status q8_linear_noalloc(const void* x, q8_dtype xtype, const int8_t* Wq, const uint16_t* Wd,
+                            float* y, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
  * q8_set_timing_events -- timing hook for benchmarks.  With count > 0, each later
  * q8_linear / q8_linear_ex call records starts[i] on its stream right before the launch
  * of its main kernel (the decode kernel, or the tensor-core GEMM) and stops[i] right after

@@ -19,7 +19,7 @@ import torch
 
 __all__ = ["Q8Error", "q8_quantize_weights", "q8_quantize_act", "q8_linear", "q8_linear_ex",
            "q8_linear_workspace_size", "q8_block_sums", "q8_device_error", "q8_release",
-           "q8_set_timing_events",
+           "q8_set_timing_events", "q8_linear_noalloc", "NOALLOC_SCRATCH_BYTES",
            "q8_version", "lib_path", "QK", "PATHS"]
 
 QK = 32
@@ -53,6 +53,7 @@ def _load():
         "q8_linear": [p, p, p, p, i64, i64, i64, p],
         "q8_linear_ex": [p, i32, p, p, p, i64, i64, i64, i32, p, sz, p],
         "q8_block_sums": [p, p, p, i64, i64, i64, i32, p],
+        "q8_linear_noalloc": [p, i32, p, p, p, i64, i64, i64, p],
     }
     for name, args in sigs.items():
         f = getattr(L, name)
@@ -180,6 +181,24 @@ def q8_linear_ex(x, Wq, Wd, y=None, path="auto", workspace=None, stream=None):
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_L.q8_linear_ex(_ptr(x), DTYPES[x.dtype], _ptr(Wq), _ptr(Wd), _ptr(y), M, N, K,
                            PATHS[path], _ptr(workspace), nbytes, _stream(stream)), "q8_linear_ex")
+    return y
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def q8_linear_noalloc(x, Wq, Wd, y=None, stream=None):
+    """Tensor-core Q8_0 linear that allocates no device memory: its scratch is a static
+    device array of NOALLOC_SCRATCH_BYTES in the library (see include/q8.h).  For callers
+    whose memory is owned by a fixed pool or whose step must not allocate.  Calls that
+    overlap on the GPU share that array and race; make the first call on a device before
+    any stream capture."""
+    if x.dtype not in DTYPES:
+        raise TypeError(f"x: expected bfloat16 or float32, got {x.dtype}")
+    _need(x, x.dtype, tuple(x.shape), "x")
+    M, N, K, y = _lin_check(x, Wq, Wd, y)
+    _check(_L.q8_linear_noalloc(_ptr(x), DTYPES[x.dtype], _ptr(Wq), _ptr(Wd), _ptr(y), M, N, K,
+                                _stream(stream)), "q8_linear_noalloc")
     return y
 
 
