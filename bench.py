@@ -292,14 +292,18 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
     wsz = q8.q8_linear_workspace_size(M, N, K)
     ws = torch.empty(max(wsz, 1), dtype=torch.uint8, device=dev) if wsz else None
-    path = "decode" if wsz == 0 else "tensor"
+    wsz_batch = q8.q8_linear_workspace_size(M, N, K, "batch") if M <= 64 else 0
+    path = "decode" if wsz == 0 else ("batch" if wsz == wsz_batch else "tensor")
     fns = [lambda i=i: q8.q8_linear_ex(x, Wqs[i], Wds[i], y=y, workspace=ws) for i in range(copies)]
     bytes_step = workloads.algorithmic_bytes(M, N, K, x_bytes=xsize)
     ops_step = workloads.algorithmic_ops(M, N, K)
     t_hbm = bytes_step / (pk["hbm_gbs"] * 1e9)
     t_tc = ops_step / (pk["bf16_tflops"] * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
-    inst = path != "decode"  # multi-kernel steps: time the GEMM itself with event nodes
+    # the tensor path's steps hold three kernels: time the GEMM itself with event nodes; the
+    # streaming paths (one kernel, or the activation quantizer chained by programmatic
+    # dependent launch to the batched kernel) are timed per step
+    inst = path == "tensor"
     if clocks:
         with ClockSampler(torch.cuda.current_device()) as clk:
             total, kern = time_graph_steps(torch, q8, fns, steps, warmup, instrument=inst)
@@ -324,16 +328,20 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
                 "algorithmic_flops_per_launch": ops_step,
                 "peak_source": f"bf16_tflops (burst) of the {pk_src} peaks: the kernel runs on "
                                "the dense kind::f16 tensor pipe (int8 codes as binary16)"}
-    roof["kernel"] = "q8::decode_kernel" if path == "decode" else "q8::gemm_tc_kernel"
+    roof["kernel"] = {"decode": "q8::decode_kernel", "batch": "q8::batch_kernel"}.get(
+        path, "q8::gemm_tc_kernel")
     roof["kernel_us"] = round(kern * 1e6, 3)
     roof["kernel_time"] = ("time per step of the timed region (one kernel per step; "
                            "consecutive launches overlap by programmatic dependent launch)"
-                           if not inst else "mean of event-node pairs around the GEMM launches")
+                           if path == "decode" else
+                           "time per step of the timed region (activation quantizer + batched "
+                           "kernel, chained by programmatic dependent launch)"
+                           if path == "batch" else "mean of event-node pairs around the GEMM launches")
     prof = TRAFFIC_PROFILES.get(name)
     roof["traffic"] = profiled_traffic(*prof) if prof else None
     out = {"name": name, "M": M, "K": K, "N": N, "path": path, "unit": unit, "value": value,
            "t_max": t_max, "roofline": roof, "copies": copies, "wbytes": wbytes,
-           "launches_per_step": 1 if path == "decode" else 3, "clocks": clk_summary,
+           "launches_per_step": {"decode": 1, "batch": 2}.get(path, 3), "clocks": clk_summary,
            "bytes_step": bytes_step, "xsize": xsize, "bf16": wl.bf16}
     if e2e:
         out["e2e"] = e2e_measure(torch, q8, dev, x_np, wl.bf16, Wqs, Wds, M, N, K, steps, warmup,

@@ -62,12 +62,16 @@ typedef enum q8_dtype {
     Q8_BF16 = 1          /* bfloat16 activations (uint16 bit patterns)                  */
 } q8_dtype;
 
-/* Which kernel family computes the product.  AUTO picks by M (decode kernel for small
- * M, tensor-core GEMM otherwise); the explicit choices exist for tests and benchmarks. */
+/* Which kernel family computes the product.  AUTO picks by M (decode kernel for one
+ * token, batched-decode kernel for a few tokens, tensor-core GEMM otherwise); the explicit
+ * choices exist for tests and benchmarks. */
 typedef enum q8_path {
     Q8_PATH_AUTO = 0,
-    Q8_PATH_DECODE = 1,  /* weight-streaming kernel (int8 dot products, fused act-quant) */
-    Q8_PATH_TENSOR = 2   /* tcgen05 tensor-core GEMM with per-block rescale             */
+    Q8_PATH_DECODE = 1,  /* weight-streaming kernel (int8 dot products, fused act-quant);
+                            M <= 8                                                        */
+    Q8_PATH_TENSOR = 2,  /* tcgen05 tensor-core GEMM with per-block rescale               */
+    Q8_PATH_BATCH = 3    /* weight-streaming kernel with mma.sync block sums; 1 <= M <= 64,
+                            K % 256 == 0                                                  */
 } q8_path;
 
 /*

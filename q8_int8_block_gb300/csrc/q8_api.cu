@@ -84,22 +84,31 @@ q8_status check_shape(int64_t M, int64_t N, int64_t K) {
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 // Resolves AUTO; returns Q8_ERR_SHAPE if the requested path cannot run this shape.
-q8_status resolve_path(int64_t M, int64_t K, q8_path req, const DeviceInfo& dev, q8_path* out) {
+q8_status resolve_path(int64_t M, int64_t N, int64_t K, q8_path req, const DeviceInfo& dev,
+                       q8_path* out) {
   const bool decode_ok = decode_smem_bytes(M < 1 ? 1 : M, K, dev) != 0 && M <= kDecodeMaxM;
-  if (req == Q8_PATH_AUTO) {
-    *out = decode_ok ? Q8_PATH_DECODE : Q8_PATH_TENSOR;
-    return Q8_OK;
+  const bool batch_ok = batch_supported(M < 1 ? 1 : M, N < 1 ? 1 : N, K, dev);
+  switch (req) {
+    case Q8_PATH_AUTO:
+      if (M <= 1 && decode_ok) *out = Q8_PATH_DECODE;
+      else if (batch_ok) *out = Q8_PATH_BATCH;
+      else if (decode_ok) *out = Q8_PATH_DECODE;
+      else *out = Q8_PATH_TENSOR;
+      return Q8_OK;
+    case Q8_PATH_DECODE:
+      if (!decode_ok) return Q8_ERR_SHAPE;
+      *out = req;
+      return Q8_OK;
+    case Q8_PATH_BATCH:
+      if (!batch_ok) return Q8_ERR_SHAPE;
+      *out = req;
+      return Q8_OK;
+    case Q8_PATH_TENSOR:
+      *out = req;
+      return Q8_OK;
+    default:
+      return Q8_ERR_DTYPE;
   }
-  if (req == Q8_PATH_DECODE) {
-    if (!decode_ok) return Q8_ERR_SHAPE;
-    *out = req;
-    return Q8_OK;
-  }
-  if (req == Q8_PATH_TENSOR) {
-    *out = req;
-    return Q8_OK;
-  }
-  return Q8_ERR_DTYPE;
 }
 
 // Scratch of the tensor path: A16 [M,K] f16 codes, xd [M,K/32] f32, B16 [N,K] f16 codes.
@@ -176,7 +185,9 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
                       float* y, int64_t M, int64_t N, int64_t K, q8_path path, void* ws,
                       size_t ws_bytes, bool library_ws, cudaStream_t stream) {
   if (xtype != Q8_F32 && xtype != Q8_BF16) return Q8_ERR_DTYPE;
-  if (path != Q8_PATH_AUTO && path != Q8_PATH_DECODE && path != Q8_PATH_TENSOR) return Q8_ERR_DTYPE;
+  if (path != Q8_PATH_AUTO && path != Q8_PATH_DECODE && path != Q8_PATH_TENSOR &&
+      path != Q8_PATH_BATCH)
+    return Q8_ERR_DTYPE;
   q8_status st = check_shape(M, N, K);
   if (st != Q8_OK) return st;
   // pointers of empty arrays may be NULL
@@ -187,7 +198,7 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
   DeviceInfo dev;
   if ((st = current_device(&dev)) != Q8_OK) return st;
   q8_path p;
-  if ((st = resolve_path(M, K, path, dev, &p)) != Q8_OK) return st;
+  if ((st = resolve_path(M, N, K, path, dev, &p)) != Q8_OK) return st;
   if (M == 0 || N == 0) return Q8_OK;
   if (K == 0) return launch_status(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 4, stream));
   if (p == Q8_PATH_DECODE)
@@ -195,7 +206,7 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
       return launch_decode(x, static_cast<int>(xtype), nullptr, Wq, Wd, y, nullptr, M, N, K, dev,
                            stream);
     }));
-  const size_t need = tensor_ws_bytes(M, N, K);
+  const size_t need = p == Q8_PATH_BATCH ? batch_ws_bytes(M, K) : tensor_ws_bytes(M, N, K);
   if (library_ws) {
     if ((st = library_workspace(dev, stream, need, &ws)) != Q8_OK) return st;
   } else {
@@ -203,6 +214,11 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
     if (!aligned16(ws)) return Q8_ERR_ALIGN;
     if (ws_bytes < need) return Q8_ERR_NOMEM;
   }
+  if (p == Q8_PATH_BATCH)
+    return launch_status(timed_launch(stream, [&] {
+      return launch_batch(x, static_cast<int>(xtype), nullptr, Wq, Wd, y, nullptr, M, N, K, ws, dev,
+                          stream);
+    }));
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   uint16_t* A16 = reinterpret_cast<uint16_t*>(w8);
   float* xd = reinterpret_cast<float*>(w8 + align256(static_cast<size_t>(M) * K * 2));
@@ -264,14 +280,16 @@ size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path) {
   DeviceInfo dev;
   if (current_device(&dev) != Q8_OK) return 0;
   q8_path p;
-  if (resolve_path(M, K, path, dev, &p) != Q8_OK) return 0;
+  if (resolve_path(M, N, K, path, dev, &p) != Q8_OK) return 0;
   if (p == Q8_PATH_DECODE || M == 0 || N == 0 || K == 0) return 0;
-  return tensor_ws_bytes(M, N, K);
+  return p == Q8_PATH_BATCH ? batch_ws_bytes(M, K) : tensor_ws_bytes(M, N, K);
 }
 
 q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64_t M, int64_t N,
                         int64_t K, q8_path path, cudaStream_t stream) {
-  if (path != Q8_PATH_AUTO && path != Q8_PATH_DECODE && path != Q8_PATH_TENSOR) return Q8_ERR_DTYPE;
+  if (path != Q8_PATH_AUTO && path != Q8_PATH_DECODE && path != Q8_PATH_TENSOR &&
+      path != Q8_PATH_BATCH)
+    return Q8_ERR_DTYPE;
   q8_status st = check_shape(M, N, K);
   if (st != Q8_OK) return st;
   if ((M * K > 0 && xq == nullptr) || (N * K > 0 && Wq == nullptr) || (M * N * K > 0 && isum == nullptr))
@@ -280,11 +298,17 @@ q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64
   DeviceInfo dev;
   if ((st = current_device(&dev)) != Q8_OK) return st;
   q8_path p;
-  if ((st = resolve_path(M, K, path, dev, &p)) != Q8_OK) return st;
+  if ((st = resolve_path(M, N, K, path, dev, &p)) != Q8_OK) return st;
   if (M == 0 || N == 0 || K == 0) return Q8_OK;
   if (p == Q8_PATH_DECODE)
     return launch_status(
         launch_decode(nullptr, 0, xq, Wq, nullptr, nullptr, isum, M, N, K, dev, stream));
+  if (p == Q8_PATH_BATCH) {
+    void* wsb = nullptr;
+    if ((st = library_workspace(dev, stream, batch_ws_bytes(M, K), &wsb)) != Q8_OK) return st;
+    return launch_status(
+        launch_batch(nullptr, 0, xq, Wq, nullptr, nullptr, isum, M, N, K, wsb, dev, stream));
+  }
   const size_t need = align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(N) * K * 2);
   void* ws = nullptr;
   if ((st = library_workspace(dev, stream, need, &ws)) != Q8_OK) return st;

@@ -1,0 +1,570 @@
+// q8_batch.cu -- batched-decode Q8_0 linear (2 <= M <= 64 tokens): streams the weights from
+// HBM once, forms the exact int32 block sums on the mma.sync tensor path, rescales in
+// registers.
+//
+// Operation: y[m,n] = sum_b Wd[n,b] * xd[m,b] * isum[m,n,b], the Q8_0 int8 GEMM of
+// "CUDA inference engine for running Qwen3.5/3.6 hybrid models on mining cards
+// (CMP 100-210)" (news.hada.io topic 29953, list of un-throttled paths: the DP4A int8
+// GEMM), at batched-decode sizes, where reading the weights still dominates but one dp4a
+// per 4 MACs and token is too slow.
+//
+// Exact block sums.  The int8 codes enter mma.sync.m16n8k16 (binary16 in, binary32
+// accumulate) as binary16 values: |q| <= 127 is exact, each product is exact, and every
+// partial sum of one 32-element block is an integer below 2^24, exact in binary32.  Two
+// MMAs from zero give the block sum.  The K order inside a block does not matter for an
+// exact sum, so A and B only have to agree on it: lane (g, c) of the warp (g = lane / 4,
+// c = lane % 4) supplies K positions {4c..4c+3} to the first MMA and {16+4c..16+4c+3} to
+// the second, in fragment slots (2c, 2c+1) and (2c+8, 2c+9).
+//
+// Design (one CTA per 16 * RG weight rows, 1 producer warp + 16 consumer warps):
+//   * the CTA's weight rows stream through a ring of 256-wide K chunks: two TMA boxes of
+//     16 RG rows x 128 int8 codes with 128-byte swizzle (so ldmatrix reads them without
+//     bank conflicts), one box of the rows' 8 binary16 scales, and the chunk's activation
+//     codes and scales by bulk copies;
+//   * the activations arrive from quantize_batch_kernel in a fragment-ordered layout,
+//     xb[b][m][32] binary16 (for each 16-byte piece c: K 4c..4c+3 then K 16+4c..16+4c+3)
+//     and xbd[b][m] binary32, so each lane's B fragments of one block are one 16-byte load;
+//   * consumer warp w works on row group rg = w % RG (16 rows) and a share of the token
+//     groups (8 tokens each); when token groups are fewer than the warps of a row group,
+//     the warps split the chunk's 8 blocks instead and their partial sums are added in
+//     shared memory at the end;
+//   * per block and 16 x 8 tile: ldmatrix.x4 of the weight codes (shared by the warp's token
+//     groups), widening to binary16, one 16-byte load of activation codes, two MMAs, then
+//     y_acc += (Wd * xd) * S in binary32 registers;
+//   * programmatic dependent launch: the producer loads the first stages' weights before
+//     waiting for the previous kernel (the activation quantizer), then their activations.
+//   * Block-sum mode (for checking) stores the MMA results as int32 instead.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "q8_internal.h"
+#include "q8_ptx.cuh"
+#include "q8_quant_dev.cuh"
+
+namespace q8 {
+namespace {
+
+constexpr int kChunkK = 256;                 // K per stage
+constexpr int kChunkBlocks = kChunkK / kQK;  // 8 Q8_0 blocks
+constexpr int kConsumerWarps = 16;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kMaxTG = kBatchMaxM / 8;       // token groups of 8
+constexpr int kMaxRG = 16;                   // 16 * RG rows <= 256, the TMA box limit
+constexpr int kMaxStages = 8;
+constexpr int kRingTarget = 192 * 1024;
+
+struct BatchParams {
+  const uint16_t* xb;   // [nb][M][32] binary16 codes, fragment order
+  const float* xbd;     // [nb][M] scales
+  float* y;             // [M,N]
+  int32_t* isum;        // [M,N,nb] (block-sum mode)
+  int M, N, K;
+  int RG;               // row groups of 16 per CTA
+  int KPall;            // partial-sum layers (block splits) of the busiest row group
+  int stages;
+  uint32_t stage_bytes;
+  uint32_t off_w1, off_wd, off_x, off_xd;  // offsets inside a stage
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// 4 int8 codes -> 2 half2 (bytes 0,1 and bytes 2,3), exactly: byte b = q + 128 goes under
+// the binary16 exponent of 1024 (0x6400 | b = 1024 + b), then 1152 = 1024 + 128 is
+// subtracted; all values are small integers, nothing rounds.
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t magic = 0x64646464u;
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(a) : "r"(u), "r"(magic));
+  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(b) : "r"(u), "r"(magic));
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  lo = *reinterpret_cast<const uint32_t*>(&ha);
+  hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A (16 x 16, row) * B (16 x 8, col) + C, binary16 in, binary32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <bool kBlockSums>
+__global__ void __launch_bounds__(kThreads, 1)
+    batch_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
+                 const BatchParams p) {
+  pdl_launch_dependents();
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M = p.M, N = p.N, K = p.K, RG = p.RG, S = p.stages;
+  const int nb = K / kQK;
+  const int nchunks = K / kChunkK;
+  const int rows = 16 * RG;
+  const int row0 = blockIdx.x * rows;
+  const int TG = (M + 7) >> 3;
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* ring = smem_raw + (((raw + 1023) & ~1023u) - raw);
+
+  if (S > kMaxStages || S < 2 || RG < 1 || RG > kMaxRG || M < 1 || M > kBatchMaxM) {
+    if (threadIdx.x == 0) report_error(p.err, kErrBadLaunch, nullptr);  // the launcher never does this
+    return;
+  }
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    fence_barrier_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmS);
+  }
+  __syncthreads();
+
+  const uint32_t wbytes = static_cast<uint32_t>(rows) * (2 * 128 + kChunkBlocks * 2);
+  const uint32_t xbytes = static_cast<uint32_t>(kChunkBlocks * M) * (64 + 4);
+
+  if (warp == 0) {
+    // ---------------- producer ---------------------------------------------------------
+    if (lane == 0) {
+      auto load_w = [&](int st) {
+        uint8_t* stg = ring + static_cast<size_t>(st % S) * p.stage_bytes;
+        uint64_t* bar = &full_bar[st % S];
+        tma_load_2d(stg, &tmW, bar, st * kChunkK, row0);
+        tma_load_2d(stg + p.off_w1, &tmW, bar, st * kChunkK + 128, row0);
+        tma_load_2d(stg + p.off_wd, &tmS, bar, st * kChunkBlocks, row0);
+      };
+      auto load_x = [&](int st) {
+        uint8_t* stg = ring + static_cast<size_t>(st % S) * p.stage_bytes;
+        uint64_t* bar = &full_bar[st % S];
+        const size_t blk0 = static_cast<size_t>(st) * kChunkBlocks * M;
+        bulk_load(stg + p.off_x, p.xb + blk0 * 32, static_cast<uint32_t>(kChunkBlocks * M) * 64, bar);
+        bulk_load(stg + p.off_xd, p.xbd + blk0, static_cast<uint32_t>(kChunkBlocks * M) * 4, bar);
+      };
+      // weights of the first stages before waiting for the previous kernel, activations after
+      const int pre = nchunks < S ? nchunks : S;
+      for (int st = 0; st < pre; ++st) {
+        mbar_arrive_expect_tx(&full_bar[st], wbytes + xbytes);
+        load_w(st);
+      }
+      pdl_wait();
+      for (int st = 0; st < pre; ++st) load_x(st);
+      int issued = pre;
+      for (int st = pre; st < nchunks; ++st) {
+        const int s = st % S;
+        if (!mbar_wait(&empty_bar[s], ((st / S) & 1) ^ 1, &abort_flag)) {
+          report_error(p.err, kErrWaitTimeout, &abort_flag);
+          break;
+        }
+        mbar_arrive_expect_tx(&full_bar[s], wbytes + xbytes);
+        load_w(st);
+        load_x(st);
+        issued = st + 1;
+      }
+      // never leave with copies in flight
+      for (int st = (issued > S ? issued - S : 0); st < issued; ++st)
+        if (!mbar_wait(&full_bar[st % S], (st / S) & 1, nullptr)) {
+          report_error(p.err, kErrWaitTimeout, nullptr);
+          break;
+        }
+    }
+  } else {
+    // ---------------- consumers --------------------------------------------------------
+    const int cw = warp - 1;
+    pdl_wait();  // y / isum: wait for the previous kernel before writing
+    const int rg = cw % RG;
+    const int idx = cw / RG;
+    const int nw = (kConsumerWarps - 1 - rg) / RG + 1;  // warps of this row group
+    // token groups tg0, tg0 + tgstep, ... (ntg of them); blocks b' = kp (mod KP) of a chunk
+    int tg0, tgstep, ntg, kp, KP;
+    if (TG >= nw) {
+      KP = 1;
+      kp = 0;
+      tg0 = idx;
+      tgstep = nw;
+      ntg = (TG - idx + nw - 1) / nw;
+    } else {
+      KP = nw / TG;
+      if (KP > kChunkBlocks) KP = kChunkBlocks;
+      tg0 = idx % TG;
+      tgstep = TG;
+      kp = idx / TG;
+      ntg = kp < KP ? 1 : 0;
+    }
+    const int g = lane >> 2, c = lane & 3;
+    // ldmatrix row address of this lane: matrix mi = lane / 8 (0: rows 0-7, 1: rows 8-15 of
+    // the group; 2, 3: the same rows, next 16-byte chunk), row r = lane % 8
+    const int mi = lane >> 3, lr = lane & 7;
+    const int lrow = 16 * rg + lr + 8 * (mi & 1);
+    float acc[kMaxTG][4];
+#pragma unroll
+    for (int i = 0; i < kMaxTG; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+    bool failed = false;
+    for (int st = 0; st < nchunks; ++st) {
+      const int s = st % S;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full_bar[s], (st / S) & 1, &abort_flag))) {
+        if (lane == 0) report_error(p.err, kErrWaitTimeout, &abort_flag);
+        failed = true;
+        break;
+      }
+      const uint8_t* stg = ring + static_cast<size_t>(s) * p.stage_bytes;
+      if (ntg > 0) {
+        const uint16_t* wd = reinterpret_cast<const uint16_t*>(stg + p.off_wd);
+        const uint8_t* xs = stg + p.off_x;
+        const float* xds = reinterpret_cast<const float*>(stg + p.off_xd);
+#pragma unroll 1
+        for (int bp = kp; bp < kChunkBlocks; bp += KP) {
+          const int half = bp >> 2, bq = bp & 3;
+          const int chunk = 2 * bq + (mi >> 1);
+          const uint32_t aaddr = smem_u32(stg + (half ? p.off_w1 : 0u)) +
+                                 static_cast<uint32_t>(lrow * 128 + ((chunk ^ lr) << 4));
+          uint32_t w0, w1, w2, w3;
+          ldmatrix_x4(aaddr, w0, w1, w2, w3);
+          uint32_t a1[4], a2[4];
+          widen4(w0, a1[0], a1[2]);  // row g,     K 4c..4c+3 of the block's first half
+          widen4(w1, a1[1], a1[3]);  // row g + 8
+          widen4(w2, a2[0], a2[2]);  // row g,     K 16+4c..
+          widen4(w3, a2[1], a2[3]);  // row g + 8
+          float dw0 = 0.0f, dw1 = 0.0f;
+          if constexpr (!kBlockSums) {
+            dw0 = __half2float(__ushort_as_half(wd[(16 * rg + g) * kChunkBlocks + bp]));
+            dw1 = __half2float(__ushort_as_half(wd[(16 * rg + g + 8) * kChunkBlocks + bp]));
+          }
+#pragma unroll
+          for (int i = 0; i < kMaxTG; ++i) {
+            if (i < ntg) {
+              const int tg = tg0 + i * tgstep;
+              const int tok = 8 * tg + g;  // B column of this lane (may be >= M: discarded)
+              const uint4 xv =
+                  *reinterpret_cast<const uint4*>(xs + (static_cast<size_t>(bp) * M + tok) * 64 + 16 * c);
+              float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+              mma_16816(d, a1[0], a1[1], a1[2], a1[3], xv.x, xv.y);
+              mma_16816(d, a2[0], a2[1], a2[2], a2[3], xv.z, xv.w);
+              const int t0 = 8 * tg + 2 * c;  // C columns (tokens) of this lane: t0, t0 + 1
+              if constexpr (kBlockSums) {
+                const int b = st * kChunkBlocks + bp;
+                const int n0 = row0 + 16 * rg + g;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int t = t0 + (e & 1), n = n0 + 8 * (e >> 1);
+                  if (t < M && n < N)
+                    p.isum[(static_cast<int64_t>(t) * N + n) * nb + b] = __float2int_rn(d[e]);
+                }
+              } else {
+                const float dx0 = xds[bp * M + (t0 < M ? t0 : 0)];
+                const float dx1 = xds[bp * M + (t0 + 1 < M ? t0 + 1 : 0)];
+                acc[i][0] = fmaf(dw0 * dx0, d[0], acc[i][0]);
+                acc[i][1] = fmaf(dw0 * dx1, d[1], acc[i][1]);
+                acc[i][2] = fmaf(dw1 * dx0, d[2], acc[i][2]);
+                acc[i][3] = fmaf(dw1 * dx1, d[3], acc[i][3]);
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);  // this warp no longer reads the stage
+    }
+    if constexpr (!kBlockSums) {
+      // partial sums [kp][token][row] in the ring (every copy has landed: the consumers
+      // waited for the last stage), then one coalesced pass adds the layers and writes y
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
+      const bool any_fail = wg_barrier_any<32 * kConsumerWarps>(2, failed);
+      if (!any_fail) {
+        float* red = reinterpret_cast<float*>(ring);
+        const int TP = 8 * TG;
+        const int layer = rows * TP;
+        for (int i = threadIdx.x - 32; i < p.KPall * layer; i += 32 * kConsumerWarps) red[i] = 0.0f;
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
+#pragma unroll
+        for (int i = 0; i < kMaxTG; ++i) {
+          if (i < ntg) {
+            const int t0 = 8 * (tg0 + i * tgstep) + 2 * c;
+            float* l = red + kp * layer + t0 * rows + 16 * rg + g;
+            l[0] = acc[i][0];
+            l[rows] = acc[i][1];
+            l[8] = acc[i][2];
+            l[rows + 8] = acc[i][3];
+          }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
+        for (int i = threadIdx.x - 32; i < M * rows; i += 32 * kConsumerWarps) {
+          const int t = i / rows, r = i - t * rows;
+          const int n = row0 + r;
+          if (n < N) {
+            float v = 0.0f;
+            for (int k = 0; k < p.KPall; ++k) v += red[k * layer + t * rows + r];
+            p.y[static_cast<int64_t>(t) * N + n] = v;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Activations -> xb [nb][M][32] binary16 codes in fragment order and xbd [nb][M] scales.
+// Four lanes own one block of one row (8 values each); lane sub holds K 8 sub..8 sub+7 and
+// writes them as two 8-byte halves: K 8 sub..+3 to piece 2 (sub & 1), K 8 sub+4..+7 to
+// piece 2 (sub & 1) + 1, in the piece's first half for sub < 2, second half otherwise.
+// kCodes: the input is int8 codes already (block-sum mode); no scales.
+template <typename InT, bool kCodes>
+__global__ void __launch_bounds__(256) quantize_batch_kernel(const InT* __restrict__ x,
+                                                             uint16_t* __restrict__ xb,
+                                                             float* __restrict__ xbd, int M,
+                                                             int nb) {
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 3;
+  const unsigned group_mask = 0xFu << (lane & ~3);
+  const int64_t nblocks = static_cast<int64_t>(M) * nb;
+  const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 2;
+  for (int64_t blk = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 2;
+       blk < nblocks; blk += stride) {
+    const int m = static_cast<int>(blk / nb);
+    const int b = static_cast<int>(blk - static_cast<int64_t>(m) * nb);
+    const int64_t off = blk * kQK + sub * 8;
+    int q[8];
+    float d = 0.0f;
+    if constexpr (kCodes) {
+      const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const int8_t*>(x) + off);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        q[i] = static_cast<int8_t>((v.x >> (8 * i)) & 0xFFu);
+        q[4 + i] = static_cast<int8_t>((v.y >> (8 * i)) & 0xFFu);
+      }
+    } else {
+      float v[8];
+      if constexpr (sizeof(InT) == 2) {
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(x + off), v);
+      } else {
+        const float4 a = reinterpret_cast<const float4*>(x + off)[0];
+        const float4 c = reinterpret_cast<const float4*>(x + off)[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+      }
+      d = quantize_block_x4(v, group_mask, q);
+    }
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 t = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
+      h[i] = *reinterpret_cast<const uint32_t*>(&t);
+    }
+    uint16_t* dst = xb + (static_cast<int64_t>(b) * M + m) * 32;
+    const int p0 = 2 * (sub & 1), hoff = (sub >> 1) * 4;  // halves: piece p at 8 p, second half +4
+    *reinterpret_cast<uint2*>(dst + 8 * p0 + hoff) = make_uint2(h[0], h[1]);
+    *reinterpret_cast<uint2*>(dst + 8 * (p0 + 1) + hoff) = make_uint2(h[2], h[3]);
+    if constexpr (!kCodes)
+      if (sub == 0) xbd[static_cast<int64_t>(b) * M + m] = d;
+  }
+}
+
+// ---- host ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+struct BatchPlan {
+  int RG = 0, S = 0, grid = 0, KPall = 1;
+  uint32_t stage = 0, off_w1 = 0, off_wd = 0, off_x = 0, off_xd = 0;
+  size_t smem = 0;
+};
+
+uint32_t up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+// The consumers' block split: a row group served by more warps than it has token groups
+// splits each chunk's blocks among them (kp layers).  Must match the kernel's mapping.
+int kp_layers(int RG, int TG) {
+  int all = 1;
+  for (int r = 0; r < RG; ++r) {
+    const int nwr = (kConsumerWarps - 1 - r) / RG + 1;
+    if (TG < nwr) {
+      int k = nwr / TG;
+      if (k > kChunkBlocks) k = kChunkBlocks;
+      if (k > all) all = k;
+    }
+  }
+  return all;
+}
+
+BatchPlan batch_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+  BatchPlan pl;
+  if (M < 1 || M > kBatchMaxM || N < 1 || K < kChunkK || K % kChunkK != 0 || dev.sm_count < 1)
+    return pl;
+  const int64_t groups = (N + 15) / 16;
+  const int64_t RG = (groups + dev.sm_count - 1) / dev.sm_count;
+  if (RG > kMaxRG) return pl;
+  const uint32_t rows = static_cast<uint32_t>(16 * RG);
+  const uint32_t m = static_cast<uint32_t>(M);
+  pl.RG = static_cast<int>(RG);
+  pl.grid = static_cast<int>((groups + RG - 1) / RG);
+  pl.off_w1 = rows * 128;                               // multiple of 2048: swizzle atoms aligned
+  pl.off_wd = 2 * rows * 128;
+  pl.off_x = pl.off_wd + rows * kChunkBlocks * 2;       // 16-byte aligned
+  // fragment reads reach up to 8 tokens past the last block's M rows: pad by 8 tokens
+  pl.off_xd = pl.off_x + (kChunkBlocks * m + 8) * 64;
+  pl.stage = up(pl.off_xd + (kChunkBlocks * m + 8) * 4, 1024);
+  const uint32_t tp = static_cast<uint32_t>(8 * ((M + 7) / 8));
+  pl.KPall = kp_layers(pl.RG, static_cast<int>((M + 7) / 8));
+  const size_t red = static_cast<size_t>(pl.KPall) * rows * tp * 4;  // partial-sum layers
+  const size_t budget = static_cast<size_t>(dev.max_smem_optin) - 2048 - 1024;
+  int S = static_cast<int>((kRingTarget + pl.stage - 1) / pl.stage);
+  if (S < 2) S = 2;
+  if (S > kMaxStages) S = kMaxStages;
+  while (S > 2 && static_cast<size_t>(S) * pl.stage > budget) --S;
+  size_t ring = static_cast<size_t>(S) * pl.stage;
+  if (ring > budget) return BatchPlan{};
+  if (ring < red) ring = red;
+  if (ring > budget) return BatchPlan{};
+  pl.S = S;
+  pl.smem = ring + 1024;
+  return pl;
+}
+
+template <bool kBS>
+cudaError_t launch_batch_kernel(const CUtensorMap& tw, const CUtensorMap& ts, const BatchParams& p,
+                                int grid, size_t smem, cudaStream_t stream) {
+  auto fn = batch_kernel<kBS>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, tw, ts, p);
+}
+
+}  // namespace
+
+bool batch_supported(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+  return batch_plan(M, N, K, dev).smem != 0;
+}
+
+size_t batch_ws_bytes(int64_t M, int64_t K) {
+  const size_t nbm = static_cast<size_t>(K / kQK) * static_cast<size_t>(M);
+  return ((nbm * 64 + 255) & ~static_cast<size_t>(255)) + ((nbm * 4 + 255) & ~static_cast<size_t>(255));
+}
+
+cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const int8_t* Wq,
+                         const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
+                         int64_t K, void* ws, const DeviceInfo& dev, cudaStream_t stream) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  const BatchPlan pl = batch_plan(M, N, K, dev);
+  if (pl.smem == 0 || ws == nullptr) return cudaErrorInvalidValue;
+  const bool bs = isum != nullptr;
+  const int64_t nb = K / kQK;
+  const size_t nbm = static_cast<size_t>(nb) * static_cast<size_t>(M);
+  uint16_t* xb = static_cast<uint16_t*>(ws);
+  float* xbd = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                        ((nbm * 64 + 255) & ~static_cast<size_t>(255)));
+  // 1. activations -> fragment-ordered binary16 codes (+ scales)
+  {
+    const int64_t threads = static_cast<int64_t>(nbm) * 4;
+    int blocks = static_cast<int>((threads + 255) / 256);
+    const int cap = 8 * dev.sm_count;
+    if (blocks > cap) blocks = cap;
+    if (bs)
+      quantize_batch_kernel<int8_t, true><<<blocks, 256, 0, stream>>>(xq_in, xb, xbd,
+                                                                      static_cast<int>(M), static_cast<int>(nb));
+    else if (xtype == 1)
+      quantize_batch_kernel<uint16_t, false><<<blocks, 256, 0, stream>>>(
+          static_cast<const uint16_t*>(x), xb, xbd, static_cast<int>(M), static_cast<int>(nb));
+    else
+      quantize_batch_kernel<float, false><<<blocks, 256, 0, stream>>>(
+          static_cast<const float*>(x), xb, xbd, static_cast<int>(M), static_cast<int>(nb));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // 2. tensor maps of the weight codes and scales; box = the CTA's 16 RG rows
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return cudaErrorInvalidValue;
+  const cuuint32_t rows = static_cast<cuuint32_t>(16 * pl.RG);
+  CUtensorMap tw, ts;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    const cuuint32_t box[2] = {128, rows};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(Wq), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nb), static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nb) * 2};
+    const cuuint32_t box[2] = {kChunkBlocks, rows};
+    const cuuint32_t es[2] = {1, 1};
+    // block-sum mode reads no scales; the map still needs a valid address
+    const void* base = bs ? static_cast<const void*>(Wq) : static_cast<const void*>(Wd);
+    if (enc(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  BatchParams p;
+  p.xb = xb;
+  p.xbd = xbd;
+  p.y = y;
+  p.isum = isum;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.RG = pl.RG;
+  p.KPall = pl.KPall;
+  p.stages = pl.S;
+  p.stage_bytes = pl.stage;
+  p.off_w1 = pl.off_w1;
+  p.off_wd = pl.off_wd;
+  p.off_x = pl.off_x;
+  p.off_xd = pl.off_xd;
+  p.err = dev.err_word;
+  return bs ? launch_batch_kernel<true>(tw, ts, p, pl.grid, pl.smem, stream)
+            : launch_batch_kernel<false>(tw, ts, p, pl.grid, pl.smem, stream);
+}
+
+}  // namespace q8

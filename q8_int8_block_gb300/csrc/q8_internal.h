@@ -39,6 +39,18 @@ cudaError_t launch_decode(const void* x, int xtype, const int8_t* xq_in, const i
                           const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
                           int64_t K, const DeviceInfo& dev, cudaStream_t stream);
 
+// ---- q8_batch.cu ------------------------------------------------------------------
+// Batched decode (2..kBatchMaxM tokens): weight streaming with mma.sync block sums.
+constexpr int kBatchMaxM = 64;
+// True if the batched kernel can run this shape (K % 256 == 0, N small enough, smem).
+bool batch_supported(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
+// Scratch: fragment-ordered binary16 activation codes and their scales.
+size_t batch_ws_bytes(int64_t M, int64_t K);
+// y = linear(x), or (isum != nullptr) the raw block sums of the codes xq_in.
+cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const int8_t* Wq,
+                         const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
+                         int64_t K, void* ws, const DeviceInfo& dev, cudaStream_t stream);
+
 // ---- q8_gemm.cu -------------------------------------------------------------------
 // Tensor-core GEMM on binary16 codes: A16 [M,K] activation codes, B16 [N,K] weight codes,
 // xd [M,K/32] f32, Wd [N,K/32] binary16 bits.  Writes y [M,N] (rescaled sum) or, when

@@ -95,7 +95,10 @@ def _codes(rng, rows, K):
     ("decode", 1, 7, 64), ("decode", 3, 100, 288), ("decode", 8, 33, 4096),
     ("decode", 5, 257, 4128), ("decode", 1, 700, 17408), ("decode", 6, 1500, 4096),
     ("tensor", 16, 256, 512), ("tensor", 130, 300, 96), ("tensor", 1, 1, 32),
-    ("tensor", 257, 513, 160), ("tensor", 3, 40, 4096)])
+    ("tensor", 257, 513, 160), ("tensor", 3, 40, 4096),
+    ("batch", 2, 7, 256), ("batch", 5, 300, 512), ("batch", 16, 1000, 4096), ("batch", 33, 257, 768),
+    ("batch", 64, 2500, 4096), ("batch", 8, 17408, 256), ("batch", 1, 100, 1024),
+    ("batch", 61, 3001, 5120)])
 def test_block_sums_bit_exact(q8, path, M, N, K):
     rng = np.random.default_rng(M * 7 + N)
     xq = _codes(rng, M, K)
@@ -115,7 +118,10 @@ def test_block_sums_bit_exact(q8, path, M, N, K):
     ("decode", 1, 5120, 17408, True), ("decode", 4, 3000, 12288, True), ("decode", 8, 2000, 4096, True),
     ("tensor", 16, 256, 512, False), ("tensor", 130, 300, 96, True), ("tensor", 257, 513, 1056, True),
     ("tensor", 128, 256, 4096, True), ("tensor", 1, 17, 32, True), ("tensor", 200, 100, 4128, False),
-    ("auto", 16, 256, 512, False), ("auto", 1, 256, 512, True)])
+    ("batch", 2, 300, 4096, True), ("batch", 7, 129, 256, False), ("batch", 16, 1000, 512, True),
+    ("batch", 33, 77, 1024, True), ("batch", 64, 2000, 4096, True), ("batch", 17, 40, 17408, True),
+    ("batch", 64, 2432, 256, False), ("batch", 9, 2433, 512, True), ("batch", 1, 5, 256, True),
+    ("auto", 16, 256, 512, False), ("auto", 1, 256, 512, True), ("auto", 40, 256, 1024, True)])
 def test_linear_small_shapes(q8, path, M, N, K, bf16):
     rng = np.random.default_rng(M * 31 + N * 7 + K)
     W = workloads.weights(rng, N, K)
@@ -223,15 +229,24 @@ def test_library_workspace_matches_caller_workspace_and_is_deterministic(q8):
     y3 = q8.q8_linear(xt, Wq, Wd)
     torch.cuda.synchronize()
     assert torch.equal(y1, y2) and torch.equal(y1, y3)
-    for M in (1, 3, 8):
+    for M in (1, 3, 8, 20, 64):
         a = q8.q8_linear(xt[:M].contiguous(), Wq, Wd)
         b = q8.q8_linear(xt[:M].contiguous(), Wq, Wd)
         assert torch.equal(a, b)
+    # the batched path with a caller workspace gives the same bits as with the library's
+    xb = xt[:24].contiguous()
+    ws = torch.empty(q8.q8_linear_workspace_size(24, 700, 2048, "batch"), dtype=torch.uint8,
+                     device="cuda")
+    a = q8.q8_linear_ex(xb, Wq, Wd, path="batch", workspace=ws)
+    b = q8.q8_linear_ex(xb, Wq, Wd, path="batch")
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
 
 
 def test_outputs_stay_inside_their_buffers(q8):
     rng = np.random.default_rng(13)
-    for (M, N, K, path) in ((5, 77, 256, "decode"), (131, 259, 96, "tensor")):
+    for (M, N, K, path) in ((5, 77, 256, "decode"), (131, 259, 96, "tensor"), (13, 77, 256, "batch"),
+                            (64, 3001, 512, "batch")):
         W = workloads.weights(rng, N, K)
         x, _ = workloads.activations(rng, M, K)
         Wq, Wd = q8.q8_quantize_weights(T(W))
@@ -266,3 +281,19 @@ def test_decode_path_rejects_large_m(q8):
     with pytest.raises(q8.Q8Error) as e:
         q8.q8_linear_ex(x, Wq, Wd, path="decode")
     assert e.value.status == 2
+
+
+def test_batch_path_rejects_unsupported_shapes(q8):
+    Wq = torch.zeros((4, 512), dtype=torch.int8, device="cuda")
+    Wd = torch.zeros((4, 16), dtype=torch.int16, device="cuda")
+    with pytest.raises(q8.Q8Error) as e:   # more than 64 tokens
+        q8.q8_linear_ex(torch.zeros((65, 512), dtype=torch.bfloat16, device="cuda"), Wq, Wd,
+                        path="batch")
+    assert e.value.status == 2
+    Wq = torch.zeros((4, 288), dtype=torch.int8, device="cuda")
+    Wd = torch.zeros((4, 9), dtype=torch.int16, device="cuda")
+    with pytest.raises(q8.Q8Error) as e:   # K not a multiple of 256
+        q8.q8_linear_ex(torch.zeros((4, 288), dtype=torch.bfloat16, device="cuda"), Wq, Wd,
+                        path="batch")
+    assert e.value.status == 2
+    assert q8.q8_device_error() == 0
