@@ -239,8 +239,9 @@ def time_graph_steps(torch, q8, step_fns, steps, warmup, instrument=True):
                 f()
         rem = steps % R
         part = None
-        if rem and instrument:
-            q8.q8_set_timing_events(starts, stops)
+        if rem:
+            if instrument:
+                q8.q8_set_timing_events(starts, stops)
             part = torch.cuda.CUDAGraph()
             with torch.cuda.graph(part):
                 for f in step_fns[:rem]:

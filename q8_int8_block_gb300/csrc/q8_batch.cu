@@ -11,12 +11,12 @@
 // Exact block sums.  The int8 codes enter mma.sync.m16n8k16 (binary16 in, binary32
 // accumulate) as binary16 values: |q| <= 127 is exact, each product is exact, and every
 // partial sum of one 32-element block is an integer below 2^24, exact in binary32.  Two
-// MMAs from zero give the block sum.  The K order inside a block does not matter for an
+// MMAs from zero (one per 16-wide half) and their sum give the block sum.  The K order inside a block does not matter for an
 // exact sum, so A and B only have to agree on it: lane (g, c) of the warp (g = lane / 4,
 // c = lane % 4) supplies K positions {4c..4c+3} to the first MMA and {16+4c..16+4c+3} to
 // the second, in fragment slots (2c, 2c+1) and (2c+8, 2c+9).
 //
-// Design (one CTA per 16 * RG weight rows, 1 producer warp + 16 consumer warps):
+// Design (one CTA per 16 * RG weight rows, 1 producer warp + 15 consumer warps):
 //   * the CTA's weight rows stream through a ring of 256-wide K chunks: two TMA boxes of
 //     16 RG rows x 128 int8 codes with 128-byte swizzle (so ldmatrix reads them without
 //     bank conflicts), one box of the rows' 8 binary16 scales, and the chunk's activation
@@ -48,12 +48,15 @@ namespace {
 
 constexpr int kChunkK = 256;                 // K per stage
 constexpr int kChunkBlocks = kChunkK / kQK;  // 8 Q8_0 blocks
-constexpr int kConsumerWarps = 16;
+constexpr int kConsumerWarps = 15;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxTG = kBatchMaxM / 8;       // token groups of 8
-constexpr int kMaxRG = 16;                   // 16 * RG rows <= 256, the TMA box limit
+constexpr int kMaxRG = kConsumerWarps;       // every row group needs a warp (16 * RG <= 256 rows)
 constexpr int kMaxStages = 8;
 constexpr int kRingTarget = 192 * 1024;
+// 16 warps, 4 per SM sub-partition: 4 x 32 x 128 registers fill a sub-partition's 16384
+constexpr int kMaxRegs = 128;
+static_assert((kConsumerWarps + 1 + 3) / 4 * 32 * kMaxRegs <= 16384, "registers per sub-partition");
 
 struct BatchParams {
   const uint16_t* xb;   // [nb][M][32] binary16 codes, fragment order
@@ -90,25 +93,46 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
+// Not volatile: the compiler may schedule it freely after the point where `addr` is known
+// (the callers derive `addr` from a value laundered after the stage's barrier wait).
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
                                             uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+  asm("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(addr));
+}
+
+// Shared-memory loads by 32-bit shared address (not volatile: callers derive the address
+// from a value laundered after the stage's barrier wait).
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float2 lds64f(uint32_t a) {
+  float2 v;
+  asm("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds_f16(uint32_t a) {
+  unsigned short h;
+  asm("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
+  return __half2float(__ushort_as_half(h));
 }
 
 // D = A (16 x 16, row) * B (16 x 8, col) + C, binary16 in, binary32 accumulate.
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1, const float (&c)[4]) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%10, %11, %12, %13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+        "f"(c[2]), "f"(c[3]));
 }
 
-template <bool kBlockSums>
-__global__ void __launch_bounds__(kThreads, 1)
+// kNTG: the most token groups one warp handles (a warp handles ntg <= kNTG of them).
+template <bool kBlockSums, int kNTG>
+__global__ void __maxnreg__(kMaxRegs)
     batch_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
                  const BatchParams p) {
   pdl_launch_dependents();
@@ -143,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 
   const uint32_t wbytes = static_cast<uint32_t>(rows) * (2 * 128 + kChunkBlocks * 2);
-  const uint32_t xbytes = static_cast<uint32_t>(kChunkBlocks * M) * (64 + 4);
+  const uint32_t xbytes = static_cast<uint32_t>(kChunkBlocks * 8 * TG) * (64 + 4);
 
   if (warp == 0) {
     // ---------------- producer ---------------------------------------------------------
@@ -158,9 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_x = [&](int st) {
         uint8_t* stg = ring + static_cast<size_t>(st % S) * p.stage_bytes;
         uint64_t* bar = &full_bar[st % S];
-        const size_t blk0 = static_cast<size_t>(st) * kChunkBlocks * M;
-        bulk_load(stg + p.off_x, p.xb + blk0 * 32, static_cast<uint32_t>(kChunkBlocks * M) * 64, bar);
-        bulk_load(stg + p.off_xd, p.xbd + blk0, static_cast<uint32_t>(kChunkBlocks * M) * 4, bar);
+        const size_t blk0 = static_cast<size_t>(st) * kChunkBlocks * (8 * TG);
+        bulk_load(stg + p.off_x, p.xb + blk0 * 32, static_cast<uint32_t>(kChunkBlocks * 8 * TG) * 64, bar);
+        bulk_load(stg + p.off_xd, p.xbd + blk0, static_cast<uint32_t>(kChunkBlocks * 8 * TG) * 4, bar);
       };
       // weights of the first stages before waiting for the previous kernel, activations after
       const int pre = nchunks < S ? nchunks : S;
@@ -217,11 +241,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the group; 2, 3: the same rows, next 16-byte chunk), row r = lane % 8
     const int mi = lane >> 3, lr = lane & 7;
     const int lrow = 16 * rg + lr + 8 * (mi & 1);
-    float acc[kMaxTG][4];
-#pragma unroll
-    for (int i = 0; i < kMaxTG; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
     bool failed = false;
-    for (int st = 0; st < nchunks; ++st) {
+    const int TP = 8 * TG;  // tokens padded to whole groups of 8
+    float2 acc[kNTG][2];    // (row g, tokens t0, t0+1), (row g+8, tokens t0, t0+1)
+#pragma unroll
+    for (int i = 0; i < kNTG; ++i) acc[i][0] = acc[i][1] = make_float2(0.0f, 0.0f);
+    if (ntg > kNTG) {  // the launcher never does this
+      if (lane == 0) report_error(p.err, kErrBadLaunch, &abort_flag);
+      failed = true;
+    }
+    // per-lane byte offsets inside a stage
+    const uint32_t a_lane = static_cast<uint32_t>(lrow * 128);
+    const uint32_t x_lane = static_cast<uint32_t>(p.off_x + g * 64 + 16 * c);
+    const uint32_t x_block = static_cast<uint32_t>(TP * 64);
+    const uint32_t dx_lane = static_cast<uint32_t>(p.off_xd + 8 * c);
+    const uint32_t wd_lane = static_cast<uint32_t>(p.off_wd + (16 * rg + g) * kChunkBlocks * 2);
+    for (int st = 0; st < nchunks && !failed; ++st) {
       const int s = st % S;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full_bar[s], (st / S) & 1, &abort_flag))) {
         if (lane == 0) report_error(p.err, kErrWaitTimeout, &abort_flag);
@@ -229,55 +264,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const uint8_t* stg = ring + static_cast<size_t>(s) * p.stage_bytes;
+      // the stage's shared-memory address, passed through an empty asm after the wait so
+      // that no load of the stage can be scheduled before the wait
+      uint32_t stg32 = smem_u32(stg);
+      asm volatile("" : "+r"(stg32)::"memory");
       if (ntg > 0) {
-        const uint16_t* wd = reinterpret_cast<const uint16_t*>(stg + p.off_wd);
-        const uint8_t* xs = stg + p.off_x;
-        const float* xds = reinterpret_cast<const float*>(stg + p.off_xd);
-#pragma unroll 1
-        for (int bp = kp; bp < kChunkBlocks; bp += KP) {
-          const int half = bp >> 2, bq = bp & 3;
-          const int chunk = 2 * bq + (mi >> 1);
-          const uint32_t aaddr = smem_u32(stg + (half ? p.off_w1 : 0u)) +
-                                 static_cast<uint32_t>(lrow * 128 + ((chunk ^ lr) << 4));
-          uint32_t w0, w1, w2, w3;
-          ldmatrix_x4(aaddr, w0, w1, w2, w3);
-          uint32_t a1[4], a2[4];
-          widen4(w0, a1[0], a1[2]);  // row g,     K 4c..4c+3 of the block's first half
-          widen4(w1, a1[1], a1[3]);  // row g + 8
-          widen4(w2, a2[0], a2[2]);  // row g,     K 16+4c..
-          widen4(w3, a2[1], a2[3]);  // row g + 8
-          float dw0 = 0.0f, dw1 = 0.0f;
-          if constexpr (!kBlockSums) {
-            dw0 = __half2float(__ushort_as_half(wd[(16 * rg + g) * kChunkBlocks + bp]));
-            dw1 = __half2float(__ushort_as_half(wd[(16 * rg + g + 8) * kChunkBlocks + bp]));
+        // this warp's blocks of the chunk: kp, kp + KP, ...; two at a time, so that the
+        // shared-memory loads and MMAs of both are in flight together
+        const int nmine = (kChunkBlocks - kp + KP - 1) / KP;
+        for (int j = 0; j < nmine; j += 2) {
+          const bool two = j + 1 < nmine;
+          const int bpa = kp + j * KP;
+          const int bpb = two ? bpa + KP : bpa;
+          uint32_t a1[2][4], a2[2][4];
+          float2 dwg[2], dwh[2];  // (Wd, Wd) of rows g and g + 8
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int bp = u ? bpb : bpa;
+            const uint32_t chunk = static_cast<uint32_t>(2 * (bp & 3) + (mi >> 1));
+            const uint32_t aaddr = stg32 + ((bp >> 2) ? p.off_w1 : 0u) + a_lane + ((chunk ^ lr) << 4);
+            uint32_t w0, w1, w2, w3;
+            ldmatrix_x4(aaddr, w0, w1, w2, w3);
+            widen4(w0, a1[u][0], a1[u][2]);  // row g,     K 4c..4c+3 of the block's first half
+            widen4(w1, a1[u][1], a1[u][3]);  // row g + 8
+            widen4(w2, a2[u][0], a2[u][2]);  // row g,     K 16+4c..
+            widen4(w3, a2[u][1], a2[u][3]);  // row g + 8
+            if constexpr (!kBlockSums) {
+              const uint32_t wa = stg32 + wd_lane + 2 * bp;
+              const float f0 = lds_f16(wa);
+              const float f1 = lds_f16(wa + 8 * kChunkBlocks * 2);  // row g + 8
+              dwg[u] = make_float2(f0, f0);
+              dwh[u] = make_float2(f1, f1);
+            }
           }
 #pragma unroll
-          for (int i = 0; i < kMaxTG; ++i) {
+          for (int i = 0; i < kNTG; ++i) {
             if (i < ntg) {
               const int tg = tg0 + i * tgstep;
-              const int tok = 8 * tg + g;  // B column of this lane (may be >= M: discarded)
-              const uint4 xv =
-                  *reinterpret_cast<const uint4*>(xs + (static_cast<size_t>(bp) * M + tok) * 64 + 16 * c);
-              float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-              mma_16816(d, a1[0], a1[1], a1[2], a1[3], xv.x, xv.y);
-              mma_16816(d, a2[0], a2[1], a2[2], a2[3], xv.z, xv.w);
-              const int t0 = 8 * tg + 2 * c;  // C columns (tokens) of this lane: t0, t0 + 1
-              if constexpr (kBlockSums) {
-                const int b = st * kChunkBlocks + bp;
-                const int n0 = row0 + 16 * rg + g;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int t = t0 + (e & 1), n = n0 + 8 * (e >> 1);
-                  if (t < M && n < N)
-                    p.isum[(static_cast<int64_t>(t) * N + n) * nb + b] = __float2int_rn(d[e]);
+              for (int u = 0; u < 2; ++u) {
+                if (u == 1 && !two) break;
+                const int bp = u ? bpb : bpa;
+                // B fragments of token 8 tg + g; tokens are padded to TP with zero codes
+                const uint4 xv = lds128(stg32 + x_lane + bp * x_block + tg * 512);
+                const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                float h[4], d[4];
+                mma_16816(h, a1[u], xv.x, xv.y, z);
+                mma_16816(d, a2[u], xv.z, xv.w, h);  // exact: integers below 2^24
+                if constexpr (kBlockSums) {
+                  const int b = st * kChunkBlocks + bp;
+                  const int n0 = row0 + 16 * rg + g;
+                  const int t0 = 8 * tg + 2 * c;
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const int t = t0 + (e & 1), n = n0 + 8 * (e >> 1);
+                    if (t < M && n < N)
+                      p.isum[(static_cast<int64_t>(t) * N + n) * nb + b] = __float2int_rn(d[e]);
+                  }
+                } else {
+                  const float2 dx = lds64f(stg32 + dx_lane + (bp * TP + 8 * tg) * 4);
+                  acc[i][0] = __ffma2_rn(__fmul2_rn(dwg[u], dx), make_float2(d[0], d[1]), acc[i][0]);
+                  acc[i][1] = __ffma2_rn(__fmul2_rn(dwh[u], dx), make_float2(d[2], d[3]), acc[i][1]);
                 }
-              } else {
-                const float dx0 = xds[bp * M + (t0 < M ? t0 : 0)];
-                const float dx1 = xds[bp * M + (t0 + 1 < M ? t0 + 1 : 0)];
-                acc[i][0] = fmaf(dw0 * dx0, d[0], acc[i][0]);
-                acc[i][1] = fmaf(dw0 * dx1, d[1], acc[i][1]);
-                acc[i][2] = fmaf(dw1 * dx0, d[2], acc[i][2]);
-                acc[i][3] = fmaf(dw1 * dx1, d[3], acc[i][3]);
               }
             }
           }
@@ -293,19 +341,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool any_fail = wg_barrier_any<32 * kConsumerWarps>(2, failed);
       if (!any_fail) {
         float* red = reinterpret_cast<float*>(ring);
-        const int TP = 8 * TG;
         const int layer = rows * TP;
         for (int i = threadIdx.x - 32; i < p.KPall * layer; i += 32 * kConsumerWarps) red[i] = 0.0f;
         asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
 #pragma unroll
-        for (int i = 0; i < kMaxTG; ++i) {
+        for (int i = 0; i < kNTG; ++i) {
           if (i < ntg) {
             const int t0 = 8 * (tg0 + i * tgstep) + 2 * c;
             float* l = red + kp * layer + t0 * rows + 16 * rg + g;
-            l[0] = acc[i][0];
-            l[rows] = acc[i][1];
-            l[8] = acc[i][2];
-            l[rows + 8] = acc[i][3];
+            l[0] = acc[i][0].x;
+            l[rows] = acc[i][0].y;
+            l[8] = acc[i][1].x;
+            l[rows + 8] = acc[i][1].y;
           }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
@@ -333,21 +380,23 @@ template <typename InT, bool kCodes>
 __global__ void __launch_bounds__(256) quantize_batch_kernel(const InT* __restrict__ x,
                                                              uint16_t* __restrict__ xb,
                                                              float* __restrict__ xbd, int M,
-                                                             int nb) {
+                                                             int TP, int nb) {
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int sub = lane & 3;
   const unsigned group_mask = 0xFu << (lane & ~3);
-  const int64_t nblocks = static_cast<int64_t>(M) * nb;
+  const int64_t nblocks = static_cast<int64_t>(TP) * nb;  // rows M..TP-1 are zero padding
   const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 2;
   for (int64_t blk = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 2;
        blk < nblocks; blk += stride) {
     const int m = static_cast<int>(blk / nb);
     const int b = static_cast<int>(blk - static_cast<int64_t>(m) * nb);
     const int64_t off = blk * kQK + sub * 8;
-    int q[8];
+    int q[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     float d = 0.0f;
-    if constexpr (kCodes) {
+    if (m >= M) {
+      // padding token: zero codes and scale
+    } else if constexpr (kCodes) {
       const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const int8_t*>(x) + off);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -372,12 +421,12 @@ __global__ void __launch_bounds__(256) quantize_batch_kernel(const InT* __restri
       const __half2 t = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
       h[i] = *reinterpret_cast<const uint32_t*>(&t);
     }
-    uint16_t* dst = xb + (static_cast<int64_t>(b) * M + m) * 32;
+    uint16_t* dst = xb + (static_cast<int64_t>(b) * TP + m) * 32;
     const int p0 = 2 * (sub & 1), hoff = (sub >> 1) * 4;  // halves: piece p at 8 p, second half +4
     *reinterpret_cast<uint2*>(dst + 8 * p0 + hoff) = make_uint2(h[0], h[1]);
     *reinterpret_cast<uint2*>(dst + 8 * (p0 + 1) + hoff) = make_uint2(h[2], h[3]);
     if constexpr (!kCodes)
-      if (sub == 0) xbd[static_cast<int64_t>(b) * M + m] = d;
+      if (sub == 0) xbd[static_cast<int64_t>(b) * TP + m] = d;
   }
 }
 
@@ -438,10 +487,9 @@ BatchPlan batch_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
   pl.off_w1 = rows * 128;                               // multiple of 2048: swizzle atoms aligned
   pl.off_wd = 2 * rows * 128;
   pl.off_x = pl.off_wd + rows * kChunkBlocks * 2;       // 16-byte aligned
-  // fragment reads reach up to 8 tokens past the last block's M rows: pad by 8 tokens
-  pl.off_xd = pl.off_x + (kChunkBlocks * m + 8) * 64;
-  pl.stage = up(pl.off_xd + (kChunkBlocks * m + 8) * 4, 1024);
-  const uint32_t tp = static_cast<uint32_t>(8 * ((M + 7) / 8));
+  const uint32_t tp = 8 * ((m + 7) / 8);  // tokens padded to whole groups of 8
+  pl.off_xd = pl.off_x + kChunkBlocks * tp * 64;
+  pl.stage = up(pl.off_xd + kChunkBlocks * tp * 4, 1024);
   pl.KPall = kp_layers(pl.RG, static_cast<int>((M + 7) / 8));
   const size_t red = static_cast<size_t>(pl.KPall) * rows * tp * 4;  // partial-sum layers
   const size_t budget = static_cast<size_t>(dev.max_smem_optin) - 2048 - 1024;
@@ -458,10 +506,10 @@ BatchPlan batch_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
   return pl;
 }
 
-template <bool kBS>
+template <bool kBS, int kNTG>
 cudaError_t launch_batch_kernel(const CUtensorMap& tw, const CUtensorMap& ts, const BatchParams& p,
                                 int grid, size_t smem, cudaStream_t stream) {
-  auto fn = batch_kernel<kBS>;
+  auto fn = batch_kernel<kBS, kNTG>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -485,7 +533,7 @@ bool batch_supported(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
 }
 
 size_t batch_ws_bytes(int64_t M, int64_t K) {
-  const size_t nbm = static_cast<size_t>(K / kQK) * static_cast<size_t>(M);
+  const size_t nbm = static_cast<size_t>(K / kQK) * static_cast<size_t>((M + 7) / 8 * 8);
   return ((nbm * 64 + 255) & ~static_cast<size_t>(255)) + ((nbm * 4 + 255) & ~static_cast<size_t>(255));
 }
 
@@ -497,25 +545,28 @@ cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const in
   if (pl.smem == 0 || ws == nullptr) return cudaErrorInvalidValue;
   const bool bs = isum != nullptr;
   const int64_t nb = K / kQK;
-  const size_t nbm = static_cast<size_t>(nb) * static_cast<size_t>(M);
+  const int64_t TP = (M + 7) / 8 * 8;
+  const size_t nbm = static_cast<size_t>(nb) * static_cast<size_t>(TP);
   uint16_t* xb = static_cast<uint16_t*>(ws);
   float* xbd = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
                                         ((nbm * 64 + 255) & ~static_cast<size_t>(255)));
   // 1. activations -> fragment-ordered binary16 codes (+ scales)
   {
-    const int64_t threads = static_cast<int64_t>(nbm) * 4;
+    const int64_t threads = static_cast<int64_t>(nbm) * 4;  // 4 lanes per block
     int blocks = static_cast<int>((threads + 255) / 256);
     const int cap = 8 * dev.sm_count;
     if (blocks > cap) blocks = cap;
     if (bs)
-      quantize_batch_kernel<int8_t, true><<<blocks, 256, 0, stream>>>(xq_in, xb, xbd,
-                                                                      static_cast<int>(M), static_cast<int>(nb));
+      quantize_batch_kernel<int8_t, true><<<blocks, 256, 0, stream>>>(
+          xq_in, xb, xbd, static_cast<int>(M), static_cast<int>(TP), static_cast<int>(nb));
     else if (xtype == 1)
       quantize_batch_kernel<uint16_t, false><<<blocks, 256, 0, stream>>>(
-          static_cast<const uint16_t*>(x), xb, xbd, static_cast<int>(M), static_cast<int>(nb));
+          static_cast<const uint16_t*>(x), xb, xbd, static_cast<int>(M), static_cast<int>(TP),
+          static_cast<int>(nb));
     else
       quantize_batch_kernel<float, false><<<blocks, 256, 0, stream>>>(
-          static_cast<const float*>(x), xb, xbd, static_cast<int>(M), static_cast<int>(nb));
+          static_cast<const float*>(x), xb, xbd, static_cast<int>(M), static_cast<int>(TP),
+          static_cast<int>(nb));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -563,8 +614,23 @@ cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const in
   p.off_x = pl.off_x;
   p.off_xd = pl.off_xd;
   p.err = dev.err_word;
-  return bs ? launch_batch_kernel<true>(tw, ts, p, pl.grid, pl.smem, stream)
-            : launch_batch_kernel<false>(tw, ts, p, pl.grid, pl.smem, stream);
+  // token groups per warp: at most ceil(TG / warps of a row group)
+  const int TG = static_cast<int>((M + 7) / 8);
+  int ntg_max = 1;
+  for (int r = 0; r < pl.RG; ++r) {
+    const int nwr = (kConsumerWarps - 1 - r) / pl.RG + 1;
+    if (TG >= nwr && (TG + nwr - 1) / nwr > ntg_max) ntg_max = (TG + nwr - 1) / nwr;
+  }
+  if (bs) {
+    if (ntg_max <= 1) return launch_batch_kernel<true, 1>(tw, ts, p, pl.grid, pl.smem, stream);
+    if (ntg_max <= 2) return launch_batch_kernel<true, 2>(tw, ts, p, pl.grid, pl.smem, stream);
+    if (ntg_max <= 4) return launch_batch_kernel<true, 4>(tw, ts, p, pl.grid, pl.smem, stream);
+    return launch_batch_kernel<true, 8>(tw, ts, p, pl.grid, pl.smem, stream);
+  }
+  if (ntg_max <= 1) return launch_batch_kernel<false, 1>(tw, ts, p, pl.grid, pl.smem, stream);
+  if (ntg_max <= 2) return launch_batch_kernel<false, 2>(tw, ts, p, pl.grid, pl.smem, stream);
+  if (ntg_max <= 4) return launch_batch_kernel<false, 4>(tw, ts, p, pl.grid, pl.smem, stream);
+  return launch_batch_kernel<false, 8>(tw, ts, p, pl.grid, pl.smem, stream);
 }
 
 }  // namespace q8
