@@ -16,24 +16,31 @@
 // c = lane % 4) supplies K positions {4c..4c+3} to the first MMA and {16+4c..16+4c+3} to
 // the second, in fragment slots (2c, 2c+1) and (2c+8, 2c+9).
 //
-// Design (one CTA per 16 * RG weight rows, 1 producer warp + 15 consumer warps):
+// Design (one CTA per 16 * RG weight rows, 1 producer warp + 15 consumer warps, so that
+// 16 warps with up to 128 registers each fill an SM):
 //   * the CTA's weight rows stream through a ring of 256-wide K chunks: two TMA boxes of
 //     16 RG rows x 128 int8 codes with 128-byte swizzle (so ldmatrix reads them without
 //     bank conflicts), one box of the rows' 8 binary16 scales, and the chunk's activation
 //     codes and scales by bulk copies;
 //   * the activations arrive from quantize_batch_kernel in a fragment-ordered layout,
-//     xb[b][m][32] binary16 (for each 16-byte piece c: K 4c..4c+3 then K 16+4c..16+4c+3)
-//     and xbd[b][m] binary32, so each lane's B fragments of one block are one 16-byte load;
+//     xb[b][t][32] binary16 (for each 16-byte piece c: K 4c..4c+3 then K 16+4c..16+4c+3)
+//     and xbd[b][t] binary32, tokens padded with zeros to whole groups of 8, so each lane's
+//     B fragments of one block are one 16-byte load;
 //   * consumer warp w works on row group rg = w % RG (16 rows) and a share of the token
 //     groups (8 tokens each); when token groups are fewer than the warps of a row group,
 //     the warps split the chunk's 8 blocks instead and their partial sums are added in
 //     shared memory at the end;
-//   * per block and 16 x 8 tile: ldmatrix.x4 of the weight codes (shared by the warp's token
-//     groups), widening to binary16, one 16-byte load of activation codes, two MMAs, then
-//     y_acc += (Wd * xd) * S in binary32 registers;
+//   * a warp takes its blocks of a chunk up to 4 at a time: ldmatrix.x4 of the weight codes
+//     (shared by the warp's token groups), widening to binary16, one 16-byte load of
+//     activation codes and two MMAs per token group and block, all issued before the
+//     rescale y_acc += (Wd * xd) * S in packed binary32 (f32x2) registers;
 //   * programmatic dependent launch: the producer loads the first stages' weights before
 //     waiting for the previous kernel (the activation quantizer), then their activations.
 //   * Block-sum mode (for checking) stores the MMA results as int32 instead.
+//
+// Measured limits (GB300, 12288 x 4096 weights): weight streaming alone runs at the HBM
+// rate (9 us); the separate quantizer kernel costs ~4 us of each call; at large M the
+// activation chunks (32 KB per 256-wide chunk at M = 64) outweigh the weights in the ring.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -50,7 +57,6 @@ constexpr int kChunkK = 256;                 // K per stage
 constexpr int kChunkBlocks = kChunkK / kQK;  // 8 Q8_0 blocks
 constexpr int kConsumerWarps = 15;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kMaxTG = kBatchMaxM / 8;       // token groups of 8
 constexpr int kMaxRG = kConsumerWarps;       // every row group needs a warp (16 * RG <= 256 rows)
 constexpr int kMaxStages = 8;
 constexpr int kRingTarget = 192 * 1024;
@@ -59,8 +65,8 @@ constexpr int kMaxRegs = 128;
 static_assert((kConsumerWarps + 1 + 3) / 4 * 32 * kMaxRegs <= 16384, "registers per sub-partition");
 
 struct BatchParams {
-  const uint16_t* xb;   // [nb][M][32] binary16 codes, fragment order
-  const float* xbd;     // [nb][M] scales
+  const uint16_t* xb;   // [nb][TP][32] binary16 codes, fragment order
+  const float* xbd;     // [nb][TP] scales
   float* y;             // [M,N]
   int32_t* isum;        // [M,N,nb] (block-sum mode)
   int M, N, K;
@@ -197,7 +203,7 @@ __global__ void __maxnreg__(kMaxRegs)
       int issued = pre;
       for (int st = pre; st < nchunks; ++st) {
         const int s = st % S;
-        if (!mbar_wait(&empty_bar[s], ((st / S) & 1) ^ 1, &abort_flag)) {
+        if (!mbar_wait_sleep(&empty_bar[s], ((st / S) & 1) ^ 1, &abort_flag)) {
           report_error(p.err, kErrWaitTimeout, &abort_flag);
           break;
         }
@@ -216,7 +222,7 @@ __global__ void __maxnreg__(kMaxRegs)
   } else {
     // ---------------- consumers --------------------------------------------------------
     const int cw = warp - 1;
-    pdl_wait();  // y / isum: wait for the previous kernel before writing
+    pdl_wait();  // x, y / isum: wait for the previous kernel before reading or writing
     const int rg = cw % RG;
     const int idx = cw / RG;
     const int nw = (kConsumerWarps - 1 - rg) / RG + 1;  // warps of this row group
@@ -256,9 +262,10 @@ __global__ void __maxnreg__(kMaxRegs)
     const uint32_t x_block = static_cast<uint32_t>(TP * 64);
     const uint32_t dx_lane = static_cast<uint32_t>(p.off_xd + 8 * c);
     const uint32_t wd_lane = static_cast<uint32_t>(p.off_wd + (16 * rg + g) * kChunkBlocks * 2);
-    for (int st = 0; st < nchunks && !failed; ++st) {
-      const int s = st % S;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full_bar[s], (st / S) & 1, &abort_flag))) {
+    int s = 0;
+    uint32_t phase = 0;  // slot s and parity of stage st, kept without divisions
+    for (int st = 0; st < nchunks && !failed; ++st, s = (s + 1 == S ? 0 : s + 1), phase ^= (s == 0)) {
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(&full_bar[s], phase, &abort_flag))) {
         if (lane == 0) report_error(p.err, kErrWaitTimeout, &abort_flag);
         failed = true;
         break;
@@ -272,59 +279,80 @@ __global__ void __maxnreg__(kMaxRegs)
         // this warp's blocks of the chunk: kp, kp + KP, ...; two at a time, so that the
         // shared-memory loads and MMAs of both are in flight together
         const int nmine = (kChunkBlocks - kp + KP - 1) / KP;
-        for (int j = 0; j < nmine; j += 2) {
-          const bool two = j + 1 < nmine;
-          const int bpa = kp + j * KP;
-          const int bpb = two ? bpa + KP : bpa;
-          uint32_t a1[2][4], a2[2][4];
-          float2 dwg[2], dwh[2];  // (Wd, Wd) of rows g and g + 8
+        // kGB of this warp's blocks at a time: all their shared-memory loads and MMAs are
+        // issued before any result is used (the chains are long-latency: ldmatrix, MMA, FMA);
+        // slots past the last block repeat it and are not accumulated
+        constexpr int kGB = kNTG <= 2 ? 4 : 2;
+        for (int j0 = 0; j0 < nmine; j0 += kGB) {
+          int bps[kGB];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int bp = u ? bpb : bpa;
+          for (int k = 0; k < kGB; ++k) bps[k] = kp + (j0 + k < nmine ? j0 + k : nmine - 1) * KP;
+          uint32_t wa[kGB][4];
+#pragma unroll
+          for (int k = 0; k < kGB; ++k) {
+            const int bp = bps[k];
             const uint32_t chunk = static_cast<uint32_t>(2 * (bp & 3) + (mi >> 1));
-            const uint32_t aaddr = stg32 + ((bp >> 2) ? p.off_w1 : 0u) + a_lane + ((chunk ^ lr) << 4);
-            uint32_t w0, w1, w2, w3;
-            ldmatrix_x4(aaddr, w0, w1, w2, w3);
-            widen4(w0, a1[u][0], a1[u][2]);  // row g,     K 4c..4c+3 of the block's first half
-            widen4(w1, a1[u][1], a1[u][3]);  // row g + 8
-            widen4(w2, a2[u][0], a2[u][2]);  // row g,     K 16+4c..
-            widen4(w3, a2[u][1], a2[u][3]);  // row g + 8
+            ldmatrix_x4(stg32 + ((bp >> 2) ? p.off_w1 : 0u) + a_lane + ((chunk ^ lr) << 4), wa[k][0],
+                        wa[k][1], wa[k][2], wa[k][3]);
+          }
+          float dw0[kGB], dw1[kGB];  // Wd of rows g and g + 8
+#pragma unroll
+          for (int k = 0; k < kGB; ++k) {
+            dw0[k] = dw1[k] = 0.0f;
             if constexpr (!kBlockSums) {
-              const uint32_t wa = stg32 + wd_lane + 2 * bp;
-              const float f0 = lds_f16(wa);
-              const float f1 = lds_f16(wa + 8 * kChunkBlocks * 2);  // row g + 8
-              dwg[u] = make_float2(f0, f0);
-              dwh[u] = make_float2(f1, f1);
+              const uint32_t wda = stg32 + wd_lane + 2 * bps[k];
+              dw0[k] = lds_f16(wda);
+              dw1[k] = lds_f16(wda + 8 * kChunkBlocks * 2);
             }
           }
+          {
+            uint32_t a1[kGB][4], a2[kGB][4];
 #pragma unroll
-          for (int i = 0; i < kNTG; ++i) {
-            if (i < ntg) {
-              const int tg = tg0 + i * tgstep;
+            for (int k = 0; k < kGB; ++k) {
+              widen4(wa[k][0], a1[k][0], a1[k][2]);  // row g,     K 4c..4c+3 of the block's first half
+              widen4(wa[k][1], a1[k][1], a1[k][3]);  // row g + 8
+              widen4(wa[k][2], a2[k][0], a2[k][2]);  // row g,     K 16+4c..
+              widen4(wa[k][3], a2[k][1], a2[k][3]);  // row g + 8
+            }
 #pragma unroll
-              for (int u = 0; u < 2; ++u) {
-                if (u == 1 && !two) break;
-                const int bp = u ? bpb : bpa;
-                // B fragments of token 8 tg + g; tokens are padded to TP with zero codes
-                const uint4 xv = lds128(stg32 + x_lane + bp * x_block + tg * 512);
-                const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                float h[4], d[4];
-                mma_16816(h, a1[u], xv.x, xv.y, z);
-                mma_16816(d, a2[u], xv.z, xv.w, h);  // exact: integers below 2^24
-                if constexpr (kBlockSums) {
-                  const int b = st * kChunkBlocks + bp;
-                  const int n0 = row0 + 16 * rg + g;
-                  const int t0 = 8 * tg + 2 * c;
+            for (int i = 0; i < kNTG; ++i) {
+              if (i < ntg) {
+                const int tg = tg0 + i * tgstep;
+                uint4 xv[kGB];
+                float d[kGB][4];
 #pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    const int t = t0 + (e & 1), n = n0 + 8 * (e >> 1);
-                    if (t < M && n < N)
-                      p.isum[(static_cast<int64_t>(t) * N + n) * nb + b] = __float2int_rn(d[e]);
+                for (int k = 0; k < kGB; ++k)  // B fragments of token 8 tg + g (tokens padded to TP)
+                  xv[k] = lds128(stg32 + x_lane + bps[k] * x_block + tg * 512);
+#pragma unroll
+                for (int k = 0; k < kGB; ++k) {
+                  if (j0 + k < nmine) {
+                    const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    float h[4];
+                    mma_16816(h, a1[k], xv[k].x, xv[k].y, z);
+                    mma_16816(d[k], a2[k], xv[k].z, xv[k].w, h);  // exact: integers below 2^24
                   }
-                } else {
-                  const float2 dx = lds64f(stg32 + dx_lane + (bp * TP + 8 * tg) * 4);
-                  acc[i][0] = __ffma2_rn(__fmul2_rn(dwg[u], dx), make_float2(d[0], d[1]), acc[i][0]);
-                  acc[i][1] = __ffma2_rn(__fmul2_rn(dwh[u], dx), make_float2(d[2], d[3]), acc[i][1]);
+                }
+#pragma unroll
+                for (int k = 0; k < kGB; ++k) {
+                  if (j0 + k < nmine) {
+                    if constexpr (kBlockSums) {
+                      const int b = st * kChunkBlocks + bps[k];
+                      const int n0 = row0 + 16 * rg + g;
+                      const int t0 = 8 * tg + 2 * c;
+#pragma unroll
+                      for (int e = 0; e < 4; ++e) {
+                        const int t = t0 + (e & 1), n = n0 + 8 * (e >> 1);
+                        if (t < M && n < N)
+                          p.isum[(static_cast<int64_t>(t) * N + n) * nb + b] = __float2int_rn(d[k][e]);
+                      }
+                    } else {
+                      const float2 dx = lds64f(stg32 + dx_lane + (bps[k] * TP + 8 * tg) * 4);
+                      acc[i][0] = __ffma2_rn(__fmul2_rn(make_float2(dw0[k], dw0[k]), dx),
+                                             make_float2(d[k][0], d[k][1]), acc[i][0]);
+                      acc[i][1] = __ffma2_rn(__fmul2_rn(make_float2(dw1[k], dw1[k]), dx),
+                                             make_float2(d[k][2], d[k][3]), acc[i][1]);
+                    }
+                  }
                 }
               }
             }
@@ -415,16 +443,19 @@ __global__ void __launch_bounds__(256) quantize_batch_kernel(const InT* __restri
       }
       d = quantize_block_x4(v, group_mask, q);
     }
-    uint32_t h[4];
+    const int p0 = 2 * (sub & 1);
+    {
+      uint32_t h[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __half2 t = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
-      h[i] = *reinterpret_cast<const uint32_t*>(&t);
+      for (int i = 0; i < 4; ++i) {
+        const __half2 t = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
+        h[i] = *reinterpret_cast<const uint32_t*>(&t);
+      }
+      uint16_t* dst = xb + (static_cast<int64_t>(b) * TP + m) * 32;
+      const int hoff = (sub >> 1) * 4;  // halves: piece p at 8 p, second half +4
+      *reinterpret_cast<uint2*>(dst + 8 * p0 + hoff) = make_uint2(h[0], h[1]);
+      *reinterpret_cast<uint2*>(dst + 8 * (p0 + 1) + hoff) = make_uint2(h[2], h[3]);
     }
-    uint16_t* dst = xb + (static_cast<int64_t>(b) * TP + m) * 32;
-    const int p0 = 2 * (sub & 1), hoff = (sub >> 1) * 4;  // halves: piece p at 8 p, second half +4
-    *reinterpret_cast<uint2*>(dst + 8 * p0 + hoff) = make_uint2(h[0], h[1]);
-    *reinterpret_cast<uint2*>(dst + 8 * (p0 + 1) + hoff) = make_uint2(h[2], h[3]);
     if constexpr (!kCodes)
       if (sub == 0) xbd[static_cast<int64_t>(b) * TP + m] = d;
   }
@@ -550,7 +581,7 @@ cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const in
   uint16_t* xb = static_cast<uint16_t*>(ws);
   float* xbd = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
                                         ((nbm * 64 + 255) & ~static_cast<size_t>(255)));
-  // 1. activations -> fragment-ordered binary16 codes (+ scales)
+  // 1. activations -> fragment-ordered binary16 codes and scales
   {
     const int64_t threads = static_cast<int64_t>(nbm) * 4;  // 4 lanes per block
     int blocks = static_cast<int>((threads + 255) / 256);

@@ -66,6 +66,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete yet sleeps in
+// hardware until the phase completes or about `ns` nanoseconds pass, instead of spinning on
+// issue slots that the working warps of its SM sub-partition need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait for warps that may wait long while other warps of their SM work: after the
+// first test it sleeps between tests (bounded like mbar_wait).
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (clock64() - t0 > kWaitBudgetCycles) return false;
+  }
+}
+
 // Waits for the phase with the given parity to complete.  Returns false if the cycle
 // budget ran out or another thread of the CTA already flagged an abort.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
