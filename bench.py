@@ -271,8 +271,8 @@ def time_graph_steps(torch, q8, step_fns, steps, warmup, instrument=True):
     return total, kern
 
 
-def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=False):
-    wname, p, mi = CASES[name]
+def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=False, spec=None):
+    wname, p, mi = spec if spec is not None else CASES[name]
     wl = workloads.WORKLOADS[wname]
     W = wl.make_weights(p)
     x_np, _ = wl.make_act(p, mi)
@@ -546,6 +546,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=sorted(CASES), default="decode_m1",
                     help="which configured shape to time (default: decode GEMV, M=1)")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every point of the dense-layer sweep workload (one GPU) and exit")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     a = ap.parse_args(argv)
@@ -556,8 +558,50 @@ def parse_args(argv=None):
     return a
 
 
+def sweep_arm(args):
+    """Every (projection, M) point of the dense-layer sweep workload, each timed like the
+    headline workload (graph replays, rotating weight copies > 2 x L2), with its roofline
+    fraction against max(bytes / HBM, ops / tensor peak).  One JSON line with all points."""
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__ as g
+    g.build()
+    import q8_int8_block_gb300 as q8
+    pk, pk_src = peaks()
+    dev = torch.device("cuda", 0)
+    wl = workloads.WORKLOADS["sweep"]
+    points = []
+    seen = set()
+    for p, proj in enumerate(wl.projections):
+        if (proj.K, proj.N) in seen:  # q, k, v, o share one shape
+            continue
+        seen.add((proj.K, proj.N))
+        for mi, M in enumerate(wl.Ms):
+            ops = workloads.algorithmic_ops(M, proj.N, proj.K)
+            steps = max(20, min(2000, int(2e12 / max(ops, 1))))
+            r = run_case(torch, q8, dev, f"sweep_{proj.name}_m{M}", steps, max(3, steps // 20), pk,
+                         pk_src, spec=("sweep", p, mi))
+            b = workloads.algorithmic_bytes(M, proj.N, proj.K, x_bytes=r["xsize"])
+            t = r["t_max"] / steps
+            t_roof = max(b / (pk["hbm_gbs"] * 1e9), ops / (pk["bf16_tflops"] * 1e12))
+            points.append({"projection": proj.name, "K": proj.K, "N": proj.N, "M": M,
+                           "path": r["path"], "us_per_call": round(t * 1e6, 3),
+                           "GBps": round(b / t / 1e9, 1), "TOPS": round(ops / t / 1e12, 2),
+                           "bound": "hbm" if b / (pk["hbm_gbs"] * 1e9) >= ops / (pk["bf16_tflops"] * 1e12)
+                           else "tensor",
+                           "roofline_frac": round(t_roof / t, 4)})
+    return {"metric": METRIC, "sweep": "dense-layer sweep, hidden 5120 (q/k/v/o 5120x5120, "
+            "gate/up 5120x17408, down 17408x5120, GDN in-proj 5120x10240)",
+            "time": "whole call per step (all kernels of the path), CUDA graph replays",
+            "peaks": {k: pk[k] for k in ("hbm_gbs", "bf16_tflops")}, "peak_source": pk_src,
+            "points": points, "device_error_word": q8.q8_device_error()}
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.sweep:
+        print(json.dumps(sweep_arm(args)), flush=True)
+        return
     if args.impl == "reference":
         rank, line = reference_arm(args)
     else:

@@ -111,10 +111,12 @@ q8_status resolve_path(int64_t M, int64_t N, int64_t K, q8_path req, const Devic
   }
 }
 
-// Scratch of the tensor path: A16 [M,K] f16 codes, xd [M,K/32] f32, B16 [N,K] f16 codes.
-size_t tensor_ws_bytes(int64_t M, int64_t N, int64_t K) {
+// Scratch of the tensor path: A16 [M,K] f16 codes, xd [M,K/32] f32, B16 [N,K] f16 codes, and
+// with split-K the partial outputs [splits,M,N] f32.
+size_t tensor_ws_bytes(int64_t M, int64_t N, int64_t K, int splits) {
   return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(M) * (K / kQK) * 4) +
-         align256(static_cast<size_t>(N) * K * 2);
+         align256(static_cast<size_t>(N) * K * 2) +
+         (splits > 1 ? align256(static_cast<size_t>(splits) * M * N * 4) : 0);
 }
 
 // Library-owned scratch for (current device, stream), grown on demand.
@@ -206,7 +208,8 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
       return launch_decode(x, static_cast<int>(xtype), nullptr, Wq, Wd, y, nullptr, M, N, K, dev,
                            stream);
     }));
-  const size_t need = p == Q8_PATH_BATCH ? batch_ws_bytes(M, K) : tensor_ws_bytes(M, N, K);
+  const int splits = gemm_splits(M, N, K, dev);
+  const size_t need = p == Q8_PATH_BATCH ? batch_ws_bytes(M, K) : tensor_ws_bytes(M, N, K, splits);
   if (library_ws) {
     if ((st = library_workspace(dev, stream, need, &ws)) != Q8_OK) return st;
   } else {
@@ -224,11 +227,13 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
   float* xd = reinterpret_cast<float*>(w8 + align256(static_cast<size_t>(M) * K * 2));
   uint16_t* B16 = reinterpret_cast<uint16_t*>(w8 + align256(static_cast<size_t>(M) * K * 2) +
                                               align256(static_cast<size_t>(M) * (K / kQK) * 4));
+  float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(B16) +
+                                         align256(static_cast<size_t>(N) * K * 2));
   cudaError_t e = launch_quantize(x, static_cast<int>(xtype), A16, true, xd, false, M, K, dev, stream);
   if (e == cudaSuccess) e = launch_codes_to_f16(Wq, B16, N * K, dev, stream);
   if (e == cudaSuccess)
     e = timed_launch(stream, [&] {
-      return launch_gemm_tc(A16, B16, xd, Wd, y, nullptr, M, N, K, dev, stream);
+      return launch_gemm_tc(A16, B16, xd, Wd, y, nullptr, part, splits, M, N, K, dev, stream);
     });
   return launch_status(e);
 }
@@ -282,7 +287,8 @@ size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path) {
   q8_path p;
   if (resolve_path(M, N, K, path, dev, &p) != Q8_OK) return 0;
   if (p == Q8_PATH_DECODE || M == 0 || N == 0 || K == 0) return 0;
-  return p == Q8_PATH_BATCH ? batch_ws_bytes(M, K) : tensor_ws_bytes(M, N, K);
+  return p == Q8_PATH_BATCH ? batch_ws_bytes(M, K)
+                            : tensor_ws_bytes(M, N, K, gemm_splits(M, N, K, dev));
 }
 
 q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64_t M, int64_t N,
@@ -318,7 +324,7 @@ q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64
   cudaError_t e = launch_codes_to_f16(xq, A16, M * K, dev, stream);
   if (e == cudaSuccess) e = launch_codes_to_f16(Wq, B16, N * K, dev, stream);
   if (e == cudaSuccess)
-    e = launch_gemm_tc(A16, B16, nullptr, nullptr, nullptr, isum, M, N, K, dev, stream);
+    e = launch_gemm_tc(A16, B16, nullptr, nullptr, nullptr, isum, nullptr, 1, M, N, K, dev, stream);
   return launch_status(e);
 }
 

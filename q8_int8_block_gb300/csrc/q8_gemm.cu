@@ -30,6 +30,7 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "q8_internal.h"
@@ -67,6 +68,8 @@ struct GemmParams {
   const float* xd;     // [M, nb]
   const uint16_t* Wd;  // [N, nb]
   float* y;            // [M, N]
+  float* part;         // [splits, M, N] partial outputs (split-K), or nullptr
+  int splits;          // K split into this many ranges of whole scale windows (blockIdx.y)
   int32_t* isum;       // [M, N, nb] (block-sum mode)
   int M, N, K;
   uint32_t* err;
@@ -144,8 +147,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = p.M, N = p.N, K = p.K;
   const int nb = K / kQK;
-  const int nk = (K + BK - 1) / BK;
-  const int nwin = (nb + kWin - 1) / kWin;
+  // split-K: this CTA takes scale windows [w_begin, w_end) of the K range, i.e. Q8_0 blocks
+  // [b_begin, b_end) and 64-wide stages [kb_begin, kb_end); ring slots, TMEM buffers and
+  // barrier phases count from the start of the range
+  const int nwin_all = (nb + kWin - 1) / kWin;
+  const int w_begin = static_cast<int>(static_cast<int64_t>(blockIdx.y) * nwin_all / p.splits);
+  const int w_end = static_cast<int>(static_cast<int64_t>(blockIdx.y + 1) * nwin_all / p.splits);
+  const int b_begin = w_begin * kWin;
+  const int b_end = (w_end * kWin < nb) ? w_end * kWin : nb;
+  const int kb_begin = b_begin / 2;
+  const int kb_end = (b_end + 1) / 2;
   const int mtiles = (M + BM - 1) / BM;
   const int m0 = (blockIdx.x % mtiles) * BM;
   const int n0 = (blockIdx.x / mtiles) * BN;
@@ -188,9 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------- TMA producer -----------------------------------
       if (lane == 0) {
         int issued = 0;
-        for (int kb = 0; kb < nk; ++kb) {
-          const int s = kb % kStages;
-          if (!mbar_wait(&empty_bar[s], ((kb / kStages) & 1) ^ 1, &abort_flag)) {
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
+          const int i = kb - kb_begin;
+          const int s = i % kStages;
+          if (!mbar_wait(&empty_bar[s], ((i / kStages) & 1) ^ 1, &abort_flag)) {
             report_error(p.err, kErrWaitTimeout, &abort_flag);
             break;
           }
@@ -199,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sB + s * kStageB, &tmB, &full_bar[s], kb * BK, n0);
           ++issued;
         }
-        for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb)
-          if (!mbar_wait(&full_bar[kb % kStages], (kb / kStages) & 1, nullptr)) {
+        for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+          if (!mbar_wait(&full_bar[i % kStages], (i / kStages) & 1, nullptr)) {
             report_error(p.err, kErrWaitTimeout, nullptr);
             break;
           }
@@ -210,19 +222,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
         int last_stage = -1;
-        for (int kb = 0; kb < nk; ++kb) {
-          const int s = kb % kStages;
-          if (!mbar_wait(&full_bar[s], (kb / kStages) & 1, &abort_flag)) {
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
+          const int i = kb - kb_begin;
+          const int s = i % kStages;
+          if (!mbar_wait(&full_bar[s], (i / kStages) & 1, &abort_flag)) {
             report_error(p.err, kErrWaitTimeout, &abort_flag);
             break;
           }
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + s * kStageA);
           const uint32_t b0 = smem_u32(sB + s * kStageB);
-          const int nblk = (nb - 2 * kb) < 2 ? (nb - 2 * kb) : 2;
+          const int nblk = (b_end - 2 * kb) < 2 ? (b_end - 2 * kb) : 2;
           bool ok = true;
           for (int j = 0; j < nblk; ++j) {
-            const int blk = 2 * kb + j;
+            const int blk = 2 * kb + j - b_begin;  // block of the range
             const int buf = blk & 1;
             if (!mbar_wait(&tempty_bar[buf], ((blk >> 1) & 1) ^ 1, &abort_flag)) {
               report_error(p.err, kErrWaitTimeout, &abort_flag);
@@ -240,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&tfull_bar[buf]);
           }
           mma_commit(&empty_bar[s]);
-          last_stage = kb;
+          last_stage = i;
           if (!ok) break;
         }
         // do not leave while MMAs are still reading shared memory / writing TMEM
@@ -251,9 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if constexpr (!kBlockSums) {
       // ------------------------------- scale producer (warps 2-3) ---------------------
       const int t = threadIdx.x - 64;  // 0..63
-      for (int w = 0; w < nwin; ++w) {
-        const int slot = w % kWinSlots;
-        if (!mbar_wait(&sempty_bar[slot], ((w / kWinSlots) & 1) ^ 1, &abort_flag)) {
+      for (int w = w_begin; w < w_end; ++w) {
+        const int u = w - w_begin;
+        const int slot = u % kWinSlots;
+        if (!mbar_wait(&sempty_bar[slot], ((u / kWinSlots) & 1) ^ 1, &abort_flag)) {
           report_error(p.err, kErrWaitTimeout, &abort_flag);
           break;
         }
@@ -280,12 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
     }
     bool failed = false;
-    for (int w = 0; w < nwin && !failed; ++w) {
-      const int slot = w % kWinSlots;
+    for (int w = w_begin; w < w_end && !failed; ++w) {
+      const int u = w - w_begin;
+      const int slot = u % kWinSlots;
       const float* dws = sW + slot * kWin * BN + wg * 128;
       const float* dxs = sX + slot * kWin * BM;
       if constexpr (!kBlockSums) {
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sfull_bar[slot], (w / kWinSlots) & 1, &abort_flag))) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sfull_bar[slot], (u / kWinSlots) & 1, &abort_flag))) {
           if (lane == 0) report_error(p.err, kErrWaitTimeout, &abort_flag);
           failed = true;
           break;
@@ -294,9 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nbw = (nb - w * kWin) < kWin ? (nb - w * kWin) : kWin;
 #pragma unroll 1
       for (int bb = 0; bb < nbw; ++bb) {
-        const int blk = w * kWin + bb;
-        const int buf = blk & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull_bar[buf], (blk >> 1) & 1, &abort_flag))) {
+        const int blk = w * kWin + bb;  // absolute block (block-sum output index)
+        const int lb = blk - b_begin;   // block of the range: TMEM buffer and phase
+        const int buf = lb & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull_bar[buf], (lb >> 1) & 1, &abort_flag))) {
           if (lane == 0) report_error(p.err, kErrWaitTimeout, &abort_flag);
           failed = true;
           break;
@@ -363,7 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if constexpr (!kBlockSums) {
       if (m_ok && !failed) {
-        float* yrow = p.y + static_cast<int64_t>(m) * N;
+        float* yrow = (p.part ? p.part + static_cast<int64_t>(blockIdx.y) * M * N : p.y) +
+                      static_cast<int64_t>(m) * N;
         const int nbase = n0 + wg * 128;
         if ((N & 3) == 0 && nbase + 128 <= N) {
 #pragma unroll
@@ -423,6 +440,35 @@ bool make_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t co
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// y = sum over s of part[s] (fixed order: the result does not depend on timing).
+__global__ void __launch_bounds__(256) reduce_splits_kernel(const float4* __restrict__ part,
+                                                            float4* __restrict__ y, int64_t n4,
+                                                            int splits) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 a = part[i];
+    for (int s = 1; s < splits; ++s) {
+      const float4 b = part[static_cast<int64_t>(s) * n4 + i];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    y[i] = a;
+  }
+}
+
+__global__ void __launch_bounds__(256) reduce_splits_scalar_kernel(const float* __restrict__ part,
+                                                                   float* __restrict__ y, int64_t n,
+                                                                   int splits) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float a = part[i];
+    for (int s = 1; s < splits; ++s) a += part[static_cast<int64_t>(s) * n + i];
+    y[i] = a;
+  }
+}
+
 template <bool kBS>
 cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
                         cudaStream_t stream) {
@@ -436,15 +482,26 @@ cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const GemmPa
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  fn<<<grid, kThreads, kSmemBytes, stream>>>(a, b, p);
+  fn<<<dim3(grid, p.splits), kThreads, kSmemBytes, stream>>>(a, b, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+int gemm_splits(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+  if (M <= 0 || N <= 0 || K <= 0 || dev.sm_count <= 0) return 1;
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int64_t nwin = (K / kQK + kWin - 1) / kWin;
+  if (tiles >= dev.sm_count) return 1;
+  int64_t s = dev.sm_count / tiles;
+  if (s > nwin) s = nwin;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
 cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float* xd,
-                           const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
-                           int64_t K, const DeviceInfo& dev, cudaStream_t stream) {
+                           const uint16_t* Wd, float* y, int32_t* isum, float* part, int splits,
+                           int64_t M, int64_t N, int64_t K, const DeviceInfo& dev,
+                           cudaStream_t stream) {
   (void)dev;
   if (M == 0 || N == 0) return cudaSuccess;
   if (K == 0) return cudaErrorInvalidValue;  // the API handles K == 0 without a launch
@@ -457,14 +514,26 @@ cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float
   p.Wd = Wd;
   p.y = y;
   p.isum = isum;
+  if (isum != nullptr || splits < 1 || part == nullptr) splits = 1;  // block sums: one range
+  p.splits = splits;
+  p.part = splits > 1 ? part : nullptr;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.err = dev.err_word;
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  return isum ? launch_impl<true>(ta, tb, p, static_cast<int>(tiles), stream)
-              : launch_impl<false>(ta, tb, p, static_cast<int>(tiles), stream);
+  if (isum) return launch_impl<true>(ta, tb, p, static_cast<int>(tiles), stream);
+  cudaError_t e = launch_impl<false>(ta, tb, p, static_cast<int>(tiles), stream);
+  if (e != cudaSuccess || splits == 1) return e;
+  const int64_t n = M * N;
+  const int blocks = static_cast<int>(std::min<int64_t>((n / 4 + 255) / 256, 4 * dev.sm_count)) + 1;
+  if (n % 4 == 0)
+    reduce_splits_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(part),
+                                                     reinterpret_cast<float4*>(y), n / 4, splits);
+  else
+    reduce_splits_scalar_kernel<<<blocks, 256, 0, stream>>>(part, y, n, splits);
+  return cudaGetLastError();
 }
 
 }  // namespace q8

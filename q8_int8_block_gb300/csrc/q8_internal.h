@@ -55,8 +55,14 @@ cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const in
 // Tensor-core GEMM on binary16 codes: A16 [M,K] activation codes, B16 [N,K] weight codes,
 // xd [M,K/32] f32, Wd [N,K/32] binary16 bits.  Writes y [M,N] (rescaled sum) or, when
 // isum != nullptr, the raw block sums isum [M,N,K/32].
+// K ranges (of whole 16-block scale windows) the GEMM splits into when the output has fewer
+// 128 x 256 tiles than the GPU has SMs; 1 otherwise.
+int gemm_splits(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
+// With splits > 1, part [splits, M, N] f32 receives the partial outputs and a second kernel
+// adds them (in a fixed order) into y.
 cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float* xd,
-                           const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
-                           int64_t K, const DeviceInfo& dev, cudaStream_t stream);
+                           const uint16_t* Wd, float* y, int32_t* isum, float* part, int splits,
+                           int64_t M, int64_t N, int64_t K, const DeviceInfo& dev,
+                           cudaStream_t stream);
 
 }  // namespace q8
