@@ -204,6 +204,7 @@ CASES = {
 TRAFFIC_PROFILES = {  # committed ncu summaries that record DRAM bytes per launch
     "decode_m1": ("decode_kernel_m1_k4096_n12288.md", ["q8_decode.cu", "q8_ptx.cuh", "q8_quant_dev.cuh"]),
     "prefill9b_up": ("gemm_tc_kernel_m2048_k4096_n12288.md", ["q8_gemm.cu", "q8_ptx.cuh"]),
+    "decode_m16": ("batch_kernel_m16_k4096_n12288.md", ["q8_batch.cu", "q8_ptx.cuh", "q8_quant_dev.cuh"]),
 }
 
 
