@@ -132,8 +132,9 @@ q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64
 uint32_t q8_device_error(q8_status* status);
 
 /*
- * q8_linear_noalloc -- the tensor-core Q8_0 linear layer (same kernels and results as
- * q8_linear_ex with Q8_PATH_TENSOR) for callers that cannot allocate device memory during
+ * q8_linear_noalloc -- the tensor-core Q8_0 linear layer (the same kernels as q8_linear_ex
+ * with Q8_PATH_TENSOR, without its split of K on small outputs, so results agree within the
+ * library's tolerance) for callers that cannot allocate device memory during
  * a call: a host framework that owns every device allocation through its own fixed pool,
  * or a serving loop where cudaMalloc's implicit device synchronization, or running out of
  * memory in the middle of a step, is not acceptable.  The post has no counterpart of this
