@@ -174,7 +174,9 @@ const char* q8_status_string(q8_status status);
 /* Text of the last CUDA error seen by the calling thread in this library (static/TLS). */
 const char* q8_last_cuda_error(void);
 
-/* Frees library-owned scratch memory on every device.  Not thread-safe against calls in
+/* Frees library-owned scratch memory on every device and forgets the per-kernel launch
+ * attributes the library has set (shared-memory limits, register counts), so that a new
+ * CUDA context, e.g. after cudaDeviceReset, starts afresh.  Not thread-safe against calls in
  * flight: call it when no q8_linear / q8_block_sums call is running. */
 void q8_release(void);
 

@@ -389,8 +389,49 @@ void q8_release(void) {
   }
   g_ws.clear();
   if (cur >= 0) cudaSetDevice(cur);
+  forget_kernel_attributes();  // a later context (e.g. after cudaDeviceReset) starts afresh
 }
 
 const char* q8_version(void) { return "0.1.0"; }
 
 }  // extern "C"
+
+namespace q8 {
+namespace {
+std::mutex g_attr_mu;
+std::map<std::pair<const void*, int>, size_t> g_smem_set;
+std::map<std::pair<const void*, int>, int> g_regs;
+}  // namespace
+
+cudaError_t ensure_smem(const void* fn, size_t bytes, int device) {
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  size_t& cur = g_smem_set[{fn, device}];
+  if (cur >= bytes) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) cur = bytes;
+  return e;
+}
+
+void forget_kernel_attributes() {
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  g_smem_set.clear();
+  g_regs.clear();
+}
+
+cudaError_t kernel_regs(const void* fn, int device, int* regs) {
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  auto it = g_regs.find({fn, device});
+  if (it != g_regs.end()) {
+    *regs = it->second;
+    return cudaSuccess;
+  }
+  cudaFuncAttributes fa;
+  const cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+  if (e != cudaSuccess) return e;
+  g_regs[{fn, device}] = fa.numRegs;
+  *regs = fa.numRegs;
+  return cudaSuccess;
+}
+
+}  // namespace q8

@@ -539,10 +539,9 @@ BatchPlan batch_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
 
 template <bool kBS, int kNTG>
 cudaError_t launch_batch_kernel(const CUtensorMap& tw, const CUtensorMap& ts, const BatchParams& p,
-                                int grid, size_t smem, cudaStream_t stream) {
+                                int grid, size_t smem, cudaStream_t stream, int dev_id) {
   auto fn = batch_kernel<kBS, kNTG>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(fn), smem, dev_id);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -653,15 +652,15 @@ cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const in
     if (TG >= nwr && (TG + nwr - 1) / nwr > ntg_max) ntg_max = (TG + nwr - 1) / nwr;
   }
   if (bs) {
-    if (ntg_max <= 1) return launch_batch_kernel<true, 1>(tw, ts, p, pl.grid, pl.smem, stream);
-    if (ntg_max <= 2) return launch_batch_kernel<true, 2>(tw, ts, p, pl.grid, pl.smem, stream);
-    if (ntg_max <= 4) return launch_batch_kernel<true, 4>(tw, ts, p, pl.grid, pl.smem, stream);
-    return launch_batch_kernel<true, 8>(tw, ts, p, pl.grid, pl.smem, stream);
+    if (ntg_max <= 1) return launch_batch_kernel<true, 1>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
+    if (ntg_max <= 2) return launch_batch_kernel<true, 2>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
+    if (ntg_max <= 4) return launch_batch_kernel<true, 4>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
+    return launch_batch_kernel<true, 8>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
   }
-  if (ntg_max <= 1) return launch_batch_kernel<false, 1>(tw, ts, p, pl.grid, pl.smem, stream);
-  if (ntg_max <= 2) return launch_batch_kernel<false, 2>(tw, ts, p, pl.grid, pl.smem, stream);
-  if (ntg_max <= 4) return launch_batch_kernel<false, 4>(tw, ts, p, pl.grid, pl.smem, stream);
-  return launch_batch_kernel<false, 8>(tw, ts, p, pl.grid, pl.smem, stream);
+  if (ntg_max <= 1) return launch_batch_kernel<false, 1>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
+  if (ntg_max <= 2) return launch_batch_kernel<false, 2>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
+  if (ntg_max <= 4) return launch_batch_kernel<false, 4>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
+  return launch_batch_kernel<false, 8>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
 }
 
 }  // namespace q8

@@ -315,10 +315,10 @@ Plan plan_for(int64_t M, int64_t K, bool block_sums, const DeviceInfo& dev) {
 }
 
 template <int MT, bool kBS, bool kSc, int kXP = 0>
-cudaError_t launch_one(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream) {
+cudaError_t launch_one(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream,
+                       int dev_id) {
   auto fn = decode_kernel<MT, kBS, kSc, kXP>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(fn), smem, dev_id);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -335,17 +335,17 @@ cudaError_t launch_one(const DecodeParams& p, int grid, size_t smem, cudaStream_
 
 template <int MT>
 cudaError_t launch_mt(const DecodeParams& p, bool bs, bool sc, int grid, size_t smem,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, int dev_id) {
   if constexpr (MT == 1) {
     if (p.K <= 512 * kXRegPieces) {  // activation codes in registers
-      if (bs) return launch_one<1, true, false, kXRegPieces>(p, grid, smem, stream);
-      return sc ? launch_one<1, false, true, kXRegPieces>(p, grid, smem, stream)
-                : launch_one<1, false, false, kXRegPieces>(p, grid, smem, stream);
+      if (bs) return launch_one<1, true, false, kXRegPieces>(p, grid, smem, stream, dev_id);
+      return sc ? launch_one<1, false, true, kXRegPieces>(p, grid, smem, stream, dev_id)
+                : launch_one<1, false, false, kXRegPieces>(p, grid, smem, stream, dev_id);
     }
   }
-  if (bs) return launch_one<MT, true, false>(p, grid, smem, stream);
-  return sc ? launch_one<MT, false, true>(p, grid, smem, stream)
-            : launch_one<MT, false, false>(p, grid, smem, stream);
+  if (bs) return launch_one<MT, true, false>(p, grid, smem, stream, dev_id);
+  return sc ? launch_one<MT, false, true>(p, grid, smem, stream, dev_id)
+            : launch_one<MT, false, false>(p, grid, smem, stream, dev_id);
 }
 
 }  // namespace
@@ -377,10 +377,10 @@ cudaError_t launch_decode(const void* x, int xtype, const int8_t* xq_in, const i
   p.err = dev.err_word;
   const int grid = static_cast<int>(N < dev.sm_count ? N : dev.sm_count);
   switch (mt_for(M)) {
-    case 1: return launch_mt<1>(p, bs, pl.scales_in_stage, grid, pl.smem, stream);
-    case 2: return launch_mt<2>(p, bs, pl.scales_in_stage, grid, pl.smem, stream);
-    case 4: return launch_mt<4>(p, bs, pl.scales_in_stage, grid, pl.smem, stream);
-    default: return launch_mt<8>(p, bs, pl.scales_in_stage, grid, pl.smem, stream);
+    case 1: return launch_mt<1>(p, bs, pl.scales_in_stage, grid, pl.smem, stream, dev.device);
+    case 2: return launch_mt<2>(p, bs, pl.scales_in_stage, grid, pl.smem, stream, dev.device);
+    case 4: return launch_mt<4>(p, bs, pl.scales_in_stage, grid, pl.smem, stream, dev.device);
+    default: return launch_mt<8>(p, bs, pl.scales_in_stage, grid, pl.smem, stream, dev.device);
   }
 }
 

@@ -471,16 +471,15 @@ __global__ void __launch_bounds__(256) reduce_splits_scalar_kernel(const float* 
 
 template <bool kBS>
 cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, int dev_id) {
   auto fn = gemm_tc_kernel<kBS>;
   // setmaxnreg.inc waits until the registers exist: the split above is exact only if the
   // kernel was compiled for kLaunchRegs per thread.  Refuse to launch otherwise.
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+  int regs = 0;
+  cudaError_t e = kernel_regs(reinterpret_cast<const void*>(fn), dev_id, &regs);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBytes));
+  if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  e = ensure_smem(reinterpret_cast<const void*>(fn), kSmemBytes, dev_id);
   if (e != cudaSuccess) return e;
   fn<<<dim3(grid, p.splits), kThreads, kSmemBytes, stream>>>(a, b, p);
   return cudaGetLastError();
@@ -502,7 +501,6 @@ cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float
                            const uint16_t* Wd, float* y, int32_t* isum, float* part, int splits,
                            int64_t M, int64_t N, int64_t K, const DeviceInfo& dev,
                            cudaStream_t stream) {
-  (void)dev;
   if (M == 0 || N == 0) return cudaSuccess;
   if (K == 0) return cudaErrorInvalidValue;  // the API handles K == 0 without a launch
   CUtensorMap ta, tb;
@@ -523,8 +521,8 @@ cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float
   p.err = dev.err_word;
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  if (isum) return launch_impl<true>(ta, tb, p, static_cast<int>(tiles), stream);
-  cudaError_t e = launch_impl<false>(ta, tb, p, static_cast<int>(tiles), stream);
+  if (isum) return launch_impl<true>(ta, tb, p, static_cast<int>(tiles), stream, dev.device);
+  cudaError_t e = launch_impl<false>(ta, tb, p, static_cast<int>(tiles), stream, dev.device);
   if (e != cudaSuccess || splits == 1) return e;
   const int64_t n = M * N;
   const int blocks = static_cast<int>(std::min<int64_t>((n / 4 + 255) / 256, 4 * dev.sm_count)) + 1;

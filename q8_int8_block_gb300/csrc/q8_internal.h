@@ -16,6 +16,15 @@ struct DeviceInfo {
   uint32_t* err_word = nullptr;  // device address of the library's error word
 };
 
+// ---- q8_api.cu --------------------------------------------------------------------
+// Raises kernel `fn`'s dynamic shared-memory limit on `device` (the current device) to at
+// least `bytes`, remembering what was set so that repeated launches skip the driver call.
+cudaError_t ensure_smem(const void* fn, size_t bytes, int device);
+// The kernel's register count per thread (cudaFuncGetAttributes, cached per kernel/device).
+cudaError_t kernel_regs(const void* fn, int device, int* regs);
+// Drops both caches (q8_release: a later context starts afresh).
+void forget_kernel_attributes();
+
 // ---- q8_quant.cu ------------------------------------------------------------------
 // Quantizes `rows` rows of K values (xtype 0 = f32, 1 = bf16 bits) into codes and scales.
 //   codes_f16 == false: int8 codes;  true: binary16 codes (exact small integers).
