@@ -272,7 +272,8 @@ def time_graph_steps(torch, q8, step_fns, steps, warmup, instrument=True):
     return total, kern
 
 
-def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=False, spec=None):
+def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=False, spec=None,
+             force_path=None):
     wname, p, mi = spec if spec is not None else CASES[name]
     wl = workloads.WORKLOADS[wname]
     W = wl.make_weights(p)
@@ -292,11 +293,15 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
     else:
         x = torch.from_numpy(x_np).to(dev)
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
-    wsz = q8.q8_linear_workspace_size(M, N, K)
+    wsz = q8.q8_linear_workspace_size(M, N, K, force_path or "auto")
     ws = torch.empty(max(wsz, 1), dtype=torch.uint8, device=dev) if wsz else None
-    wsz_batch = q8.q8_linear_workspace_size(M, N, K, "batch") if M <= 64 else 0
-    path = "decode" if wsz == 0 else ("batch" if wsz == wsz_batch else "tensor")
-    fns = [lambda i=i: q8.q8_linear_ex(x, Wqs[i], Wds[i], y=y, workspace=ws) for i in range(copies)]
+    if force_path:
+        path = force_path
+    else:
+        wsz_batch = q8.q8_linear_workspace_size(M, N, K, "batch") if M <= 64 else 0
+        path = "decode" if wsz == 0 else ("batch" if wsz == wsz_batch else "tensor")
+    fns = [lambda i=i: q8.q8_linear_ex(x, Wqs[i], Wds[i], y=y, path=path, workspace=ws)
+           for i in range(copies)]
     bytes_step = workloads.algorithmic_bytes(M, N, K, x_bytes=xsize)
     ops_step = workloads.algorithmic_ops(M, N, K)
     t_hbm = bytes_step / (pk["hbm_gbs"] * 1e9)
@@ -305,7 +310,7 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
     # the tensor path's steps hold three kernels: time the GEMM itself with event nodes; the
     # streaming paths (one kernel, or the activation quantizer chained by programmatic
     # dependent launch to the batched kernel) are timed per step
-    inst = path == "tensor"
+    inst = path in ("tensor", "dp4a")
     if clocks:
         with ClockSampler(torch.cuda.current_device()) as clk:
             total, kern = time_graph_steps(torch, q8, fns, steps, warmup, instrument=inst)
@@ -330,8 +335,18 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
                 "algorithmic_flops_per_launch": ops_step,
                 "peak_source": f"bf16_tflops (burst) of the {pk_src} peaks: the kernel runs on "
                                "the dense kind::f16 tensor pipe (int8 codes as binary16)"}
-    roof["kernel"] = {"decode": "q8::decode_kernel", "batch": "q8::batch_kernel"}.get(
-        path, "q8::gemm_tc_kernel")
+    if path == "dp4a":
+        # CUDA-core integer path: peak from unit counts, 64 dp4a per clock per SM (measured),
+        # 4 int8 MACs each, at the maximum SM clock
+        dp4a_peak = 64 * 4 * 2 * 152 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": round(ops_step / kern / 1e12, 2),
+                "peak": round(dp4a_peak, 1), "unit": "TOPS",
+                "frac": round(ops_step / kern / 1e12 / dp4a_peak, 4),
+                "algorithmic_flops_per_launch": ops_step,
+                "peak_source": "dp4a: 64 per clock per SM (microbenchmark) x 4 MACs x 2 ops x "
+                               "152 SMs x maximum SM clock"}
+    roof["kernel"] = {"decode": "q8::decode_kernel", "batch": "q8::batch_kernel",
+                      "dp4a": "q8::dp4a_gemm_kernel"}.get(path, "q8::gemm_tc_kernel")
     roof["kernel_us"] = round(kern * 1e6, 3)
     roof["kernel_time"] = ("time per step of the timed region (one kernel per step; "
                            "consecutive launches overlap by programmatic dependent launch)"
@@ -343,17 +358,17 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
     roof["traffic"] = profiled_traffic(*prof) if prof else None
     out = {"name": name, "M": M, "K": K, "N": N, "path": path, "unit": unit, "value": value,
            "t_max": t_max, "roofline": roof, "copies": copies, "wbytes": wbytes,
-           "launches_per_step": {"decode": 1, "batch": 2}.get(path, 3), "clocks": clk_summary,
+           "launches_per_step": {"decode": 1, "batch": 2, "dp4a": 2}.get(path, 3), "clocks": clk_summary,
            "bytes_step": bytes_step, "xsize": xsize, "bf16": wl.bf16}
     if e2e:
         out["e2e"] = e2e_measure(torch, q8, dev, x_np, wl.bf16, Wqs, Wds, M, N, K, steps, warmup,
-                                 bytes_step, ops_step, bound)
+                                 bytes_step, ops_step, bound, path=force_path)
         out["Wq0"], out["Wd0"], out["x_np"] = Wq0, Wd0, x_np
     return out
 
 
 def e2e_measure(torch, q8, dev, x_np, bf16, Wqs, Wds, M, N, K, steps, warmup, bytes_step, ops_step,
-                bound):
+                bound, path=None):
     """End to end through the public call q8_linear / q8_linear_ex: per step the H2D copy of x
     from pinned memory, the call, and the D2H copy of y into pinned memory."""
     copies = len(Wqs)
@@ -361,11 +376,15 @@ def e2e_measure(torch, q8, dev, x_np, bf16, Wqs, Wds, M, N, K, steps, warmup, by
     if bf16:
         xh = torch.from_numpy(x_np.view(np.int16).copy()).pin_memory()
         xd = torch.empty((M, K), dtype=torch.int16, device=dev)
-        call = lambda i: q8.q8_linear(xd.view(torch.bfloat16), Wqs[i % copies], Wds[i % copies], y=yd)
+        if path is None:
+            call = lambda i: q8.q8_linear(xd.view(torch.bfloat16), Wqs[i % copies], Wds[i % copies], y=yd)
+        else:
+            call = lambda i: q8.q8_linear_ex(xd.view(torch.bfloat16), Wqs[i % copies], Wds[i % copies],
+                                             y=yd, path=path)
     else:
         xh = torch.from_numpy(x_np.copy()).pin_memory()
         xd = torch.empty((M, K), dtype=torch.float32, device=dev)
-        call = lambda i: q8.q8_linear_ex(xd, Wqs[i % copies], Wds[i % copies], y=yd)
+        call = lambda i: q8.q8_linear_ex(xd, Wqs[i % copies], Wds[i % copies], y=yd, path=path or "auto")
     yh = torch.empty((M, N), dtype=torch.float32).pin_memory()
     yd = torch.empty((M, N), dtype=torch.float32, device=dev)
     for i in range(3):
@@ -407,15 +426,20 @@ def gpu_arm(args):
     pk, pk_src = peaks()
     dev = torch.device("cuda", local)
     r = run_case(torch, q8, dev, args.workload, args.steps, args.warmup, pk, pk_src, clocks=True,
-                 e2e=True)
+                 e2e=True, force_path=None if args.path == "auto" else args.path)
     extra = {}
     if not args.no_extra and args.workload == "decode_m1":
-        for name, st in (("decode_m4", 20000), ("decode_m16", 20000), ("decode_m64", 20000),
-                         ("prefill9b_up", 200), ("prefill9b_down", 200)):
-            e = run_case(torch, q8, dev, name, st, max(3, st // 50), pk, pk_src)
-            extra[name] = {"value": round(e["value"], 3), "unit": e["unit"], "path": e["path"],
-                           "us_per_step": round(e["t_max"] / st * 1e6, 3),
-                           "roofline": e["roofline"], "steps": st}
+        for name, st, fp in (("decode_m4", 20000, None), ("decode_m16", 20000, None),
+                             ("decode_m64", 20000, None), ("prefill9b_up", 200, None),
+                             ("prefill9b_down", 200, None), ("prefill9b_up", 50, "dp4a")):
+            e = run_case(torch, q8, dev, name, st, max(3, st // 50), pk, pk_src, force_path=fp)
+            key = name if fp is None else f"{name}_{fp}"
+            extra[key] = {"value": round(e["value"], 3), "unit": e["unit"], "path": e["path"],
+                          "us_per_step": round(e["t_max"] / st * 1e6, 3),
+                          "roofline": e["roofline"], "steps": st}
+            if fp == "dp4a":
+                extra[key]["note"] = ("the post's own design (dp4a int8 GEMM on CUDA cores), "
+                                      "kept as the prior-art comparison on this GPU")
     err = q8.q8_device_error()
     wname = CASES[args.workload][0]
     desc = {"decode": "decode GEMV, FFN up-projection of a dense ~9B-class layer",
@@ -547,6 +571,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=sorted(CASES), default="decode_m1",
                     help="which configured shape to time (default: decode GEMV, M=1)")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--path", choices=["auto", "decode", "batch", "tensor", "dp4a"], default="auto",
+                    help="force a kernel family for --workload (default: the library's choice)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every point of the dense-layer sweep workload (one GPU) and exit")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -70,8 +70,10 @@ typedef enum q8_path {
     Q8_PATH_DECODE = 1,  /* weight-streaming kernel (int8 dot products, fused act-quant);
                             M <= 8                                                        */
     Q8_PATH_TENSOR = 2,  /* tcgen05 tensor-core GEMM with per-block rescale               */
-    Q8_PATH_BATCH = 3    /* weight-streaming kernel with mma.sync block sums; 1 <= M <= 64,
+    Q8_PATH_BATCH = 3,   /* weight-streaming kernel with mma.sync block sums; 1 <= M <= 64,
                             K % 256 == 0                                                  */
+    Q8_PATH_DP4A = 4     /* the post's own design: dp4a int8 GEMM on CUDA cores, kept as a
+                            prior-art comparison; never chosen by AUTO                     */
 } q8_path;
 
 /*

@@ -29,7 +29,7 @@ _LIB_PATH = os.path.join(_HERE, "libq8.so")
 STATUS = {0: "Q8_OK", 1: "Q8_ERR_NULL", 2: "Q8_ERR_SHAPE", 3: "Q8_ERR_ALIGN", 4: "Q8_ERR_DTYPE",
           5: "Q8_ERR_NOMEM", 6: "Q8_ERR_CUDA", 7: "Q8_ERR_DEVICE", 8: "Q8_ERR_CAPTURE"}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
-PATHS = {"auto": 0, "decode": 1, "tensor": 2, "batch": 3}
+PATHS = {"auto": 0, "decode": 1, "tensor": 2, "batch": 3, "dp4a": 4}
 
 
 class Q8Error(RuntimeError):

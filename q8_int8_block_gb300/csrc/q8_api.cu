@@ -103,6 +103,10 @@ q8_status resolve_path(int64_t M, int64_t N, int64_t K, q8_path req, const Devic
       if (!batch_ok) return Q8_ERR_SHAPE;
       *out = req;
       return Q8_OK;
+    case Q8_PATH_DP4A:
+      if (M > static_cast<int64_t>(65535) * 64) return Q8_ERR_SHAPE;  // grid rows of 64 tokens
+      *out = req;
+      return Q8_OK;
     case Q8_PATH_TENSOR:
       *out = req;
       return Q8_OK;
@@ -117,6 +121,11 @@ size_t tensor_ws_bytes(int64_t M, int64_t N, int64_t K, int splits) {
   return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(M) * (K / kQK) * 4) +
          align256(static_cast<size_t>(N) * K * 2) +
          (splits > 1 ? align256(static_cast<size_t>(splits) * M * N * 4) : 0);
+}
+
+// Scratch of the dp4a path: int8 activation codes [M,K] and their scales [M,K/32].
+size_t dp4a_ws_bytes(int64_t M, int64_t K) {
+  return align256(static_cast<size_t>(M) * K) + align256(static_cast<size_t>(M) * (K / kQK) * 4);
 }
 
 // Library-owned scratch for (current device, stream), grown on demand.
@@ -188,7 +197,7 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
                       size_t ws_bytes, bool library_ws, cudaStream_t stream) {
   if (xtype != Q8_F32 && xtype != Q8_BF16) return Q8_ERR_DTYPE;
   if (path != Q8_PATH_AUTO && path != Q8_PATH_DECODE && path != Q8_PATH_TENSOR &&
-      path != Q8_PATH_BATCH)
+      path != Q8_PATH_BATCH && path != Q8_PATH_DP4A)
     return Q8_ERR_DTYPE;
   q8_status st = check_shape(M, N, K);
   if (st != Q8_OK) return st;
@@ -209,7 +218,9 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
                            stream);
     }));
   const int splits = gemm_splits(M, N, K, dev);
-  const size_t need = p == Q8_PATH_BATCH ? batch_ws_bytes(M, K) : tensor_ws_bytes(M, N, K, splits);
+  const size_t need = p == Q8_PATH_BATCH  ? batch_ws_bytes(M, K)
+                      : p == Q8_PATH_DP4A ? dp4a_ws_bytes(M, K)
+                                          : tensor_ws_bytes(M, N, K, splits);
   if (library_ws) {
     if ((st = library_workspace(dev, stream, need, &ws)) != Q8_OK) return st;
   } else {
@@ -222,6 +233,15 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
       return launch_batch(x, static_cast<int>(xtype), nullptr, Wq, Wd, y, nullptr, M, N, K, ws, dev,
                           stream);
     }));
+  if (p == Q8_PATH_DP4A) {
+    int8_t* xq = static_cast<int8_t*>(ws);
+    float* xdq = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                          align256(static_cast<size_t>(M) * K));
+    cudaError_t e = launch_quantize(x, static_cast<int>(xtype), xq, false, xdq, false, M, K, dev, stream);
+    if (e == cudaSuccess)
+      e = timed_launch(stream, [&] { return launch_dp4a_gemm(xq, xdq, Wq, Wd, y, nullptr, M, N, K, stream); });
+    return launch_status(e);
+  }
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   uint16_t* A16 = reinterpret_cast<uint16_t*>(w8);
   float* xd = reinterpret_cast<float*>(w8 + align256(static_cast<size_t>(M) * K * 2));
@@ -287,6 +307,7 @@ size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path) {
   q8_path p;
   if (resolve_path(M, N, K, path, dev, &p) != Q8_OK) return 0;
   if (p == Q8_PATH_DECODE || M == 0 || N == 0 || K == 0) return 0;
+  if (p == Q8_PATH_DP4A) return dp4a_ws_bytes(M, K);
   return p == Q8_PATH_BATCH ? batch_ws_bytes(M, K)
                             : tensor_ws_bytes(M, N, K, gemm_splits(M, N, K, dev));
 }
@@ -294,7 +315,7 @@ size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path) {
 q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64_t M, int64_t N,
                         int64_t K, q8_path path, cudaStream_t stream) {
   if (path != Q8_PATH_AUTO && path != Q8_PATH_DECODE && path != Q8_PATH_TENSOR &&
-      path != Q8_PATH_BATCH)
+      path != Q8_PATH_BATCH && path != Q8_PATH_DP4A)
     return Q8_ERR_DTYPE;
   q8_status st = check_shape(M, N, K);
   if (st != Q8_OK) return st;
@@ -309,6 +330,8 @@ q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64
   if (p == Q8_PATH_DECODE)
     return launch_status(
         launch_decode(nullptr, 0, xq, Wq, nullptr, nullptr, isum, M, N, K, dev, stream));
+  if (p == Q8_PATH_DP4A)
+    return launch_status(launch_dp4a_gemm(xq, nullptr, Wq, nullptr, nullptr, isum, M, N, K, stream));
   if (p == Q8_PATH_BATCH) {
     void* wsb = nullptr;
     if ((st = library_workspace(dev, stream, batch_ws_bytes(M, K), &wsb)) != Q8_OK) return st;

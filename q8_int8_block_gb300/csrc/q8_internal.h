@@ -60,6 +60,13 @@ cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const in
                          const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
                          int64_t K, void* ws, const DeviceInfo& dev, cudaStream_t stream);
 
+// ---- q8_dp4a.cu -------------------------------------------------------------------
+// The post's design: dp4a int8 GEMM on CUDA cores (prior-art comparison).  xq [M,K] int8,
+// xd [M,K/32] f32 from launch_quantize; y [M,N], or isum [M,N,K/32] when isum != nullptr.
+cudaError_t launch_dp4a_gemm(const int8_t* xq, const float* xd, const int8_t* Wq,
+                             const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
+                             int64_t K, cudaStream_t stream);
+
 // ---- q8_gemm.cu -------------------------------------------------------------------
 // Tensor-core GEMM on binary16 codes: A16 [M,K] activation codes, B16 [N,K] weight codes,
 // xd [M,K/32] f32, Wd [N,K/32] binary16 bits.  Writes y [M,N] (rescaled sum) or, when

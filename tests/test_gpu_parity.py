@@ -98,7 +98,8 @@ def _codes(rng, rows, K):
     ("tensor", 257, 513, 160), ("tensor", 3, 40, 4096),
     ("batch", 2, 7, 256), ("batch", 5, 300, 512), ("batch", 16, 1000, 4096), ("batch", 33, 257, 768),
     ("batch", 64, 2500, 4096), ("batch", 8, 17408, 256), ("batch", 1, 100, 1024),
-    ("batch", 61, 3001, 5120)])
+    ("batch", 61, 3001, 5120),
+    ("dp4a", 1, 1, 32), ("dp4a", 65, 129, 96), ("dp4a", 200, 300, 4128), ("dp4a", 64, 128, 64)])
 def test_block_sums_bit_exact(q8, path, M, N, K):
     rng = np.random.default_rng(M * 7 + N)
     xq = _codes(rng, M, K)
@@ -121,6 +122,8 @@ def test_block_sums_bit_exact(q8, path, M, N, K):
     ("batch", 2, 300, 4096, True), ("batch", 7, 129, 256, False), ("batch", 16, 1000, 512, True),
     ("batch", 33, 77, 1024, True), ("batch", 64, 2000, 4096, True), ("batch", 17, 40, 17408, True),
     ("batch", 64, 2432, 256, False), ("batch", 9, 2433, 512, True), ("batch", 1, 5, 256, True),
+    ("dp4a", 1, 17, 32, True), ("dp4a", 65, 129, 96, False), ("dp4a", 200, 300, 4128, True),
+    ("dp4a", 128, 256, 4096, True), ("dp4a", 7, 1000, 17408, True),
     ("auto", 16, 256, 512, False), ("auto", 1, 256, 512, True), ("auto", 40, 256, 1024, True)])
 def test_linear_small_shapes(q8, path, M, N, K, bf16):
     rng = np.random.default_rng(M * 31 + N * 7 + K)
@@ -296,4 +299,19 @@ def test_batch_path_rejects_unsupported_shapes(q8):
         q8.q8_linear_ex(torch.zeros((4, 288), dtype=torch.bfloat16, device="cuda"), Wq, Wd,
                         path="batch")
     assert e.value.status == 2
+    assert q8.q8_device_error() == 0
+
+
+def test_dp4a_path_full_size_prefill(q8):
+    """The post's own design (dp4a GEMM) on the 9B-class up-projection, sampled outputs."""
+    wl = workloads.WORKLOADS["prefill9b"]
+    Wq_ref, Wd_ref, Wq, Wd = _weights(q8, wl, 0)
+    x, _ = wl.make_act(0, 0)
+    y = q8.q8_linear_ex(T(x), Wq, Wd, path="dp4a").cpu().numpy()
+    xq_ref, xd_ref = O.quantize_act(x, bf16=wl.bf16)
+    M, N = y.shape
+    rows, cols = sample_indices(np.random.default_rng(77), M, N, 3000)
+    ref = O.linear_codes_at(xq_ref, xd_ref, Wq_ref, Wd_ref, rows, cols)
+    assert_close(y[rows, cols], ref, "dp4a prefill9b up (sampled)")
+    assert np.all(np.isfinite(y))
     assert q8.q8_device_error() == 0
