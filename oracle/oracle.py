@@ -35,6 +35,12 @@ def _load(path):
     L.oq8_linear_codes.argtypes = [p, p, p, p, i64, i64, i64, p, ctypes.c_int]
     L.oq8_linear_codes_at.argtypes = [p, p, p, p, i64, p, p, i64, p]
     L.oq8_linear.argtypes = [p, ctypes.c_int, p, p, p, i64, i64, i64, p, p, ctypes.c_int]
+    L.oq8_f64_to_bf16.argtypes = [ctypes.c_double]
+    L.oq8_f64_to_bf16.restype = ctypes.c_uint16
+    L.oq8_silu.argtypes = [ctypes.c_double]
+    L.oq8_silu.restype = ctypes.c_double
+    L.oq8_linear_epilogue.argtypes = [p, p, p, p, i64, i64, i64, p, ctypes.c_int, ctypes.c_int, p]
+    L.oq8_linear_epilogue.restype = None
     for f in ("oq8_quantize_block", "oq8_quantize_weights", "oq8_quantize_act_f32",
               "oq8_quantize_act_bf16", "oq8_block_sums", "oq8_linear_codes",
               "oq8_linear_codes_at", "oq8_linear"):
@@ -175,4 +181,33 @@ def linear(x, Wq, Wd, bf16: bool = False, nthreads: int = 0):
         nthreads = os.cpu_count() or 1
     lib().oq8_linear(_ptr(x), 1 if bf16 else 0, _ptr(Wq), _ptr(Wd), _ptr(y), M, N, K, _ptr(xq),
                      _ptr(xd), nthreads)
+    return y
+
+
+EPILOGUES = {"none": 0, "add": 1, "silu_mul": 2}
+
+
+def f64_to_bf16(v: float) -> int:
+    """binary64 -> bfloat16 bits, round to nearest even."""
+    return int(lib().oq8_f64_to_bf16(float(v)))
+
+
+def silu(g: float) -> float:
+    return float(lib().oq8_silu(float(g)))
+
+
+def linear_epilogue(xq, xd, Wq, Wd, aux=None, op="none", out_bf16=False):
+    """y = op(rescaled block sums, aux) in binary64, rounded once to binary32 or to
+    bfloat16 (returned as uint16 bits).  op: "none", "add" (residual: y = acc + aux) or
+    "silu_mul" (gated unit: y = silu(aux) * acc)."""
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    xd = np.ascontiguousarray(xd, dtype=np.float32)
+    Wq = np.ascontiguousarray(Wq, dtype=np.int8)
+    Wd = np.ascontiguousarray(Wd, dtype=np.uint16)
+    M, K = xq.shape
+    N = Wq.shape[0]
+    a = np.zeros((M, N), np.float32) if aux is None else np.ascontiguousarray(aux, dtype=np.float32)
+    y = np.empty((M, N), np.uint16 if out_bf16 else np.float32)
+    lib().oq8_linear_epilogue(_ptr(xq), _ptr(xd), _ptr(Wq), _ptr(Wd), M, N, K, _ptr(a),
+                              EPILOGUES[op], 1 if out_bf16 else 0, _ptr(y))
     return y

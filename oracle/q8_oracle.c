@@ -189,8 +189,9 @@ void oq8_block_sums(const int8_t *xq, const int8_t *Wq, int64_t M, int64_t N, in
 }
 
 /* One output: y[m,n] = fl32( sum_b f16(Wd[n,b]) * xd[m,b] * isum[m,n,b] ) in binary64. */
-static float oq8_one_output(const int8_t *xq_row, const float *xd_row, const int8_t *wq_row,
-                            const uint16_t *wd_row, int64_t K)
+/* One output before its final rounding: sum over blocks of d_w * d_x * isum in binary64. */
+static double oq8_one_output_f64(const int8_t *xq_row, const float *xd_row, const int8_t *wq_row,
+                                 const uint16_t *wd_row, int64_t K)
 {
     int64_t nb = K / OQ8_QK;
     double acc = 0.0;
@@ -200,7 +201,13 @@ static float oq8_one_output(const int8_t *xq_row, const float *xd_row, const int
             s += (int64_t)xq_row[b * OQ8_QK + j] * (int64_t)wq_row[b * OQ8_QK + j];
         acc += oq8_f16_to_f64(wd_row[b]) * (double)xd_row[b] * (double)s;
     }
-    return (float)acc;
+    return acc;
+}
+
+static float oq8_one_output(const int8_t *xq_row, const float *xd_row, const int8_t *wq_row,
+                            const uint16_t *wd_row, int64_t K)
+{
+    return (float)oq8_one_output_f64(xq_row, xd_row, wq_row, wd_row, K);
 }
 
 typedef struct {
@@ -282,4 +289,73 @@ void oq8_linear(const void *x, int dtype, const int8_t *Wq, const uint16_t *Wd, 
     else
         oq8_quantize_act_bf16((const uint16_t *)x, M, K, xq, xd);
     oq8_linear_codes(xq, xd, Wq, Wd, M, N, K, y, nthreads);
+}
+
+/* ---------------------------------------------------------------------------------- */
+/* The layer's neighbours fused into its output (epilogue): y = op(x . W^T, aux).       */
+/* The post runs its Q8_0 linears inside GDN + attention blocks whose FFN multiplies     */
+/* SiLU(gate) by up and adds residuals; these readings define that step:                 */
+/*   E1 op 0: y = acc;  op 1 (residual): y = acc + aux;  op 2 (gated unit):               */
+/*      y = silu(aux) * acc with silu(g) = g / (1 + exp(-g)), aux being the gate          */
+/*      projection's output and acc the up projection's.                                 */
+/*   E2 acc, aux and op are evaluated in binary64 and rounded once, to binary32 or to     */
+/*      bfloat16 (round to nearest even, subnormals kept, overflow to infinity).          */
+/* ---------------------------------------------------------------------------------- */
+
+/* binary64 -> bfloat16 bits, round to nearest even (8-bit significand, binary32 range). */
+uint16_t oq8_f64_to_bf16(double v)
+{
+    if (v != v)
+        return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80);
+    int e;
+    double m = frexp(a, &e); /* a = m * 2^e, m in [0.5, 1) */
+    int E = e - 1;           /* a = (2m) * 2^E, 2m in [1, 2) */
+    if (E < -126) {          /* subnormal: multiples of 2^-133 */
+        double q = nearbyint(ldexp(a, 133));
+        return (uint16_t)(sign | (uint16_t)q); /* q == 128 is the smallest normal */
+    }
+    double q = nearbyint(ldexp(2.0 * m, 7)); /* 8 significant bits: [128, 256] */
+    if (q == 256.0) {
+        q = 128.0;
+        E += 1;
+    }
+    if (E > 127)
+        return (uint16_t)(sign | 0x7F80);
+    return (uint16_t)(sign | ((uint16_t)(E + 127) << 7) | (uint16_t)((int)q - 128));
+}
+
+double oq8_silu(double g) { return g / (1.0 + exp(-g)); }
+
+static double oq8_epilogue_f64(double acc, int op, const float *aux, int64_t i)
+{
+    if (op == 1)
+        return acc + (double)aux[i];
+    if (op == 2)
+        return oq8_silu((double)aux[i]) * acc;
+    return acc;
+}
+
+/* y[M,N] = op(rescaled block sums, aux), stored as binary32 (ytype 0) or bfloat16 bits
+ * (ytype 1).  aux is [M,N] binary32 (unused for op 0).  Single-threaded. */
+void oq8_linear_epilogue(const int8_t *xq, const float *xd, const int8_t *Wq, const uint16_t *Wd,
+                         int64_t M, int64_t N, int64_t K, const float *aux, int op, int ytype,
+                         void *y)
+{
+    int64_t nb = K / OQ8_QK;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            int64_t i = m * N + n;
+            double v = oq8_epilogue_f64(
+                oq8_one_output_f64(xq + m * K, xd + m * nb, Wq + n * K, Wd + n * nb, K), op, aux, i);
+            if (ytype == 1)
+                ((uint16_t *)y)[i] = oq8_f64_to_bf16(v);
+            else
+                ((float *)y)[i] = (float)v;
+        }
 }

@@ -12,6 +12,7 @@ import tempfile
 import pytest
 
 from oracle import oracle as O
+from tests import test_oracle_epilogue as E
 from tests import test_oracle_pins as P
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle",
@@ -28,6 +29,11 @@ PINS = [
     lambda: P.test_linear_within_quantization_bound(5, 7, 96, False),
     lambda: P.test_linear_within_quantization_bound(16, 40, 512, True),
     P.test_bf16_path_equals_widened_f32_path,
+    E.test_bf16_rounding_hand_worked,
+    E.test_silu_closed_forms,
+    E.test_zero_weights_give_aux,
+    E.test_residual_and_gate_index_alignment,
+    E.test_gated_unit_on_the_unit_code_closed_form,
 ]
 
 # (name, text in the source, replacement)
@@ -49,6 +55,13 @@ MUTANTS = [
      "acc -= oq8_f16_to_f64(wd_row[b]) * (double)xd_row[b] * (double)s;"),
     ("bf16 widening off by a byte", "uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 8;"),
     ("zero block gets scale 1", "*d32 = 0.0f;", "*d32 = 1.0f;"),
+    ("bf16 output truncated", "double q = nearbyint(ldexp(2.0 * m, 7));",
+     "double q = floor(ldexp(2.0 * m, 7));"),
+    ("residual subtracted", "return acc + (double)aux[i];", "return acc - (double)aux[i];"),
+    ("silu of the negated gate", "double oq8_silu(double g) { return g / (1.0 + exp(-g)); }",
+     "double oq8_silu(double g) { return g / (1.0 + exp(g)); }"),
+    ("gate from the wrong element", "return oq8_silu((double)aux[i]) * acc;",
+     "return oq8_silu((double)aux[i / 2]) * acc;"),
 ]
 
 
