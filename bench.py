@@ -273,7 +273,10 @@ def time_graph_steps(torch, q8, step_fns, steps, warmup, instrument=True):
 
 
 def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=False, spec=None,
-             force_path=None):
+             force_path=None, gated=None):
+    """gated: None (the plain layer, float32 y), "fused" (q8_linear_fused: y = silu(gate) *
+    x.W^T stored as bfloat16 by the GEMM's own epilogue) or "unfused" (the plain layer, then
+    torch's silu, multiply and bfloat16 cast as separate kernels)."""
     wname, p, mi = spec if spec is not None else CASES[name]
     wl = workloads.WORKLOADS[wname]
     W = wl.make_weights(p)
@@ -300,9 +303,26 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
     else:
         wsz_batch = q8.q8_linear_workspace_size(M, N, K, "batch") if M <= 64 else 0
         path = "decode" if wsz == 0 else ("batch" if wsz == wsz_batch else "tensor")
-    fns = [lambda i=i: q8.q8_linear_ex(x, Wqs[i], Wds[i], y=y, path=path, workspace=ws)
-           for i in range(copies)]
+    if gated is None:
+        fns = [lambda i=i: q8.q8_linear_ex(x, Wqs[i], Wds[i], y=y, path=path, workspace=ws)
+               for i in range(copies)]
+    else:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(7)
+        gate = torch.randn((M, N), device=dev, generator=gen) * 2.5
+        yb = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        if gated == "fused":
+            fns = [lambda i=i: q8.q8_linear_fused(x, Wqs[i], Wds[i], epi="silu_mul", aux=gate, y=yb,
+                                                  out_dtype=torch.bfloat16, path=path, workspace=ws)
+                   for i in range(copies)]
+        else:
+            def unfused(i):
+                q8.q8_linear_ex(x, Wqs[i], Wds[i], y=y, path=path, workspace=ws)
+                yb.copy_(torch.nn.functional.silu(gate).mul_(y))
+            fns = [lambda i=i: unfused(i) for i in range(copies)]
     bytes_step = workloads.algorithmic_bytes(M, N, K, x_bytes=xsize)
+    if gated is not None:  # the gate is read (4 bytes), y is stored as bfloat16 (2, not 4)
+        bytes_step += M * N * 2
     ops_step = workloads.algorithmic_ops(M, N, K)
     t_hbm = bytes_step / (pk["hbm_gbs"] * 1e9)
     t_tc = ops_step / (pk["bf16_tflops"] * 1e12)
@@ -310,7 +330,7 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
     # the tensor path's steps hold three kernels: time the GEMM itself with event nodes; the
     # streaming paths (one kernel, or the activation quantizer chained by programmatic
     # dependent launch to the batched kernel) are timed per step
-    inst = path in ("tensor", "dp4a")
+    inst = path in ("tensor", "dp4a") or gated == "unfused"
     if clocks:
         with ClockSampler(torch.cuda.current_device()) as clk:
             total, kern = time_graph_steps(torch, q8, fns, steps, warmup, instrument=inst)
@@ -431,8 +451,12 @@ def gpu_arm(args):
     if not args.no_extra and args.workload == "decode_m1":
         for name, st, fp in (("decode_m4", 20000, None), ("decode_m16", 20000, None),
                              ("decode_m64", 20000, None), ("prefill9b_up", 200, None),
-                             ("prefill9b_down", 200, None), ("prefill9b_up", 50, "dp4a")):
-            e = run_case(torch, q8, dev, name, st, max(3, st // 50), pk, pk_src, force_path=fp)
+                             ("prefill9b_down", 200, None), ("prefill9b_up", 50, "dp4a"),
+                             ("decode_m1", 20000, "gated_fused"), ("decode_m1", 20000, "gated_unfused"),
+                             ("prefill9b_up", 200, "gated_fused"), ("prefill9b_up", 200, "gated_unfused")):
+            gated = fp[6:] if fp and fp.startswith("gated_") else None
+            e = run_case(torch, q8, dev, name, st, max(3, st // 50), pk, pk_src,
+                         force_path=None if gated else fp, gated=gated)
             key = name if fp is None else f"{name}_{fp}"
             extra[key] = {"value": round(e["value"], 3), "unit": e["unit"], "path": e["path"],
                           "us_per_step": round(e["t_max"] / st * 1e6, 3),
@@ -440,6 +464,13 @@ def gpu_arm(args):
             if fp == "dp4a":
                 extra[key]["note"] = ("the post's own design (dp4a int8 GEMM on CUDA cores), "
                                       "kept as the prior-art comparison on this GPU")
+            if gated == "fused":
+                extra[key]["note"] = ("gated FFN unit: y = silu(gate) * x.W^T, bfloat16 y, "
+                                      "stored by the layer's epilogue (q8_linear_fused)")
+            if gated == "unfused":
+                extra[key]["note"] = ("the same unit as the plain layer (float32 y) followed by "
+                                      "torch silu, multiply and bfloat16 cast; us_per_step is "
+                                      "the whole step, roofline the layer's kernel alone")
     err = q8.q8_device_error()
     wname = CASES[args.workload][0]
     desc = {"decode": "decode GEMV, FFN up-projection of a dense ~9B-class layer",

@@ -113,6 +113,37 @@ q8_status q8_linear_ex(const void* x, q8_dtype xtype, const int8_t* Wq, const ui
                        float* y, int64_t M, int64_t N, int64_t K, q8_path path,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * q8_linear_fused -- the linear layer with its neighbours in the surrounding block fused
+ * into the output store.  The post runs its Q8_0 linears inside GDN + attention blocks
+ * ("CUDA inference engine for running Qwen3.5/3.6 hybrid models on mining cards
+ * (CMP 100-210)", news.hada.io topic 29953, feature list); the steps next to them are:
+ *   Q8_EPI_NONE      y = x . W^T
+ *   Q8_EPI_ADD       y = x . W^T + aux              (residual add; aux [M,N] float)
+ *   Q8_EPI_SILU_MUL  y = silu(aux) * (x . W^T)      (gated FFN unit: aux is the gate
+ *                    projection's output [M,N] float, W the up projection;
+ *                    silu(g) = g / (1 + e^-g))
+ * y is [M,N] float (ytype Q8_F32) or bfloat16 bits (Q8_BF16, round to nearest even).
+ * aux may be NULL for Q8_EPI_NONE, else it is 16-byte aligned and must not overlap y (the
+ * kernels read it through the read-only data path; an in-place residual add needs a
+ * separate output buffer).  x, Wq, Wd, M, N, K, path and stream as q8_linear_ex;
+ * workspace NULL with workspace_bytes 0 uses the library-owned scratch of q8_linear (same
+ * growth and capture rules), otherwise the caller's.  With K == 0 the sum is empty and y is
+ * the epilogue of zero.
+ * Errors: Q8_ERR_DTYPE for an unknown epilogue, output or activation type; Q8_ERR_NULL for
+ * a NULL aux with an epilogue that reads it; Q8_ERR_ALIGN for aux not 16-byte aligned;
+ * the rest as q8_linear_ex.
+ */
+typedef enum q8_epilogue {
+    Q8_EPI_NONE = 0,
+    Q8_EPI_ADD = 1,
+    Q8_EPI_SILU_MUL = 2
+} q8_epilogue;
+q8_status q8_linear_fused(const void* x, q8_dtype xtype, const int8_t* Wq, const uint16_t* Wd,
+                          q8_epilogue epi, const float* aux, void* y, q8_dtype ytype,
+                          int64_t M, int64_t N, int64_t K, q8_path path, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
 /* Bytes of scratch q8_linear_ex needs for this shape and path (0 if none). */
 size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path);
 

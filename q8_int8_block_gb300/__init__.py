@@ -10,6 +10,7 @@ this package fails.
     xq, xd = q8_quantize_act(x)                  # x bf16/float32 [M,K] -> int8 [M,K], float32 [M,K/32]
     y = q8_linear(x, Wq, Wd)                     # x bf16 [M,K] -> float32 [M,N]
     y = q8_linear_ex(x, Wq, Wd, path="tensor", workspace=ws)
+    y = q8_linear_fused(x, Wq, Wd, epi="silu_mul", aux=gate, out_dtype=torch.bfloat16)
     isum = q8_block_sums(xq, Wq, path="decode")  # int32 [M,N,K/32]
 """
 import ctypes
@@ -18,6 +19,7 @@ import os
 import torch
 
 __all__ = ["Q8Error", "q8_quantize_weights", "q8_quantize_act", "q8_linear", "q8_linear_ex",
+           "q8_linear_fused", "EPILOGUES",
            "q8_linear_workspace_size", "q8_block_sums", "q8_device_error", "q8_release",
            "q8_set_timing_events", "q8_linear_noalloc", "NOALLOC_SCRATCH_BYTES",
            "q8_version", "lib_path", "QK", "PATHS"]
@@ -30,6 +32,7 @@ STATUS = {0: "Q8_OK", 1: "Q8_ERR_NULL", 2: "Q8_ERR_SHAPE", 3: "Q8_ERR_ALIGN", 4:
           5: "Q8_ERR_NOMEM", 6: "Q8_ERR_CUDA", 7: "Q8_ERR_DEVICE", 8: "Q8_ERR_CAPTURE"}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 PATHS = {"auto": 0, "decode": 1, "tensor": 2, "batch": 3, "dp4a": 4}
+EPILOGUES = {"none": 0, "add": 1, "silu_mul": 2}
 
 
 class Q8Error(RuntimeError):
@@ -54,6 +57,7 @@ def _load():
         "q8_linear_ex": [p, i32, p, p, p, i64, i64, i64, i32, p, sz, p],
         "q8_block_sums": [p, p, p, i64, i64, i64, i32, p],
         "q8_linear_noalloc": [p, i32, p, p, p, i64, i64, i64, p],
+        "q8_linear_fused": [p, i32, p, p, i32, p, p, i32, i64, i64, i64, i32, p, sz, p],
     }
     for name, args in sigs.items():
         f = getattr(L, name)
@@ -181,6 +185,35 @@ def q8_linear_ex(x, Wq, Wd, y=None, path="auto", workspace=None, stream=None):
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_L.q8_linear_ex(_ptr(x), DTYPES[x.dtype], _ptr(Wq), _ptr(Wd), _ptr(y), M, N, K,
                            PATHS[path], _ptr(workspace), nbytes, _stream(stream)), "q8_linear_ex")
+    return y
+
+
+def q8_linear_fused(x, Wq, Wd, epi="none", aux=None, y=None, out_dtype=torch.float32,
+                    path="auto", workspace=None, stream=None):
+    """The linear layer with its neighbour fused into the output store:
+    epi "none": y = x.W^T; "add": y = x.W^T + aux (residual); "silu_mul":
+    y = silu(aux) * x.W^T (aux the gate projection's output).  aux float32 [M,N];
+    y float32 or bfloat16 [M,N].  workspace None uses the library-owned scratch."""
+    if x.dtype not in DTYPES:
+        raise TypeError(f"x: expected bfloat16 or float32, got {x.dtype}")
+    if out_dtype not in DTYPES:
+        raise TypeError(f"out_dtype: expected bfloat16 or float32, got {out_dtype}")
+    _need(x, x.dtype, tuple(x.shape), "x")
+    M, K = x.shape
+    N = Wq.shape[0]
+    _need(Wq, torch.int8, (N, K), "Wq")
+    _need(Wd, torch.int16, (N, K // QK), "Wd")
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    _need(y, out_dtype, (M, N), "y")
+    if EPILOGUES[epi] != 0:
+        if aux is None:
+            raise ValueError(f"epi {epi!r} needs aux")
+        _need(aux, torch.float32, (M, N), "aux")
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_L.q8_linear_fused(_ptr(x), DTYPES[x.dtype], _ptr(Wq), _ptr(Wd), EPILOGUES[epi],
+                              _ptr(aux), _ptr(y), DTYPES[out_dtype], M, N, K, PATHS[path],
+                              _ptr(workspace), nbytes, _stream(stream)), "q8_linear_fused")
     return y
 
 

@@ -194,7 +194,8 @@ cudaError_t timed_launch(cudaStream_t stream, F&& launch) {
 
 q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uint16_t* Wd,
                       float* y, int64_t M, int64_t N, int64_t K, q8_path path, void* ws,
-                      size_t ws_bytes, bool library_ws, cudaStream_t stream) {
+                      size_t ws_bytes, bool library_ws, cudaStream_t stream,
+                      const Epilogue& epi = Epilogue()) {
   if (xtype != Q8_F32 && xtype != Q8_BF16) return Q8_ERR_DTYPE;
   if (path != Q8_PATH_AUTO && path != Q8_PATH_DECODE && path != Q8_PATH_TENSOR &&
       path != Q8_PATH_BATCH && path != Q8_PATH_DP4A)
@@ -211,11 +212,14 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
   q8_path p;
   if ((st = resolve_path(M, N, K, path, dev, &p)) != Q8_OK) return st;
   if (M == 0 || N == 0) return Q8_OK;
-  if (K == 0) return launch_status(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 4, stream));
+  if (K == 0) {  // an empty sum
+    if (epi.plain()) return launch_status(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 4, stream));
+    return launch_status(launch_epilogue_only(epi, y, M * N, stream));
+  }
   if (p == Q8_PATH_DECODE)
     return launch_status(timed_launch(stream, [&] {
       return launch_decode(x, static_cast<int>(xtype), nullptr, Wq, Wd, y, nullptr, M, N, K, dev,
-                           stream);
+                           stream, epi);
     }));
   const int splits = gemm_splits(M, N, K, dev);
   const size_t need = p == Q8_PATH_BATCH  ? batch_ws_bytes(M, K)
@@ -231,7 +235,7 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
   if (p == Q8_PATH_BATCH)
     return launch_status(timed_launch(stream, [&] {
       return launch_batch(x, static_cast<int>(xtype), nullptr, Wq, Wd, y, nullptr, M, N, K, ws, dev,
-                          stream);
+                          stream, epi);
     }));
   if (p == Q8_PATH_DP4A) {
     int8_t* xq = static_cast<int8_t*>(ws);
@@ -239,7 +243,9 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
                                           align256(static_cast<size_t>(M) * K));
     cudaError_t e = launch_quantize(x, static_cast<int>(xtype), xq, false, xdq, false, M, K, dev, stream);
     if (e == cudaSuccess)
-      e = timed_launch(stream, [&] { return launch_dp4a_gemm(xq, xdq, Wq, Wd, y, nullptr, M, N, K, stream); });
+      e = timed_launch(stream, [&] {
+        return launch_dp4a_gemm(xq, xdq, Wq, Wd, y, nullptr, M, N, K, stream, epi);
+      });
     return launch_status(e);
   }
   uint8_t* w8 = static_cast<uint8_t*>(ws);
@@ -253,7 +259,7 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
   if (e == cudaSuccess) e = launch_codes_to_f16(Wq, B16, N * K, dev, stream);
   if (e == cudaSuccess)
     e = timed_launch(stream, [&] {
-      return launch_gemm_tc(A16, B16, xd, Wd, y, nullptr, part, splits, M, N, K, dev, stream);
+      return launch_gemm_tc(A16, B16, xd, Wd, y, nullptr, part, splits, M, N, K, dev, stream, epi);
     });
   return launch_status(e);
 }
@@ -298,6 +304,23 @@ q8_status q8_linear_ex(const void* x, q8_dtype xtype, const int8_t* Wq, const ui
                        float* y, int64_t M, int64_t N, int64_t K, q8_path path, void* workspace,
                        size_t workspace_bytes, cudaStream_t stream) {
   return linear_impl(x, xtype, Wq, Wd, y, M, N, K, path, workspace, workspace_bytes, false, stream);
+}
+
+q8_status q8_linear_fused(const void* x, q8_dtype xtype, const int8_t* Wq, const uint16_t* Wd,
+                          q8_epilogue epi, const float* aux, void* y, q8_dtype ytype,
+                          int64_t M, int64_t N, int64_t K, q8_path path, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  if (epi != Q8_EPI_NONE && epi != Q8_EPI_ADD && epi != Q8_EPI_SILU_MUL) return Q8_ERR_DTYPE;
+  if (ytype != Q8_F32 && ytype != Q8_BF16) return Q8_ERR_DTYPE;
+  if (epi != Q8_EPI_NONE && M > 0 && N > 0 && aux == nullptr) return Q8_ERR_NULL;
+  if (!aligned16(aux)) return Q8_ERR_ALIGN;
+  Epilogue e;
+  e.aux = aux;
+  e.op = static_cast<int>(epi);
+  e.bf16 = ytype == Q8_BF16 ? 1 : 0;
+  const bool library_ws = workspace == nullptr && workspace_bytes == 0;
+  return linear_impl(x, xtype, Wq, Wd, static_cast<float*>(y), M, N, K, path, workspace,
+                     workspace_bytes, library_ws, stream, e);
 }
 
 size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path) {

@@ -46,6 +46,7 @@
 
 #include <mutex>
 
+#include "q8_epi.cuh"
 #include "q8_internal.h"
 #include "q8_ptx.cuh"
 #include "q8_quant_dev.cuh"
@@ -76,6 +77,7 @@ struct BatchParams {
   uint32_t stage_bytes;
   uint32_t off_w1, off_wd, off_x, off_xd;  // offsets inside a stage
   uint32_t* err;
+  Epilogue epi;         // fused output step
 };
 
 __device__ __forceinline__ void pdl_launch_dependents() {
@@ -223,6 +225,12 @@ __global__ void __maxnreg__(kMaxRegs)
     // ---------------- consumers --------------------------------------------------------
     const int cw = warp - 1;
     pdl_wait();  // x, y / isum: wait for the previous kernel before reading or writing
+    if constexpr (!kBlockSums) {
+      // this CTA's aux rows (one per token) towards L2 for the epilogue
+      const int nrow = (N - row0) < rows ? (N - row0) : rows;
+      for (int t = cw; t < M; t += kConsumerWarps)
+        if (lane == 0) epi_prefetch(p.epi, static_cast<int64_t>(t) * N + row0, nrow);
+    }
     const int rg = cw % RG;
     const int idx = cw / RG;
     const int nw = (kConsumerWarps - 1 - rg) / RG + 1;  // warps of this row group
@@ -384,13 +392,26 @@ __global__ void __maxnreg__(kMaxRegs)
           }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
-        for (int i = threadIdx.x - 32; i < M * rows; i += 32 * kConsumerWarps) {
-          const int t = i / rows, r = i - t * rows;
-          const int n = row0 + r;
-          if (n < N) {
-            float v = 0.0f;
-            for (int k = 0; k < p.KPall; ++k) v += red[k * layer + t * rows + r];
-            p.y[static_cast<int64_t>(t) * N + n] = v;
+        constexpr int kT = 32 * kConsumerWarps;
+        constexpr int kU = 4;  // outputs per thread whose aux loads are in flight together
+        for (int i0 = threadIdx.x - 32; i0 < M * rows; i0 += kU * kT) {
+          float a[kU];
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const int i = i0 + u * kT;
+            const int t = i / rows, n = row0 + (i - t * rows);
+            a[u] = (i < M * rows && n < N) ? epi_aux(p.epi, static_cast<int64_t>(t) * N + n) : 0.0f;
+          }
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const int i = i0 + u * kT;
+            const int t = i / rows, r = i - t * rows;
+            const int n = row0 + r;
+            if (i < M * rows && n < N) {
+              float v = 0.0f;
+              for (int k = 0; k < p.KPall; ++k) v += red[k * layer + t * rows + r];
+              epi_put(p.epi, p.y, static_cast<int64_t>(t) * N + n, epi_apply(p.epi, v, a[u]));
+            }
           }
         }
       }
@@ -569,7 +590,8 @@ size_t batch_ws_bytes(int64_t M, int64_t K) {
 
 cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const int8_t* Wq,
                          const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
-                         int64_t K, void* ws, const DeviceInfo& dev, cudaStream_t stream) {
+                         int64_t K, void* ws, const DeviceInfo& dev, cudaStream_t stream,
+                         const Epilogue& epi) {
   if (M == 0 || N == 0) return cudaSuccess;
   const BatchPlan pl = batch_plan(M, N, K, dev);
   if (pl.smem == 0 || ws == nullptr) return cudaErrorInvalidValue;
@@ -644,6 +666,7 @@ cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const in
   p.off_x = pl.off_x;
   p.off_xd = pl.off_xd;
   p.err = dev.err_word;
+  p.epi = epi;
   // token groups per warp: at most ceil(TG / warps of a row group)
   const int TG = static_cast<int>((M + 7) / 8);
   int ntg_max = 1;

@@ -29,6 +29,7 @@
 //     sums instead of y.
 #include <cuda_fp16.h>
 
+#include "q8_epi.cuh"
 #include "q8_internal.h"
 #include "q8_ptx.cuh"
 #include "q8_quant_dev.cuh"
@@ -58,6 +59,7 @@ struct DecodeParams {
   int rows_per_stage;  // R
   int stages;          // S
   uint32_t* err;
+  Epilogue epi;        // fused output step
 };
 
 __device__ __forceinline__ void pdl_launch_dependents() {
@@ -188,6 +190,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       }
     }
     for (int j = cw; j < nrows; j += kConsumerWarps) {
+      const int64_t n = r0 + j;
+      float ax = 0.0f;  // lane t < M: aux of output (t, n), loaded before the row's weights land
+      if constexpr (!kBlockSums) {
+        if (lane < M) ax = epi_aux(p.epi, static_cast<int64_t>(lane) * N + n);
+      }
       const int st = j / R;
       const int s = st % S;
       bool ticket = issued > st;
@@ -207,7 +214,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       const uint8_t* stage = ring + static_cast<size_t>(s) * stage_bytes;
       const int jr = j - st * R;  // row within the stage
       const uint8_t* wrow = stage + static_cast<size_t>(jr) * K;
-      const int64_t n = r0 + j;
       const uint16_t* wd_row = kScalesInStage
                                    ? reinterpret_cast<const uint16_t*>(stage + code_bytes) + jr * nb
                                    : p.Wd + n * nb;
@@ -276,7 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           float a = acc[t];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
-          if (lane == 0 && t < M) p.y[static_cast<int64_t>(t) * N + n] = a;
+          // the butterfly leaves the same sum on every lane: lane t stores output t
+          if (lane == t && t < M) epi_put(p.epi, p.y, static_cast<int64_t>(t) * N + n, epi_apply(p.epi, a, ax));
         }
       }
     }
@@ -356,7 +363,8 @@ size_t decode_smem_bytes(int64_t M, int64_t K, const DeviceInfo& dev) {
 
 cudaError_t launch_decode(const void* x, int xtype, const int8_t* xq_in, const int8_t* Wq,
                           const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
-                          int64_t K, const DeviceInfo& dev, cudaStream_t stream) {
+                          int64_t K, const DeviceInfo& dev, cudaStream_t stream,
+                          const Epilogue& epi) {
   if (M == 0 || N == 0) return cudaSuccess;
   const bool bs = isum != nullptr;
   const Plan pl = plan_for(M, K, bs, dev);
@@ -375,6 +383,7 @@ cudaError_t launch_decode(const void* x, int xtype, const int8_t* xq_in, const i
   p.rows_per_stage = pl.R;
   p.stages = pl.S;
   p.err = dev.err_word;
+  p.epi = epi;
   const int grid = static_cast<int>(N < dev.sm_count ? N : dev.sm_count);
   switch (mt_for(M)) {
     case 1: return launch_mt<1>(p, bs, pl.scales_in_stage, grid, pl.smem, stream, dev.device);

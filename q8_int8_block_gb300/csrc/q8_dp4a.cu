@@ -21,6 +21,7 @@
 
 #include <algorithm>
 
+#include "q8_epi.cuh"
 #include "q8_internal.h"
 
 namespace q8 {
@@ -42,6 +43,7 @@ struct Dp4aParams {
   float* y;            // [M, N]
   int32_t* isum;       // [M, N, nb] (block-sum mode)
   int M, N, K;
+  Epilogue epi;        // fused output step
 };
 
 // 16-byte global -> shared copy; src_bytes 0 fills zeros (rows or K past the ends).
@@ -170,10 +172,16 @@ __global__ void __launch_bounds__(kThreads, 2) dp4a_gemm_kernel(const Dp4aParams
     for (int i = 0; i < 4; ++i) {
       const int m = m0 + ty + 16 * i;
       if (m >= M) continue;
+      float a[8];  // the row's aux loads in flight together
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int n = n0 + tx + 16 * j;
-        if (n < N) p.y[static_cast<int64_t>(m) * N + n] = acc[i][j];
+        a[j] = n < N ? epi_aux(p.epi, static_cast<int64_t>(m) * N + n) : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int n = n0 + tx + 16 * j;
+        if (n < N) epi_put(p.epi, p.y, static_cast<int64_t>(m) * N + n, epi_apply(p.epi, acc[i][j], a[j]));
       }
     }
   }
@@ -183,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 2) dp4a_gemm_kernel(const Dp4aParams
 
 cudaError_t launch_dp4a_gemm(const int8_t* xq, const float* xd, const int8_t* Wq,
                              const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
-                             int64_t K, cudaStream_t stream) {
+                             int64_t K, cudaStream_t stream, const Epilogue& epi) {
   if (M == 0 || N == 0) return cudaSuccess;
   if (K == 0) return cudaErrorInvalidValue;  // the API handles K == 0 without a launch
   const int64_t gx = (N + TN - 1) / TN, gy = (M + TM - 1) / TM;
@@ -198,6 +206,7 @@ cudaError_t launch_dp4a_gemm(const int8_t* xq, const float* xd, const int8_t* Wq
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
+  p.epi = epi;
   const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
   if (isum)
     dp4a_gemm_kernel<true><<<grid, kThreads, 0, stream>>>(p);

@@ -33,6 +33,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "q8_epi.cuh"
 #include "q8_internal.h"
 #include "q8_ptx.cuh"
 
@@ -73,6 +74,7 @@ struct GemmParams {
   int32_t* isum;       // [M, N, nb] (block-sum mode)
   int M, N, K;
   uint32_t* err;
+  Epilogue epi;        // fused output step (applied by the split-K reduction when splitting)
 };
 
 // Fill one window of scales: Wd of the tile's 256 columns and xd of its 128 rows, blocks
@@ -307,6 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int nbw = (nb - w * kWin) < kWin ? (nb - w * kWin) : kWin;
+      if constexpr (!kBlockSums) {
+        // the last window: bring this thread's 128 aux values towards L2 for the epilogue
+        if (w + 1 == w_end && p.part == nullptr && m_ok)
+          epi_prefetch(p.epi, static_cast<int64_t>(m) * N + n0 + wg * 128,
+                       min(128, N - (n0 + wg * 128)));
+      }
 #pragma unroll 1
       for (int bb = 0; bb < nbw; ++bb) {
         const int blk = w * kWin + bb;  // absolute block (block-sum output index)
@@ -382,7 +390,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* yrow = (p.part ? p.part + static_cast<int64_t>(blockIdx.y) * M * N : p.y) +
                       static_cast<int64_t>(m) * N;
         const int nbase = n0 + wg * 128;
-        if ((N & 3) == 0 && nbase + 128 <= N) {
+        if (p.part == nullptr && !p.epi.plain()) {
+          const int64_t r0 = static_cast<int64_t>(m) * N + nbase;
+          if ((N & 3) == 0 && nbase + 128 <= N) {
+            // 4 chunks of 32 columns; the 8 aux loads of chunk h + 1 are in flight while
+            // chunk h is computed and stored
+            float4 a[2][8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) a[0][q] = epi_aux4(p.epi, r0 + 4 * q);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              if (h + 1 < 4) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) a[(h + 1) & 1][q] = epi_aux4(p.epi, r0 + 32 * (h + 1) + 4 * q);
+              }
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const int i = 16 * h + 2 * q;  // columns 2i .. 2i + 3 of the slice
+                const float4 v = make_float4(acc[i].x, acc[i].y, acc[i + 1].x, acc[i + 1].y);
+                epi_put4(p.epi, p.y, r0 + 32 * h + 4 * q, epi_apply4(p.epi, v, a[h & 1][q]));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+              if (nbase + 2 * i < N) epi_store(p.epi, p.y, r0 + 2 * i, acc[i].x);
+              if (nbase + 2 * i + 1 < N) epi_store(p.epi, p.y, r0 + 2 * i + 1, acc[i].y);
+            }
+          }
+        } else if ((N & 3) == 0 && nbase + 128 <= N) {
 #pragma unroll
           for (int i = 0; i < 64; i += 2)
             *reinterpret_cast<float4*>(yrow + nbase + 2 * i) =
@@ -443,7 +479,7 @@ bool make_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t co
 // y = sum over s of part[s] (fixed order: the result does not depend on timing).
 __global__ void __launch_bounds__(256) reduce_splits_kernel(const float4* __restrict__ part,
                                                             float4* __restrict__ y, int64_t n4,
-                                                            int splits) {
+                                                            int splits, const Epilogue epi) {
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float4 a = part[i];
@@ -454,18 +490,21 @@ __global__ void __launch_bounds__(256) reduce_splits_kernel(const float4* __rest
       a.z += b.z;
       a.w += b.w;
     }
-    y[i] = a;
+    if (epi.plain())
+      y[i] = a;
+    else
+      epi_put4(epi, reinterpret_cast<float*>(y), 4 * i, epi_apply4(epi, a, epi_aux4(epi, 4 * i)));
   }
 }
 
 __global__ void __launch_bounds__(256) reduce_splits_scalar_kernel(const float* __restrict__ part,
                                                                    float* __restrict__ y, int64_t n,
-                                                                   int splits) {
+                                                                   int splits, const Epilogue epi) {
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float a = part[i];
     for (int s = 1; s < splits; ++s) a += part[static_cast<int64_t>(s) * n + i];
-    y[i] = a;
+    epi_store(epi, y, i, a);
   }
 }
 
@@ -500,7 +539,7 @@ int gemm_splits(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
 cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float* xd,
                            const uint16_t* Wd, float* y, int32_t* isum, float* part, int splits,
                            int64_t M, int64_t N, int64_t K, const DeviceInfo& dev,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, const Epilogue& epi) {
   if (M == 0 || N == 0) return cudaSuccess;
   if (K == 0) return cudaErrorInvalidValue;  // the API handles K == 0 without a launch
   CUtensorMap ta, tb;
@@ -519,6 +558,7 @@ cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.err = dev.err_word;
+  p.epi = epi;
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
   if (isum) return launch_impl<true>(ta, tb, p, static_cast<int>(tiles), stream, dev.device);
@@ -528,9 +568,24 @@ cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float
   const int blocks = static_cast<int>(std::min<int64_t>((n / 4 + 255) / 256, 4 * dev.sm_count)) + 1;
   if (n % 4 == 0)
     reduce_splits_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(part),
-                                                     reinterpret_cast<float4*>(y), n / 4, splits);
+                                                     reinterpret_cast<float4*>(y), n / 4, splits, epi);
   else
-    reduce_splits_scalar_kernel<<<blocks, 256, 0, stream>>>(part, y, n, splits);
+    reduce_splits_scalar_kernel<<<blocks, 256, 0, stream>>>(part, y, n, splits, epi);
+  return cudaGetLastError();
+}
+
+namespace {
+__global__ void __launch_bounds__(256) epilogue_only_kernel(const Epilogue epi, float* y, int64_t n) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    epi_store(epi, y, i, 0.0f);
+}
+}  // namespace
+
+cudaError_t launch_epilogue_only(const Epilogue& epi, float* y, int64_t n, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 4096));
+  epilogue_only_kernel<<<blocks, 256, 0, stream>>>(epi, y, n);
   return cudaGetLastError();
 }
 

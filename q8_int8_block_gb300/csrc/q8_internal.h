@@ -9,6 +9,18 @@ namespace q8 {
 
 constexpr int kQK = 32;  // elements per Q8_0 block
 
+// Fused output step y = op(acc, aux) (see q8_epi.cuh); the default stores acc as binary32.
+enum : int { kEpiNone = 0, kEpiAdd = 1, kEpiSiluMul = 2 };
+struct Epilogue {
+  const float* aux = nullptr;  // [M,N] binary32: the residual (add) or the gate (silu_mul)
+  int op = kEpiNone;
+  int bf16 = 0;                // 1: y holds bfloat16 bits
+#ifdef __CUDACC__
+  __host__ __device__
+#endif
+  bool plain() const { return op == kEpiNone && bf16 == 0; }
+};
+
 struct DeviceInfo {
   int device = -1;
   int sm_count = 0;
@@ -46,7 +58,8 @@ size_t decode_smem_bytes(int64_t M, int64_t K, const DeviceInfo& dev);
 // block sums of given codes xq (x ignored; xd ignored).
 cudaError_t launch_decode(const void* x, int xtype, const int8_t* xq_in, const int8_t* Wq,
                           const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
-                          int64_t K, const DeviceInfo& dev, cudaStream_t stream);
+                          int64_t K, const DeviceInfo& dev, cudaStream_t stream,
+                          const Epilogue& epi = Epilogue());
 
 // ---- q8_batch.cu ------------------------------------------------------------------
 // Batched decode (2..kBatchMaxM tokens): weight streaming with mma.sync block sums.
@@ -58,14 +71,15 @@ size_t batch_ws_bytes(int64_t M, int64_t K);
 // y = linear(x), or (isum != nullptr) the raw block sums of the codes xq_in.
 cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const int8_t* Wq,
                          const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
-                         int64_t K, void* ws, const DeviceInfo& dev, cudaStream_t stream);
+                         int64_t K, void* ws, const DeviceInfo& dev, cudaStream_t stream,
+                         const Epilogue& epi = Epilogue());
 
 // ---- q8_dp4a.cu -------------------------------------------------------------------
 // The post's design: dp4a int8 GEMM on CUDA cores (prior-art comparison).  xq [M,K] int8,
 // xd [M,K/32] f32 from launch_quantize; y [M,N], or isum [M,N,K/32] when isum != nullptr.
 cudaError_t launch_dp4a_gemm(const int8_t* xq, const float* xd, const int8_t* Wq,
                              const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
-                             int64_t K, cudaStream_t stream);
+                             int64_t K, cudaStream_t stream, const Epilogue& epi = Epilogue());
 
 // ---- q8_gemm.cu -------------------------------------------------------------------
 // Tensor-core GEMM on binary16 codes: A16 [M,K] activation codes, B16 [N,K] weight codes,
@@ -79,6 +93,8 @@ int gemm_splits(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
 cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float* xd,
                            const uint16_t* Wd, float* y, int32_t* isum, float* part, int splits,
                            int64_t M, int64_t N, int64_t K, const DeviceInfo& dev,
-                           cudaStream_t stream);
+                           cudaStream_t stream, const Epilogue& epi = Epilogue());
+// y = op(0, aux) for K == 0 (an empty sum), M*N outputs.
+cudaError_t launch_epilogue_only(const Epilogue& epi, float* y, int64_t n, cudaStream_t stream);
 
 }  // namespace q8

@@ -88,3 +88,21 @@ def test_valid_call_without_gpu_fails_cleanly(L):
     st = L.q8_linear(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 2, 2, 64, None)
     assert st in (6, 7)
     assert L.q8_last_cuda_error()
+
+
+def test_fused_entry_rejects_bad_arguments(L):
+    F = L.q8_linear_fused
+    ok = [P(FAKE), 1, P(FAKE), P(FAKE), 1, P(FAKE), P(FAKE), 0, 2, 2, 64, 0, None, 0, None]
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return F(*a)
+    assert call(a4=3) == 4            # unknown epilogue
+    assert call(a7=2) == 4            # unknown output type
+    assert call(a1=5) == 4            # unknown activation type
+    assert call(a5=None) == 1         # residual / gate without aux
+    assert call(a5=P(FAKE + 4)) == 3  # misaligned aux
+    assert call(a6=None) == 1
+    assert call(a10=33) == 2
