@@ -39,7 +39,9 @@ def _load(path):
     L.oq8_f64_to_bf16.restype = ctypes.c_uint16
     L.oq8_silu.argtypes = [ctypes.c_double]
     L.oq8_silu.restype = ctypes.c_double
-    L.oq8_linear_epilogue.argtypes = [p, p, p, p, i64, i64, i64, p, ctypes.c_int, ctypes.c_int, p]
+    L.oq8_linear_epilogue.argtypes = [p, p, p, p, i64, i64, i64, p, p, ctypes.c_int, ctypes.c_int, p]
+    L.oq8_rmsnorm_quantize_act.argtypes = [p, ctypes.c_int, p, ctypes.c_double, i64, i64, p, p, p]
+    L.oq8_rmsnorm_quantize_act.restype = None
     L.oq8_linear_epilogue.restype = None
     for f in ("oq8_quantize_block", "oq8_quantize_weights", "oq8_quantize_act_f32",
               "oq8_quantize_act_bf16", "oq8_block_sums", "oq8_linear_codes",
@@ -196,10 +198,11 @@ def silu(g: float) -> float:
     return float(lib().oq8_silu(float(g)))
 
 
-def linear_epilogue(xq, xd, Wq, Wd, aux=None, op="none", out_bf16=False):
-    """y = op(rescaled block sums, aux) in binary64, rounded once to binary32 or to
-    bfloat16 (returned as uint16 bits).  op: "none", "add" (residual: y = acc + aux) or
-    "silu_mul" (gated unit: y = silu(aux) * acc)."""
+def linear_epilogue(xq, xd, Wq, Wd, aux=None, op="none", out_bf16=False, rowscale=None):
+    """y = op(rowscale[m] * rescaled block sums, aux) in binary64, rounded once to binary32
+    or to bfloat16 (returned as uint16 bits).  op: "none", "add" (residual: y = acc + aux)
+    or "silu_mul" (gated unit: y = silu(aux) * acc).  rowscale: binary64 [M] (the RMSNorm
+    factor r of rmsnorm_quantize_act) or None."""
     xq = np.ascontiguousarray(xq, dtype=np.int8)
     xd = np.ascontiguousarray(xd, dtype=np.float32)
     Wq = np.ascontiguousarray(Wq, dtype=np.int8)
@@ -208,6 +211,25 @@ def linear_epilogue(xq, xd, Wq, Wd, aux=None, op="none", out_bf16=False):
     N = Wq.shape[0]
     a = np.zeros((M, N), np.float32) if aux is None else np.ascontiguousarray(aux, dtype=np.float32)
     y = np.empty((M, N), np.uint16 if out_bf16 else np.float32)
-    lib().oq8_linear_epilogue(_ptr(xq), _ptr(xd), _ptr(Wq), _ptr(Wd), M, N, K, _ptr(a),
+    rs = None if rowscale is None else np.ascontiguousarray(rowscale, dtype=np.float64)
+    lib().oq8_linear_epilogue(_ptr(xq), _ptr(xd), _ptr(Wq), _ptr(Wd), M, N, K,
+                              None if rs is None else _ptr(rs), _ptr(a),
                               EPILOGUES[op], 1 if out_bf16 else 0, _ptr(y))
     return y
+
+
+def rmsnorm_quantize_act(x, gamma, eps, bf16=False):
+    """RMSNorm fused into the activation quantizer (readings N1-N3 of q8_oracle.c):
+    x [M,K] (float32, or bfloat16 bits as uint16 when bf16), gamma [K] float32, eps > 0 ->
+    (xq int8 [M,K]: codes of u = fl32(x * gamma), xd_u float32 [M,K/32]: scales of u,
+    r float64 [M] = 1 / sqrt(mean(x^2) + eps)).  The activation scale is xd_u * r."""
+    x = np.ascontiguousarray(x, dtype=np.uint16 if bf16 else np.float32)
+    gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+    M, K = x.shape
+    assert gamma.shape == (K,) and K % QK == 0
+    xq = np.empty((M, K), np.int8)
+    xd = np.empty((M, K // QK), np.float32)
+    r = np.empty(M, np.float64)
+    lib().oq8_rmsnorm_quantize_act(_ptr(x), 1 if bf16 else 0, _ptr(gamma), float(eps), M, K,
+                                   _ptr(xq), _ptr(xd), _ptr(r))
+    return xq, xd, r

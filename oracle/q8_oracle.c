@@ -341,21 +341,72 @@ static double oq8_epilogue_f64(double acc, int op, const float *aux, int64_t i)
     return acc;
 }
 
-/* y[M,N] = op(rescaled block sums, aux), stored as binary32 (ytype 0) or bfloat16 bits
- * (ytype 1).  aux is [M,N] binary32 (unused for op 0).  Single-threaded. */
+/* y[M,N] = op(rowscale[m] * rescaled block sums, aux), stored as binary32 (ytype 0) or
+ * bfloat16 bits (ytype 1).  aux is [M,N] binary32 (unused for op 0); rowscale is [M]
+ * binary64, or NULL for 1 (it carries the RMSNorm factor r, reading N1).
+ * Single-threaded. */
 void oq8_linear_epilogue(const int8_t *xq, const float *xd, const int8_t *Wq, const uint16_t *Wd,
-                         int64_t M, int64_t N, int64_t K, const float *aux, int op, int ytype,
-                         void *y)
+                         int64_t M, int64_t N, int64_t K, const double *rowscale, const float *aux,
+                         int op, int ytype, void *y)
 {
     int64_t nb = K / OQ8_QK;
     for (int64_t m = 0; m < M; ++m)
         for (int64_t n = 0; n < N; ++n) {
             int64_t i = m * N + n;
-            double v = oq8_epilogue_f64(
-                oq8_one_output_f64(xq + m * K, xd + m * nb, Wq + n * K, Wd + n * nb, K), op, aux, i);
+            double acc = oq8_one_output_f64(xq + m * K, xd + m * nb, Wq + n * K, Wd + n * nb, K);
+            if (rowscale != NULL)
+                acc = acc * rowscale[m];
+            double v = oq8_epilogue_f64(acc, op, aux, i);
             if (ytype == 1)
                 ((uint16_t *)y)[i] = oq8_f64_to_bf16(v);
             else
                 ((float *)y)[i] = (float)v;
         }
+}
+
+/* ---------------------------------------------------------------------------------- */
+/* RMSNorm fused into the activation quantizer (the layer's prologue).                  */
+/* In these hybrid blocks a projection's input is the RMS-normalised hidden state       */
+/* (root mean square layer normalisation, Zhang and Sennrich, NeurIPS 2019):             */
+/*   z[m,k] = x[m,k] * r[m] * gamma[k],   r[m] = 1 / sqrt(mean over k of x[m,k]^2 + eps). */
+/* Readings:                                                                             */
+/*   N1 r[m] is one factor per row, so it rides on the row's block scales: the codes    */
+/*      are those of u[m,k] = fl32(x[m,k] * gamma[k]) (R1-R8 applied to u) and the       */
+/*      activation scale is d_u[m,b] * r[m].  In exact arithmetic this is the            */
+/*      quantization of z itself (amax and every ratio u / d scale by r alike); it       */
+/*      keeps every code independent of how r is rounded.                               */
+/*   N2 the oracle evaluates r in binary64 from the exactly widened x and applies it to  */
+/*      y in binary64 before the one rounding (the kernels: binary32).                  */
+/*   N3 eps > 0 (the entry point rejects anything else), so r is finite; rows whose sum  */
+/*      of squares leaves the binary32 range are outside the domain, like NaN and Inf.   */
+/* ---------------------------------------------------------------------------------- */
+
+static float oq8_act_value(const void *x, int dtype, int64_t i)
+{
+    return dtype == 1 ? oq8_bf16_to_f32(((const uint16_t *)x)[i]) : ((const float *)x)[i];
+}
+
+/* x[M,K] (binary32, or bfloat16 bits for dtype 1), gamma[K] binary32 ->
+ * xq[M,K] codes of u, xd_u[M,K/32] binary32 scales of u, r[M] binary64. */
+void oq8_rmsnorm_quantize_act(const void *x, int dtype, const float *gamma, double eps, int64_t M,
+                              int64_t K, int8_t *xq, float *xd_u, double *r)
+{
+    int64_t nb = K / OQ8_QK;
+    float u[OQ8_QK];
+    for (int64_t m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double a = (double)oq8_act_value(x, dtype, m * K + k);
+            ss += a * a;
+        }
+        double mean = K > 0 ? ss / (double)K : 0.0;
+        r[m] = 1.0 / sqrt(mean + eps);
+        for (int64_t b = 0; b < nb; ++b) {
+            for (int j = 0; j < OQ8_QK; ++j) {
+                int64_t k = b * OQ8_QK + j;
+                u[j] = oq8_act_value(x, dtype, m * K + k) * gamma[k];
+            }
+            oq8_quantize_block(u, xq + m * K + b * OQ8_QK, xd_u + m * nb + b);
+        }
+    }
 }

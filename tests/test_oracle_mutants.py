@@ -13,6 +13,7 @@ import pytest
 
 from oracle import oracle as O
 from tests import test_oracle_epilogue as E
+from tests import test_oracle_norm as R
 from tests import test_oracle_pins as P
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle",
@@ -34,6 +35,11 @@ PINS = [
     E.test_zero_weights_give_aux,
     E.test_residual_and_gate_index_alignment,
     E.test_gated_unit_on_the_unit_code_closed_form,
+    R.test_constant_rows_closed_form,
+    lambda: R.test_two_level_rows(1.0, 3.0, 1e-6),
+    R.test_gamma_on_one_block_scales_only_that_block,
+    R.test_gamma_zero_on_odd_columns,
+    lambda: R.test_normalised_layer_within_the_quantization_bound(5, 7, 96, False),
 ]
 
 # (name, text in the source, replacement)
@@ -62,6 +68,15 @@ MUTANTS = [
      "double oq8_silu(double g) { return g / (1.0 + exp(g)); }"),
     ("gate from the wrong element", "return oq8_silu((double)aux[i]) * acc;",
      "return oq8_silu((double)aux[i / 2]) * acc;"),
+    ("norm mean over K - 1", "double mean = K > 0 ? ss / (double)K : 0.0;",
+     "double mean = K > 1 ? ss / (double)(K - 1) : 0.0;"),
+    ("norm eps outside the root", "r[m] = 1.0 / sqrt(mean + eps);", "r[m] = 1.0 / (sqrt(mean) + eps);"),
+    ("norm factor not inverted", "r[m] = 1.0 / sqrt(mean + eps);", "r[m] = sqrt(mean + eps);"),
+    ("norm mean of (x * gamma)^2", "double a = (double)oq8_act_value(x, dtype, m * K + k);",
+     "double a = (double)oq8_act_value(x, dtype, m * K + k) * gamma[k];"),
+    ("norm gamma one column off", "u[j] = oq8_act_value(x, dtype, m * K + k) * gamma[k];",
+     "u[j] = oq8_act_value(x, dtype, m * K + k) * gamma[(k + 1) % K];"),
+    ("norm row factor dropped", "acc = acc * rowscale[m];", "acc = acc;"),
 ]
 
 
