@@ -273,10 +273,11 @@ def time_graph_steps(torch, q8, step_fns, steps, warmup, instrument=True):
 
 
 def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=False, spec=None,
-             force_path=None, gated=None):
+             force_path=None, gated=None, norm=False):
     """gated: None (the plain layer, float32 y), "fused" (q8_linear_fused: y = silu(gate) *
     x.W^T stored as bfloat16 by the GEMM's own epilogue) or "unfused" (the plain layer, then
-    torch's silu, multiply and bfloat16 cast as separate kernels)."""
+    torch's silu, multiply and bfloat16 cast as separate kernels).  norm (with "fused"): x is
+    the un-normalised hidden state and its RMSNorm runs inside the layer's quantizer."""
     wname, p, mi = spec if spec is not None else CASES[name]
     wl = workloads.WORKLOADS[wname]
     W = wl.make_weights(p)
@@ -312,8 +313,10 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
         gate = torch.randn((M, N), device=dev, generator=gen) * 2.5
         yb = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         if gated == "fused":
+            nw = torch.rand(K, device=dev, generator=gen) + 0.5 if norm else None
             fns = [lambda i=i: q8.q8_linear_fused(x, Wqs[i], Wds[i], epi="silu_mul", aux=gate, y=yb,
-                                                  out_dtype=torch.bfloat16, path=path, workspace=ws)
+                                                  out_dtype=torch.bfloat16, path=path, workspace=ws,
+                                                  norm_weight=nw, norm_eps=1e-6)
                    for i in range(copies)]
         else:
             def unfused(i):
@@ -453,10 +456,14 @@ def gpu_arm(args):
                              ("decode_m64", 20000, None), ("prefill9b_up", 200, None),
                              ("prefill9b_down", 200, None), ("prefill9b_up", 50, "dp4a"),
                              ("decode_m1", 20000, "gated_fused"), ("decode_m1", 20000, "gated_unfused"),
-                             ("prefill9b_up", 200, "gated_fused"), ("prefill9b_up", 200, "gated_unfused")):
-            gated = fp[6:] if fp and fp.startswith("gated_") else None
+                             ("prefill9b_up", 200, "gated_fused"), ("prefill9b_up", 200, "gated_unfused"),
+                             ("decode_m1", 20000, "norm_gated_fused"),
+                             ("prefill9b_up", 200, "norm_gated_fused")):
+            norm = bool(fp) and fp.startswith("norm_")
+            tag = fp[5:] if norm else fp
+            gated = tag[6:] if tag and tag.startswith("gated_") else None
             e = run_case(torch, q8, dev, name, st, max(3, st // 50), pk, pk_src,
-                         force_path=None if gated else fp, gated=gated)
+                         force_path=None if gated else fp, gated=gated, norm=norm)
             key = name if fp is None else f"{name}_{fp}"
             extra[key] = {"value": round(e["value"], 3), "unit": e["unit"], "path": e["path"],
                           "us_per_step": round(e["t_max"] / st * 1e6, 3),
@@ -467,6 +474,9 @@ def gpu_arm(args):
             if gated == "fused":
                 extra[key]["note"] = ("gated FFN unit: y = silu(gate) * x.W^T, bfloat16 y, "
                                       "stored by the layer's epilogue (q8_linear_fused)")
+                if norm:
+                    extra[key]["note"] = ("RMSNorm + linear + SiLU gate + bfloat16 y in one call "
+                                          "(q8_linear_fused with norm_weight)")
             if gated == "unfused":
                 extra[key]["note"] = ("the same unit as the plain layer (float32 y) followed by "
                                       "torch silu, multiply and bfloat16 cast; us_per_step is "

@@ -54,7 +54,8 @@ typedef enum q8_status {
     Q8_ERR_NOMEM = 5,    /* workspace too small, or the library could not allocate one  */
     Q8_ERR_CUDA = 6,     /* a CUDA runtime call failed                                  */
     Q8_ERR_DEVICE = 7,   /* the current device is not compute capability 10.3           */
-    Q8_ERR_CAPTURE = 8   /* the call would allocate while its stream is being captured  */
+    Q8_ERR_CAPTURE = 8,  /* the call would allocate while its stream is being captured  */
+    Q8_ERR_VALUE = 9     /* a scalar argument is outside its domain (e.g. eps <= 0)      */
 } q8_status;
 
 typedef enum q8_dtype {
@@ -114,10 +115,30 @@ q8_status q8_linear_ex(const void* x, q8_dtype xtype, const int8_t* Wq, const ui
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * q8_quantize_act_rmsnorm -- RMSNorm fused into the Q8_0 activation quantizer.
+ * The layer's input in a transformer block is the RMS-normalised hidden state
+ * z = x * r * gamma, r = 1 / sqrt(mean_k x^2 + eps) (root mean square layer normalisation,
+ * Zhang and Sennrich, 2019).  r is one factor per row, so it rides on the row's block
+ * scales: xq holds the Q8_0 codes of fl32(x * gamma) and xd their binary32 scales times r
+ * (in exact arithmetic the quantization of z itself; the codes do not depend on how r is
+ * rounded).  r is summed in binary32 in a fixed order and also returned.
+ *   x [M,K] of type xtype, gamma [K] float in;  xq [M,K] int8, xd [M,K/32] float,
+ *   r [M] float out.  eps finite and > 0 (else Q8_ERR_VALUE).
+ */
+q8_status q8_quantize_act_rmsnorm(const void* x, q8_dtype xtype, const float* gamma, float eps,
+                                  int8_t* xq, float* xd, float* r, int64_t M, int64_t K,
+                                  cudaStream_t stream);
+
+/*
  * q8_linear_fused -- the linear layer with its neighbours in the surrounding block fused
- * into the output store.  The post runs its Q8_0 linears inside GDN + attention blocks
+ * into it.  The post runs its Q8_0 linears inside GDN + attention blocks
  * ("CUDA inference engine for running Qwen3.5/3.6 hybrid models on mining cards
- * (CMP 100-210)", news.hada.io topic 29953, feature list); the steps next to them are:
+ * (CMP 100-210)", news.hada.io topic 29953, feature list).  Before the product:
+ *   norm_weight != NULL: x is the un-normalised hidden state and the layer's input is its
+ *                    RMSNorm with weight norm_weight [K] float and norm_eps (as
+ *                    q8_quantize_act_rmsnorm, inside the layer's own quantizer);
+ *                    norm_weight NULL: x is the input itself.
+ * After it, in the output store:
  *   Q8_EPI_NONE      y = x . W^T
  *   Q8_EPI_ADD       y = x . W^T + aux              (residual add; aux [M,N] float)
  *   Q8_EPI_SILU_MUL  y = silu(aux) * (x . W^T)      (gated FFN unit: aux is the gate
@@ -131,18 +152,20 @@ q8_status q8_linear_ex(const void* x, q8_dtype xtype, const int8_t* Wq, const ui
  * growth and capture rules), otherwise the caller's.  With K == 0 the sum is empty and y is
  * the epilogue of zero.
  * Errors: Q8_ERR_DTYPE for an unknown epilogue, output or activation type; Q8_ERR_NULL for
- * a NULL aux with an epilogue that reads it; Q8_ERR_ALIGN for aux not 16-byte aligned;
- * the rest as q8_linear_ex.
+ * a NULL aux with an epilogue that reads it; Q8_ERR_ALIGN for aux or norm_weight not
+ * 16-byte aligned; Q8_ERR_VALUE for a norm_eps that is not finite and > 0; the rest as
+ * q8_linear_ex.
  */
 typedef enum q8_epilogue {
     Q8_EPI_NONE = 0,
     Q8_EPI_ADD = 1,
     Q8_EPI_SILU_MUL = 2
 } q8_epilogue;
-q8_status q8_linear_fused(const void* x, q8_dtype xtype, const int8_t* Wq, const uint16_t* Wd,
-                          q8_epilogue epi, const float* aux, void* y, q8_dtype ytype,
-                          int64_t M, int64_t N, int64_t K, q8_path path, void* workspace,
-                          size_t workspace_bytes, cudaStream_t stream);
+q8_status q8_linear_fused(const void* x, q8_dtype xtype, const float* norm_weight,
+                          float norm_eps, const int8_t* Wq, const uint16_t* Wd, q8_epilogue epi,
+                          const float* aux, void* y, q8_dtype ytype, int64_t M, int64_t N,
+                          int64_t K, q8_path path, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
 
 /* Bytes of scratch q8_linear_ex needs for this shape and path (0 if none). */
 size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path);

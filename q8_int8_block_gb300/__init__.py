@@ -11,6 +11,8 @@ this package fails.
     y = q8_linear(x, Wq, Wd)                     # x bf16 [M,K] -> float32 [M,N]
     y = q8_linear_ex(x, Wq, Wd, path="tensor", workspace=ws)
     y = q8_linear_fused(x, Wq, Wd, epi="silu_mul", aux=gate, out_dtype=torch.bfloat16)
+    y = q8_linear_fused(h, Wq, Wd, norm_weight=g, norm_eps=1e-6)   # RMSNorm(h) . W^T
+    xq, xd, r = q8_quantize_act_rmsnorm(h, g, 1e-6)
     isum = q8_block_sums(xq, Wq, path="decode")  # int32 [M,N,K/32]
 """
 import ctypes
@@ -18,7 +20,8 @@ import os
 
 import torch
 
-__all__ = ["Q8Error", "q8_quantize_weights", "q8_quantize_act", "q8_linear", "q8_linear_ex",
+__all__ = ["Q8Error", "q8_quantize_weights", "q8_quantize_act", "q8_quantize_act_rmsnorm",
+           "q8_linear", "q8_linear_ex",
            "q8_linear_fused", "EPILOGUES",
            "q8_linear_workspace_size", "q8_block_sums", "q8_device_error", "q8_release",
            "q8_set_timing_events", "q8_linear_noalloc", "NOALLOC_SCRATCH_BYTES",
@@ -29,7 +32,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libq8.so")
 
 STATUS = {0: "Q8_OK", 1: "Q8_ERR_NULL", 2: "Q8_ERR_SHAPE", 3: "Q8_ERR_ALIGN", 4: "Q8_ERR_DTYPE",
-          5: "Q8_ERR_NOMEM", 6: "Q8_ERR_CUDA", 7: "Q8_ERR_DEVICE", 8: "Q8_ERR_CAPTURE"}
+          5: "Q8_ERR_NOMEM", 6: "Q8_ERR_CUDA", 7: "Q8_ERR_DEVICE", 8: "Q8_ERR_CAPTURE",
+          9: "Q8_ERR_VALUE"}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 PATHS = {"auto": 0, "decode": 1, "tensor": 2, "batch": 3, "dp4a": 4}
 EPILOGUES = {"none": 0, "add": 1, "silu_mul": 2}
@@ -49,7 +53,7 @@ def _load():
         raise ImportError(f"libq8.so is not built ({_LIB_PATH}); run "
                           "`python -c 'import __graft_entry__ as g; g.build()'`")
     L = ctypes.CDLL(_LIB_PATH)
-    p, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    p, i64, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
     sigs = {
         "q8_quantize_weights": [p, p, p, i64, i64, p],
         "q8_quantize_act": [p, i32, p, p, i64, i64, p],
@@ -57,7 +61,8 @@ def _load():
         "q8_linear_ex": [p, i32, p, p, p, i64, i64, i64, i32, p, sz, p],
         "q8_block_sums": [p, p, p, i64, i64, i64, i32, p],
         "q8_linear_noalloc": [p, i32, p, p, p, i64, i64, i64, p],
-        "q8_linear_fused": [p, i32, p, p, i32, p, p, i32, i64, i64, i64, i32, p, sz, p],
+        "q8_linear_fused": [p, i32, p, f32, p, p, i32, p, p, i32, i64, i64, i64, i32, p, sz, p],
+        "q8_quantize_act_rmsnorm": [p, i32, p, f32, p, p, p, i64, i64, p],
     }
     for name, args in sigs.items():
         f = getattr(L, name)
@@ -147,6 +152,30 @@ def q8_quantize_act(x, xq=None, xd=None, stream=None):
     return xq, xd
 
 
+def q8_quantize_act_rmsnorm(x, gamma, eps, xq=None, xd=None, r=None, stream=None):
+    """RMSNorm fused into the activation quantizer: x bf16/float32 [M,K], gamma float32 [K]
+    -> (xq int8 [M,K]: codes of x * gamma, xd float32 [M,K/32]: their scales times r,
+    r float32 [M] = 1 / sqrt(mean(x^2) + eps))."""
+    M, K = x.shape
+    if x.dtype not in DTYPES:
+        raise TypeError(f"x: expected bfloat16 or float32, got {x.dtype}")
+    _need(x, x.dtype, (M, K), "x")
+    _need(gamma, torch.float32, (K,), "gamma")
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if xd is None:
+        xd = torch.empty((M, K // QK), dtype=torch.float32, device=x.device)
+    if r is None:
+        r = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _need(xq, torch.int8, (M, K), "xq")
+    _need(xd, torch.float32, (M, K // QK), "xd")
+    _need(r, torch.float32, (M,), "r")
+    _check(_L.q8_quantize_act_rmsnorm(_ptr(x), DTYPES[x.dtype], _ptr(gamma), float(eps), _ptr(xq),
+                                      _ptr(xd), _ptr(r), M, K, _stream(stream)),
+           "q8_quantize_act_rmsnorm")
+    return xq, xd, r
+
+
 def _lin_check(x, Wq, Wd, y):
     M, K = x.shape
     N = Wq.shape[0]
@@ -189,8 +218,9 @@ def q8_linear_ex(x, Wq, Wd, y=None, path="auto", workspace=None, stream=None):
 
 
 def q8_linear_fused(x, Wq, Wd, epi="none", aux=None, y=None, out_dtype=torch.float32,
-                    path="auto", workspace=None, stream=None):
-    """The linear layer with its neighbour fused into the output store:
+                    path="auto", workspace=None, stream=None, norm_weight=None, norm_eps=1e-6):
+    """The linear layer with its neighbours fused into it.  norm_weight (float32 [K]): the
+    input is RMSNorm(x) with that weight and norm_eps, applied inside the layer's quantizer.
     epi "none": y = x.W^T; "add": y = x.W^T + aux (residual); "silu_mul":
     y = silu(aux) * x.W^T (aux the gate projection's output).  aux float32 [M,N];
     y float32 or bfloat16 [M,N].  workspace None uses the library-owned scratch."""
@@ -210,8 +240,11 @@ def q8_linear_fused(x, Wq, Wd, epi="none", aux=None, y=None, out_dtype=torch.flo
         if aux is None:
             raise ValueError(f"epi {epi!r} needs aux")
         _need(aux, torch.float32, (M, N), "aux")
+    if norm_weight is not None:
+        _need(norm_weight, torch.float32, (K,), "norm_weight")
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(_L.q8_linear_fused(_ptr(x), DTYPES[x.dtype], _ptr(Wq), _ptr(Wd), EPILOGUES[epi],
+    _check(_L.q8_linear_fused(_ptr(x), DTYPES[x.dtype], _ptr(norm_weight), float(norm_eps),
+                              _ptr(Wq), _ptr(Wd), EPILOGUES[epi],
                               _ptr(aux), _ptr(y), DTYPES[out_dtype], M, N, K, PATHS[path],
                               _ptr(workspace), nbytes, _stream(stream)), "q8_linear_fused")
     return y

@@ -3,6 +3,7 @@
 //
 // Nothing is launched unless every check passes.  Every launch is asynchronous on the
 // caller's stream; the library holds no lock while kernels run.
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -128,6 +129,18 @@ size_t dp4a_ws_bytes(int64_t M, int64_t K) {
   return align256(static_cast<size_t>(M) * K) + align256(static_cast<size_t>(M) * (K / kQK) * 4);
 }
 
+// Scratch of a path: its own arrays, then a slot of M binary32 RMSNorm factors (used only
+// when the call normalises its input).
+size_t norm_slot_offset(q8_path p, int64_t M, int64_t N, int64_t K, int splits) {
+  return p == Q8_PATH_BATCH  ? batch_ws_bytes(M, K)
+         : p == Q8_PATH_DP4A ? dp4a_ws_bytes(M, K)
+                             : tensor_ws_bytes(M, N, K, splits);
+}
+size_t path_ws_bytes(q8_path p, int64_t M, int64_t N, int64_t K, int splits) {
+  if (p == Q8_PATH_DECODE || M == 0 || N == 0 || K == 0) return 0;
+  return norm_slot_offset(p, M, N, K, splits) + align256(static_cast<size_t>(M) * 4);
+}
+
 // Library-owned scratch for (current device, stream), grown on demand.
 q8_status library_workspace(const DeviceInfo& dev, cudaStream_t stream, size_t bytes, void** out) {
   *out = nullptr;
@@ -195,7 +208,7 @@ cudaError_t timed_launch(cudaStream_t stream, F&& launch) {
 q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uint16_t* Wd,
                       float* y, int64_t M, int64_t N, int64_t K, q8_path path, void* ws,
                       size_t ws_bytes, bool library_ws, cudaStream_t stream,
-                      const Epilogue& epi = Epilogue()) {
+                      const Epilogue& epi = Epilogue(), Prologue pro = Prologue()) {
   if (xtype != Q8_F32 && xtype != Q8_BF16) return Q8_ERR_DTYPE;
   if (path != Q8_PATH_AUTO && path != Q8_PATH_DECODE && path != Q8_PATH_TENSOR &&
       path != Q8_PATH_BATCH && path != Q8_PATH_DP4A)
@@ -219,12 +232,10 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
   if (p == Q8_PATH_DECODE)
     return launch_status(timed_launch(stream, [&] {
       return launch_decode(x, static_cast<int>(xtype), nullptr, Wq, Wd, y, nullptr, M, N, K, dev,
-                           stream, epi);
+                           stream, epi, pro);
     }));
   const int splits = gemm_splits(M, N, K, dev);
-  const size_t need = p == Q8_PATH_BATCH  ? batch_ws_bytes(M, K)
-                      : p == Q8_PATH_DP4A ? dp4a_ws_bytes(M, K)
-                                          : tensor_ws_bytes(M, N, K, splits);
+  const size_t need = path_ws_bytes(p, M, N, K, splits);
   if (library_ws) {
     if ((st = library_workspace(dev, stream, need, &ws)) != Q8_OK) return st;
   } else {
@@ -232,16 +243,23 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
     if (!aligned16(ws)) return Q8_ERR_ALIGN;
     if (ws_bytes < need) return Q8_ERR_NOMEM;
   }
+  if (pro.on()) {  // the rows' RMSNorm factors, read by the activation quantizer
+    float* r = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + norm_slot_offset(p, M, N, K, splits));
+    cudaError_t e = launch_row_rms(x, static_cast<int>(xtype), M, K, pro.eps, r, dev, stream);
+    if (e != cudaSuccess) return launch_status(e);
+    pro.r = r;
+  }
   if (p == Q8_PATH_BATCH)
     return launch_status(timed_launch(stream, [&] {
       return launch_batch(x, static_cast<int>(xtype), nullptr, Wq, Wd, y, nullptr, M, N, K, ws, dev,
-                          stream, epi);
+                          stream, epi, pro);
     }));
   if (p == Q8_PATH_DP4A) {
     int8_t* xq = static_cast<int8_t*>(ws);
     float* xdq = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
                                           align256(static_cast<size_t>(M) * K));
-    cudaError_t e = launch_quantize(x, static_cast<int>(xtype), xq, false, xdq, false, M, K, dev, stream);
+    cudaError_t e =
+        launch_quantize(x, static_cast<int>(xtype), xq, false, xdq, false, M, K, dev, stream, pro);
     if (e == cudaSuccess)
       e = timed_launch(stream, [&] {
         return launch_dp4a_gemm(xq, xdq, Wq, Wd, y, nullptr, M, N, K, stream, epi);
@@ -255,7 +273,8 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
                                               align256(static_cast<size_t>(M) * (K / kQK) * 4));
   float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(B16) +
                                          align256(static_cast<size_t>(N) * K * 2));
-  cudaError_t e = launch_quantize(x, static_cast<int>(xtype), A16, true, xd, false, M, K, dev, stream);
+  cudaError_t e =
+      launch_quantize(x, static_cast<int>(xtype), A16, true, xd, false, M, K, dev, stream, pro);
   if (e == cudaSuccess) e = launch_codes_to_f16(Wq, B16, N * K, dev, stream);
   if (e == cudaSuccess)
     e = timed_launch(stream, [&] {
@@ -295,6 +314,30 @@ q8_status q8_quantize_act(const void* x, q8_dtype xtype, int8_t* xq, float* xd, 
       launch_quantize(x, static_cast<int>(xtype), xq, false, xd, false, M, K, dev, stream));
 }
 
+q8_status q8_quantize_act_rmsnorm(const void* x, q8_dtype xtype, const float* gamma, float eps,
+                                  int8_t* xq, float* xd, float* r, int64_t M, int64_t K,
+                                  cudaStream_t stream) {
+  if (xtype != Q8_F32 && xtype != Q8_BF16) return Q8_ERR_DTYPE;
+  q8_status st = check_shape(M, 0, K);
+  if (st != Q8_OK) return st;
+  if (!(eps > 0.0f) || !std::isfinite(eps)) return Q8_ERR_VALUE;
+  if ((M * K > 0 && (x == nullptr || xq == nullptr || xd == nullptr)) ||
+      (K > 0 && gamma == nullptr) || (M > 0 && r == nullptr))
+    return Q8_ERR_NULL;
+  if (!aligned16(x) || !aligned16(xq) || !aligned16(xd) || !aligned16(gamma) || !aligned16(r))
+    return Q8_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != Q8_OK) return st;
+  cudaError_t e = launch_row_rms(x, static_cast<int>(xtype), M, K, eps, r, dev, stream);
+  Prologue pro;
+  pro.gamma = gamma;
+  pro.r = r;
+  pro.eps = eps;
+  if (e == cudaSuccess)
+    e = launch_quantize(x, static_cast<int>(xtype), xq, false, xd, false, M, K, dev, stream, pro);
+  return launch_status(e);
+}
+
 q8_status q8_linear(const void* x, const int8_t* Wq, const uint16_t* Wd, float* y, int64_t M,
                     int64_t N, int64_t K, cudaStream_t stream) {
   return linear_impl(x, Q8_BF16, Wq, Wd, y, M, N, K, Q8_PATH_AUTO, nullptr, 0, true, stream);
@@ -306,21 +349,28 @@ q8_status q8_linear_ex(const void* x, q8_dtype xtype, const int8_t* Wq, const ui
   return linear_impl(x, xtype, Wq, Wd, y, M, N, K, path, workspace, workspace_bytes, false, stream);
 }
 
-q8_status q8_linear_fused(const void* x, q8_dtype xtype, const int8_t* Wq, const uint16_t* Wd,
-                          q8_epilogue epi, const float* aux, void* y, q8_dtype ytype,
-                          int64_t M, int64_t N, int64_t K, q8_path path, void* workspace,
-                          size_t workspace_bytes, cudaStream_t stream) {
+q8_status q8_linear_fused(const void* x, q8_dtype xtype, const float* norm_weight,
+                          float norm_eps, const int8_t* Wq, const uint16_t* Wd, q8_epilogue epi,
+                          const float* aux, void* y, q8_dtype ytype, int64_t M, int64_t N,
+                          int64_t K, q8_path path, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
   if (epi != Q8_EPI_NONE && epi != Q8_EPI_ADD && epi != Q8_EPI_SILU_MUL) return Q8_ERR_DTYPE;
   if (ytype != Q8_F32 && ytype != Q8_BF16) return Q8_ERR_DTYPE;
   if (epi != Q8_EPI_NONE && M > 0 && N > 0 && aux == nullptr) return Q8_ERR_NULL;
-  if (!aligned16(aux)) return Q8_ERR_ALIGN;
+  if (!aligned16(aux) || !aligned16(norm_weight)) return Q8_ERR_ALIGN;
+  Prologue pro;
+  if (norm_weight != nullptr) {
+    if (!(norm_eps > 0.0f) || !std::isfinite(norm_eps)) return Q8_ERR_VALUE;
+    pro.gamma = norm_weight;
+    pro.eps = norm_eps;
+  }
   Epilogue e;
   e.aux = aux;
   e.op = static_cast<int>(epi);
   e.bf16 = ytype == Q8_BF16 ? 1 : 0;
   const bool library_ws = workspace == nullptr && workspace_bytes == 0;
   return linear_impl(x, xtype, Wq, Wd, static_cast<float*>(y), M, N, K, path, workspace,
-                     workspace_bytes, library_ws, stream, e);
+                     workspace_bytes, library_ws, stream, e, pro);
 }
 
 size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path) {
@@ -329,10 +379,7 @@ size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path) {
   if (current_device(&dev) != Q8_OK) return 0;
   q8_path p;
   if (resolve_path(M, N, K, path, dev, &p) != Q8_OK) return 0;
-  if (p == Q8_PATH_DECODE || M == 0 || N == 0 || K == 0) return 0;
-  if (p == Q8_PATH_DP4A) return dp4a_ws_bytes(M, K);
-  return p == Q8_PATH_BATCH ? batch_ws_bytes(M, K)
-                            : tensor_ws_bytes(M, N, K, gemm_splits(M, N, K, dev));
+  return path_ws_bytes(p, M, N, K, gemm_splits(M, N, K, dev));
 }
 
 q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64_t M, int64_t N,
@@ -405,6 +452,7 @@ const char* q8_status_string(q8_status s) {
     case Q8_ERR_CUDA: return "CUDA runtime error (see q8_last_cuda_error)";
     case Q8_ERR_DEVICE: return "current device is not compute capability 10.3";
     case Q8_ERR_CAPTURE: return "the call would allocate scratch while its stream is captured";
+    case Q8_ERR_VALUE: return "a scalar argument is outside its domain";
   }
   return "unknown status";
 }

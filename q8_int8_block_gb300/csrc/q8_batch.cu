@@ -425,11 +425,14 @@ __global__ void __maxnreg__(kMaxRegs)
 // writes them as two 8-byte halves: K 8 sub..+3 to piece 2 (sub & 1), K 8 sub+4..+7 to
 // piece 2 (sub & 1) + 1, in the piece's first half for sub < 2, second half otherwise.
 // kCodes: the input is int8 codes already (block-sum mode); no scales.
+// gamma / r: the RMSNorm prologue (nullptr: none): codes of fl32(x * gamma), scale d * r[m].
 template <typename InT, bool kCodes>
 __global__ void __launch_bounds__(256) quantize_batch_kernel(const InT* __restrict__ x,
                                                              uint16_t* __restrict__ xb,
                                                              float* __restrict__ xbd, int M,
-                                                             int TP, int nb) {
+                                                             int TP, int nb,
+                                                             const float* __restrict__ gamma,
+                                                             const float* __restrict__ r) {
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int sub = lane & 3;
@@ -462,7 +465,19 @@ __global__ void __launch_bounds__(256) quantize_batch_kernel(const InT* __restri
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
       }
+      if (gamma != nullptr) {
+        const int k = b * kQK + sub * 8;
+        const float4 g0 = __ldg(reinterpret_cast<const float4*>(gamma + k));
+        const float4 g1 = __ldg(reinterpret_cast<const float4*>(gamma + k) + 1);
+        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], g[i]);
+      }
       d = quantize_block_x4(v, group_mask, q);
+      if (r != nullptr) {
+        pdl_wait();  // r comes from the row-RMS kernel this one may overlap
+        d = __fmul_rn(d, r[m]);
+      }
     }
     const int p0 = 2 * (sub & 1);
     {
@@ -591,7 +606,7 @@ size_t batch_ws_bytes(int64_t M, int64_t K) {
 cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const int8_t* Wq,
                          const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
                          int64_t K, void* ws, const DeviceInfo& dev, cudaStream_t stream,
-                         const Epilogue& epi) {
+                         const Epilogue& epi, const Prologue& pro) {
   if (M == 0 || N == 0) return cudaSuccess;
   const BatchPlan pl = batch_plan(M, N, K, dev);
   if (pl.smem == 0 || ws == nullptr) return cudaErrorInvalidValue;
@@ -610,15 +625,37 @@ cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const in
     if (blocks > cap) blocks = cap;
     if (bs)
       quantize_batch_kernel<int8_t, true><<<blocks, 256, 0, stream>>>(
-          xq_in, xb, xbd, static_cast<int>(M), static_cast<int>(TP), static_cast<int>(nb));
-    else if (xtype == 1)
+          xq_in, xb, xbd, static_cast<int>(M), static_cast<int>(TP), static_cast<int>(nb), nullptr,
+          nullptr);
+    else if (pro.r == nullptr && xtype == 1)
       quantize_batch_kernel<uint16_t, false><<<blocks, 256, 0, stream>>>(
           static_cast<const uint16_t*>(x), xb, xbd, static_cast<int>(M), static_cast<int>(TP),
-          static_cast<int>(nb));
-    else
+          static_cast<int>(nb), pro.gamma, nullptr);
+    else if (pro.r == nullptr)
       quantize_batch_kernel<float, false><<<blocks, 256, 0, stream>>>(
           static_cast<const float*>(x), xb, xbd, static_cast<int>(M), static_cast<int>(TP),
-          static_cast<int>(nb));
+          static_cast<int>(nb), pro.gamma, nullptr);
+    else {
+      // after the row-RMS kernel (a normal launch, so x is complete when it starts): start
+      // early and wait for it only before reading r
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(blocks);
+      cfg.blockDim = dim3(256);
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      const int iM = static_cast<int>(M), iTP = static_cast<int>(TP), inb = static_cast<int>(nb);
+      cudaError_t e =
+          xtype == 1
+              ? cudaLaunchKernelEx(&cfg, quantize_batch_kernel<uint16_t, false>,
+                                   static_cast<const uint16_t*>(x), xb, xbd, iM, iTP, inb, pro.gamma, pro.r)
+              : cudaLaunchKernelEx(&cfg, quantize_batch_kernel<float, false>,
+                                   static_cast<const float*>(x), xb, xbd, iM, iTP, inb, pro.gamma, pro.r);
+      if (e != cudaSuccess) return e;
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

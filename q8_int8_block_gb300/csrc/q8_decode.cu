@@ -60,6 +60,7 @@ struct DecodeParams {
   int stages;          // S
   uint32_t* err;
   Epilogue epi;        // fused output step
+  Prologue pro;        // fused RMSNorm (gamma, eps): r is computed here and scales y
 };
 
 __device__ __forceinline__ void pdl_launch_dependents() {
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   // every phase before st's, so the parity names st's phase exactly, whatever the number
   // of stages and consumers.
   __shared__ volatile int issued;
+  __shared__ float rs_part[kConsumerWarps][8];  // RMSNorm: per-warp sums of squares
 
   const int K = p.K, N = p.N, M = p.M, R = p.rows_per_stage, S = p.stages;
   const int nb = K / kQK;
@@ -146,6 +148,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     const int ct = threadIdx.x - 32;
     constexpr int kCT = 32 * kConsumerWarps;
     pdl_wait();  // x, y: wait for the previous kernel in the stream
+    // RMSNorm: the quantize pass below also sums each token's squares (thread ct adds its
+    // blocks' in order; a fixed xor tree per warp; the warps' sums are added in order
+    // after the pass), and r scales the token's outputs at the store
+    const bool norm = !kBlockSums && p.pro.gamma != nullptr;
+    float ss[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) ss[t] = 0.0f;
     if constexpr (kBlockSums) {
       const int n16 = M * K / 16;
       for (int i = ct; i < n16; i += kCT)
@@ -168,6 +177,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
             v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
             v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
           }
+          if (norm) {  // codes of x * gamma
+            float s2 = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s2 = fmaf(v[i], v[i], s2);
+            const int tb = blk / nb;
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+              if (t == tb) ss[t] += s2;
+            const int k = (blk % nb) * kQK + sub * 8;
+            const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.pro.gamma + k));
+            const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.pro.gamma + k) + 1);
+            const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], g[i]);
+          }
           int q[8];
           const float d = quantize_block_x4(v, gmask, q);
           *reinterpret_cast<uint2*>(xs + off) = pack_codes_i8(q);
@@ -175,7 +199,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         }
       }
     }
+    if (norm) {
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss[t] += __shfl_xor_sync(0xFFFFFFFFu, ss[t], o);
+        if (lane == 0) rs_part[cw][t] = ss[t];
+      }
+    }
     asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory");
+    float rt = 1.0f;  // lane t < M: the RMSNorm factor of token t
+    if (norm && lane < M) {
+      float s = 0.0f;
+      for (int w = 0; w < kConsumerWarps; ++w) s += rs_part[w][lane];
+      rt = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(s, static_cast<float>(K)), p.pro.eps)));
+    }
 
     const int npieces = K >> 4;  // even, since K % 32 == 0
     const int iters = (npieces + 31) >> 5;
@@ -283,7 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
           // the butterfly leaves the same sum on every lane: lane t stores output t
-          if (lane == t && t < M) epi_put(p.epi, p.y, static_cast<int64_t>(t) * N + n, epi_apply(p.epi, a, ax));
+          if (lane == t && t < M)
+            epi_put(p.epi, p.y, static_cast<int64_t>(t) * N + n, epi_apply(p.epi, norm ? a * rt : a, ax));
         }
       }
     }
@@ -364,7 +403,7 @@ size_t decode_smem_bytes(int64_t M, int64_t K, const DeviceInfo& dev) {
 cudaError_t launch_decode(const void* x, int xtype, const int8_t* xq_in, const int8_t* Wq,
                           const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
                           int64_t K, const DeviceInfo& dev, cudaStream_t stream,
-                          const Epilogue& epi) {
+                          const Epilogue& epi, const Prologue& pro) {
   if (M == 0 || N == 0) return cudaSuccess;
   const bool bs = isum != nullptr;
   const Plan pl = plan_for(M, K, bs, dev);
@@ -384,6 +423,7 @@ cudaError_t launch_decode(const void* x, int xtype, const int8_t* xq_in, const i
   p.stages = pl.S;
   p.err = dev.err_word;
   p.epi = epi;
+  p.pro = pro;
   const int grid = static_cast<int>(N < dev.sm_count ? N : dev.sm_count);
   switch (mt_for(M)) {
     case 1: return launch_mt<1>(p, bs, pl.scales_in_stage, grid, pl.smem, stream, dev.device);

@@ -21,6 +21,20 @@ struct Epilogue {
   bool plain() const { return op == kEpiNone && bf16 == 0; }
 };
 
+// RMSNorm fused into the activation quantizer: the codes are those of fl32(x * gamma),
+// and the row's scales carry r = 1 / sqrt(mean(x^2) + eps).  gamma == nullptr: no norm.
+// r: [M] factors computed beforehand (launch_row_rms), or nullptr where the kernel computes
+// them itself (decode kernel).
+struct Prologue {
+  const float* gamma = nullptr;  // [K] binary32
+  const float* r = nullptr;      // [M] binary32
+  float eps = 0.0f;
+#ifdef __CUDACC__
+  __host__ __device__
+#endif
+  bool on() const { return gamma != nullptr; }
+};
+
 struct DeviceInfo {
   int device = -1;
   int sm_count = 0;
@@ -43,7 +57,10 @@ void forget_kernel_attributes();
 //   scale_f16 == false: binary32 scales;  true: binary16 scale bits.
 cudaError_t launch_quantize(const void* x, int xtype, void* codes, bool codes_f16, void* scales,
                             bool scale_f16, int64_t rows, int64_t K, const DeviceInfo& dev,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const Prologue& pro = Prologue());
+// r[m] = 1 / sqrt(sum_k x[m,k]^2 / K + eps) in binary32, summed in a fixed order.
+cudaError_t launch_row_rms(const void* x, int xtype, int64_t M, int64_t K, float eps, float* r,
+                           const DeviceInfo& dev, cudaStream_t stream);
 
 // int8 codes -> binary16 codes (n a multiple of 16).
 cudaError_t launch_codes_to_f16(const int8_t* q, uint16_t* out, int64_t n, const DeviceInfo& dev,
@@ -59,7 +76,7 @@ size_t decode_smem_bytes(int64_t M, int64_t K, const DeviceInfo& dev);
 cudaError_t launch_decode(const void* x, int xtype, const int8_t* xq_in, const int8_t* Wq,
                           const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
                           int64_t K, const DeviceInfo& dev, cudaStream_t stream,
-                          const Epilogue& epi = Epilogue());
+                          const Epilogue& epi = Epilogue(), const Prologue& pro = Prologue());
 
 // ---- q8_batch.cu ------------------------------------------------------------------
 // Batched decode (2..kBatchMaxM tokens): weight streaming with mma.sync block sums.
@@ -72,7 +89,7 @@ size_t batch_ws_bytes(int64_t M, int64_t K);
 cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const int8_t* Wq,
                          const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
                          int64_t K, void* ws, const DeviceInfo& dev, cudaStream_t stream,
-                         const Epilogue& epi = Epilogue());
+                         const Epilogue& epi = Epilogue(), const Prologue& pro = Prologue());
 
 // ---- q8_dp4a.cu -------------------------------------------------------------------
 // The post's design: dp4a int8 GEMM on CUDA cores (prior-art comparison).  xq [M,K] int8,

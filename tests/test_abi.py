@@ -41,7 +41,7 @@ def test_exported_symbols_are_declared():
 
 def test_status_strings_and_version(L):
     import q8_int8_block_gb300 as q8
-    for code in range(9):
+    for code in range(10):
         assert L.q8_status_string(code)
     assert q8.q8_version().count(".") == 2
 
@@ -92,17 +92,30 @@ def test_valid_call_without_gpu_fails_cleanly(L):
 
 def test_fused_entry_rejects_bad_arguments(L):
     F = L.q8_linear_fused
-    ok = [P(FAKE), 1, P(FAKE), P(FAKE), 1, P(FAKE), P(FAKE), 0, 2, 2, 64, 0, None, 0, None]
+    ok = [P(FAKE), 1, None, 1e-6, P(FAKE), P(FAKE), 1, P(FAKE), P(FAKE), 0, 2, 2, 64, 0, None, 0, None]
 
     def call(**kw):
         a = list(ok)
         for i, v in kw.items():
             a[int(i[1:])] = v
         return F(*a)
-    assert call(a4=3) == 4            # unknown epilogue
-    assert call(a7=2) == 4            # unknown output type
+    assert call(a6=3) == 4            # unknown epilogue
+    assert call(a9=2) == 4            # unknown output type
     assert call(a1=5) == 4            # unknown activation type
-    assert call(a5=None) == 1         # residual / gate without aux
-    assert call(a5=P(FAKE + 4)) == 3  # misaligned aux
-    assert call(a6=None) == 1
-    assert call(a10=33) == 2
+    assert call(a7=None) == 1         # residual / gate without aux
+    assert call(a7=P(FAKE + 4)) == 3  # misaligned aux
+    assert call(a8=None) == 1
+    assert call(a12=33) == 2
+    assert call(a2=P(FAKE + 4)) == 3  # misaligned norm weight
+    for eps in (0.0, -1e-6, float("nan"), float("inf")):
+        assert call(a2=P(FAKE), a3=eps) == 9
+
+
+def test_rmsnorm_quantizer_rejects_bad_arguments(L):
+    Q = L.q8_quantize_act_rmsnorm
+    ok = [P(FAKE), 1, P(FAKE), 1e-6, P(FAKE), P(FAKE), P(FAKE), 4, 64, None]
+    for i, v, want in ((1, 3, 4), (3, 0.0, 9), (3, float("nan"), 9), (2, None, 1), (6, None, 1),
+                       (2, P(FAKE + 8), 3), (8, 48, 2)):
+        a = list(ok)
+        a[i] = v
+        assert Q(*a) == want, (i, v)
