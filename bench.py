@@ -202,9 +202,11 @@ CASES = {
     "prefill27b_up": ("prefill27b", 0, 0), "prefill27b_down": ("prefill27b", 1, 0),
 }
 TRAFFIC_PROFILES = {  # committed ncu summaries that record DRAM bytes per launch
-    "decode_m1": ("decode_kernel_m1_k4096_n12288.md", ["q8_decode.cu", "q8_ptx.cuh", "q8_quant_dev.cuh"]),
-    "prefill9b_up": ("gemm_tc_kernel_m2048_k4096_n12288.md", ["q8_gemm.cu", "q8_ptx.cuh"]),
-    "decode_m16": ("batch_kernel_m16_k4096_n12288.md", ["q8_batch.cu", "q8_ptx.cuh", "q8_quant_dev.cuh"]),
+    "decode_m1": ("decode_kernel_m1_k4096_n12288.md",
+                  ["q8_decode.cu", "q8_ptx.cuh", "q8_quant_dev.cuh", "q8_epi.cuh"]),
+    "prefill9b_up": ("gemm_tc_kernel_m2048_k4096_n12288.md", ["q8_gemm.cu", "q8_ptx.cuh", "q8_epi.cuh"]),
+    "decode_m16": ("batch_kernel_m16_k4096_n12288.md",
+                   ["q8_batch.cu", "q8_ptx.cuh", "q8_quant_dev.cuh", "q8_epi.cuh"]),
 }
 
 
