@@ -139,7 +139,9 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 }
 
 // kNTG: the most token groups one warp handles (a warp handles ntg <= kNTG of them).
-template <bool kBlockSums, int kNTG>
+// kFused: the output store applies the epilogue (residual, SiLU gate, bfloat16 y); the
+// plain layer is a separate instantiation so that it carries none of that code.
+template <bool kBlockSums, int kNTG, bool kFused>
 __global__ void __maxnreg__(kMaxRegs)
     batch_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
                  const BatchParams p) {
@@ -225,7 +227,7 @@ __global__ void __maxnreg__(kMaxRegs)
     // ---------------- consumers --------------------------------------------------------
     const int cw = warp - 1;
     pdl_wait();  // x, y / isum: wait for the previous kernel before reading or writing
-    if constexpr (!kBlockSums) {
+    if constexpr (!kBlockSums && kFused) {
       // this CTA's aux rows (one per token) towards L2 for the epilogue
       const int nrow = (N - row0) < rows ? (N - row0) : rows;
       for (int t = cw; t < M; t += kConsumerWarps)
@@ -392,25 +394,37 @@ __global__ void __maxnreg__(kMaxRegs)
           }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
-        constexpr int kT = 32 * kConsumerWarps;
-        constexpr int kU = 4;  // outputs per thread whose aux loads are in flight together
-        for (int i0 = threadIdx.x - 32; i0 < M * rows; i0 += kU * kT) {
-          float a[kU];
+        if constexpr (kFused) {
+          constexpr int kT = 32 * kConsumerWarps;
+          constexpr int kU = 4;  // outputs per thread whose aux loads are in flight together
+          for (int i0 = threadIdx.x - 32; i0 < M * rows; i0 += kU * kT) {
+            float a[kU];
 #pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            const int i = i0 + u * kT;
-            const int t = i / rows, n = row0 + (i - t * rows);
-            a[u] = (i < M * rows && n < N) ? epi_aux(p.epi, static_cast<int64_t>(t) * N + n) : 0.0f;
+            for (int u = 0; u < kU; ++u) {
+              const int i = i0 + u * kT;
+              const int t = i / rows, n = row0 + (i - t * rows);
+              a[u] = (i < M * rows && n < N) ? epi_aux(p.epi, static_cast<int64_t>(t) * N + n) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+              const int i = i0 + u * kT;
+              const int t = i / rows, r = i - t * rows;
+              const int n = row0 + r;
+              if (i < M * rows && n < N) {
+                float v = 0.0f;
+                for (int k = 0; k < p.KPall; ++k) v += red[k * layer + t * rows + r];
+                epi_put(p.epi, p.y, static_cast<int64_t>(t) * N + n, epi_apply(p.epi, v, a[u]));
+              }
+            }
           }
-#pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            const int i = i0 + u * kT;
+        } else {  // the plain layer: binary32 y
+          for (int i = threadIdx.x - 32; i < M * rows; i += 32 * kConsumerWarps) {
             const int t = i / rows, r = i - t * rows;
             const int n = row0 + r;
-            if (i < M * rows && n < N) {
+            if (n < N) {
               float v = 0.0f;
               for (int k = 0; k < p.KPall; ++k) v += red[k * layer + t * rows + r];
-              epi_put(p.epi, p.y, static_cast<int64_t>(t) * N + n, epi_apply(p.epi, v, a[u]));
+              p.y[static_cast<int64_t>(t) * N + n] = v;
             }
           }
         }
@@ -573,10 +587,10 @@ BatchPlan batch_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
   return pl;
 }
 
-template <bool kBS, int kNTG>
+template <bool kBS, int kNTG, bool kFused = false>
 cudaError_t launch_batch_kernel(const CUtensorMap& tw, const CUtensorMap& ts, const BatchParams& p,
                                 int grid, size_t smem, cudaStream_t stream, int dev_id) {
-  auto fn = batch_kernel<kBS, kNTG>;
+  auto fn = batch_kernel<kBS, kNTG, kFused>;
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(fn), smem, dev_id);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -716,6 +730,12 @@ cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const in
     if (ntg_max <= 2) return launch_batch_kernel<true, 2>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
     if (ntg_max <= 4) return launch_batch_kernel<true, 4>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
     return launch_batch_kernel<true, 8>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
+  }
+  if (!epi.plain()) {
+    if (ntg_max <= 1) return launch_batch_kernel<false, 1, true>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
+    if (ntg_max <= 2) return launch_batch_kernel<false, 2, true>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
+    if (ntg_max <= 4) return launch_batch_kernel<false, 4, true>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
+    return launch_batch_kernel<false, 8, true>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
   }
   if (ntg_max <= 1) return launch_batch_kernel<false, 1>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);
   if (ntg_max <= 2) return launch_batch_kernel<false, 2>(tw, ts, p, pl.grid, pl.smem, stream, dev.device);

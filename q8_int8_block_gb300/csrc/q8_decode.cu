@@ -72,7 +72,9 @@ __device__ __forceinline__ int4 lds128(const void* p) { return *reinterpret_cast
 
 // kXP > 0: one token, K <= 512 * kXP; each lane always covers the same K positions, so it
 // keeps its activation codes and scales in registers instead of reading shared memory.
-template <int MT, bool kBlockSums, bool kScalesInStage, int kXP>
+// kFused: the fused neighbours (RMSNorm in the quantize pass, epilogue at the store); the
+// plain layer is a separate instantiation so that it carries none of that code.
+template <int MT, bool kBlockSums, bool kScalesInStage, int kXP, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
   pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     // RMSNorm: the quantize pass below also sums each token's squares (thread ct adds its
     // blocks' in order; a fixed xor tree per warp; the warps' sums are added in order
     // after the pass), and r scales the token's outputs at the store
-    const bool norm = !kBlockSums && p.pro.gamma != nullptr;
+    const bool norm = kFused && !kBlockSums && p.pro.gamma != nullptr;
     float ss[MT];
 #pragma unroll
     for (int t = 0; t < MT; ++t) ss[t] = 0.0f;
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     for (int j = cw; j < nrows; j += kConsumerWarps) {
       const int64_t n = r0 + j;
       float ax = 0.0f;  // lane t < M: aux of output (t, n), loaded before the row's weights land
-      if constexpr (!kBlockSums) {
+      if constexpr (!kBlockSums && kFused) {
         if (lane < M) ax = epi_aux(p.epi, static_cast<int64_t>(lane) * N + n);
       }
       const int st = j / R;
@@ -320,9 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           float a = acc[t];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
-          // the butterfly leaves the same sum on every lane: lane t stores output t
-          if (lane == t && t < M)
-            epi_put(p.epi, p.y, static_cast<int64_t>(t) * N + n, epi_apply(p.epi, norm ? a * rt : a, ax));
+          if constexpr (kFused) {
+            // the butterfly leaves the same sum on every lane: lane t stores output t
+            if (lane == t && t < M)
+              epi_put(p.epi, p.y, static_cast<int64_t>(t) * N + n, epi_apply(p.epi, norm ? a * rt : a, ax));
+          } else {
+            if (lane == 0 && t < M) p.y[static_cast<int64_t>(t) * N + n] = a;
+          }
         }
       }
     }
@@ -360,10 +366,10 @@ Plan plan_for(int64_t M, int64_t K, bool block_sums, const DeviceInfo& dev) {
   return pl;
 }
 
-template <int MT, bool kBS, bool kSc, int kXP = 0>
+template <int MT, bool kBS, bool kSc, int kXP = 0, bool kFused = false>
 cudaError_t launch_one(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream,
                        int dev_id) {
-  auto fn = decode_kernel<MT, kBS, kSc, kXP>;
+  auto fn = decode_kernel<MT, kBS, kSc, kXP, kFused>;
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(fn), smem, dev_id);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -379,19 +385,29 @@ cudaError_t launch_one(const DecodeParams& p, int grid, size_t smem, cudaStream_
   return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
+template <int MT, bool kFused>
+cudaError_t launch_y(const DecodeParams& p, bool sc, int grid, size_t smem, cudaStream_t stream,
+                     int dev_id) {
+  if constexpr (MT == 1) {
+    if (p.K <= 512 * kXRegPieces)  // activation codes in registers
+      return sc ? launch_one<1, false, true, kXRegPieces, kFused>(p, grid, smem, stream, dev_id)
+                : launch_one<1, false, false, kXRegPieces, kFused>(p, grid, smem, stream, dev_id);
+  }
+  return sc ? launch_one<MT, false, true, 0, kFused>(p, grid, smem, stream, dev_id)
+            : launch_one<MT, false, false, 0, kFused>(p, grid, smem, stream, dev_id);
+}
+
 template <int MT>
 cudaError_t launch_mt(const DecodeParams& p, bool bs, bool sc, int grid, size_t smem,
                       cudaStream_t stream, int dev_id) {
-  if constexpr (MT == 1) {
-    if (p.K <= 512 * kXRegPieces) {  // activation codes in registers
-      if (bs) return launch_one<1, true, false, kXRegPieces>(p, grid, smem, stream, dev_id);
-      return sc ? launch_one<1, false, true, kXRegPieces>(p, grid, smem, stream, dev_id)
-                : launch_one<1, false, false, kXRegPieces>(p, grid, smem, stream, dev_id);
+  if (bs) {
+    if constexpr (MT == 1) {
+      if (p.K <= 512 * kXRegPieces) return launch_one<1, true, false, kXRegPieces>(p, grid, smem, stream, dev_id);
     }
+    return launch_one<MT, true, false>(p, grid, smem, stream, dev_id);
   }
-  if (bs) return launch_one<MT, true, false>(p, grid, smem, stream, dev_id);
-  return sc ? launch_one<MT, false, true>(p, grid, smem, stream, dev_id)
-            : launch_one<MT, false, false>(p, grid, smem, stream, dev_id);
+  if (!p.epi.plain() || p.pro.on()) return launch_y<MT, true>(p, sc, grid, smem, stream, dev_id);
+  return launch_y<MT, false>(p, sc, grid, smem, stream, dev_id);
 }
 
 }  // namespace

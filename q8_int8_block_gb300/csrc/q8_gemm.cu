@@ -135,7 +135,9 @@ __device__ __forceinline__ void stage_scales(const GemmParams& p, int w, int m0,
   }
 }
 
-template <bool kBlockSums>
+// kFused: the drain's final store applies the epilogue (residual, SiLU gate, bfloat16 y);
+// the plain layer is a separate instantiation so that it carries none of that code.
+template <bool kBlockSums, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
@@ -311,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nbw = (nb - w * kWin) < kWin ? (nb - w * kWin) : kWin;
       if constexpr (!kBlockSums) {
         // the last window: bring this thread's 128 aux values towards L2 for the epilogue
-        if (w + 1 == w_end && p.part == nullptr && m_ok)
+        if (kFused && w + 1 == w_end && p.part == nullptr && m_ok)
           epi_prefetch(p.epi, static_cast<int64_t>(m) * N + n0 + wg * 128,
                        min(128, N - (n0 + wg * 128)));
       }
@@ -390,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* yrow = (p.part ? p.part + static_cast<int64_t>(blockIdx.y) * M * N : p.y) +
                       static_cast<int64_t>(m) * N;
         const int nbase = n0 + wg * 128;
-        if (p.part == nullptr && !p.epi.plain()) {
+        if (kFused && p.part == nullptr) {
           const int64_t r0 = static_cast<int64_t>(m) * N + nbase;
           if ((N & 3) == 0 && nbase + 128 <= N) {
             // 4 chunks of 32 columns; the 8 aux loads of chunk h + 1 are in flight while
@@ -508,10 +510,10 @@ __global__ void __launch_bounds__(256) reduce_splits_scalar_kernel(const float* 
   }
 }
 
-template <bool kBS>
+template <bool kBS, bool kFused = false>
 cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
                         cudaStream_t stream, int dev_id) {
-  auto fn = gemm_tc_kernel<kBS>;
+  auto fn = gemm_tc_kernel<kBS, kFused>;
   // setmaxnreg.inc waits until the registers exist: the split above is exact only if the
   // kernel was compiled for kLaunchRegs per thread.  Refuse to launch otherwise.
   int regs = 0;
@@ -562,7 +564,10 @@ cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
   if (isum) return launch_impl<true>(ta, tb, p, static_cast<int>(tiles), stream, dev.device);
-  cudaError_t e = launch_impl<false>(ta, tb, p, static_cast<int>(tiles), stream, dev.device);
+  // the epilogue runs in the drain unless split-K partials take the reduce kernel's
+  cudaError_t e = (splits == 1 && !epi.plain())
+                      ? launch_impl<false, true>(ta, tb, p, static_cast<int>(tiles), stream, dev.device)
+                      : launch_impl<false>(ta, tb, p, static_cast<int>(tiles), stream, dev.device);
   if (e != cudaSuccess || splits == 1) return e;
   const int64_t n = M * N;
   const int blocks = static_cast<int>(std::min<int64_t>((n / 4 + 255) / 256, 4 * dev.sm_count)) + 1;
