@@ -117,11 +117,10 @@ q8_status resolve_path(int64_t M, int64_t N, int64_t K, q8_path req, const Devic
 }
 
 // Scratch of the tensor path: A16 [M,K] f16 codes, xd [M,K/32] f32, B16 [N,K] f16 codes, and
-// with split-K the partial outputs [splits,M,N] f32.
-size_t tensor_ws_bytes(int64_t M, int64_t N, int64_t K, int splits) {
+// the GEMM's partial outputs (split-K, or its split tail wave: gemm_part_bytes).
+size_t tensor_ws_bytes(int64_t M, int64_t N, int64_t K, size_t part_bytes) {
   return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(M) * (K / kQK) * 4) +
-         align256(static_cast<size_t>(N) * K * 2) +
-         (splits > 1 ? align256(static_cast<size_t>(splits) * M * N * 4) : 0);
+         align256(static_cast<size_t>(N) * K * 2) + align256(part_bytes);
 }
 
 // Scratch of the dp4a path: int8 activation codes [M,K] and their scales [M,K/32].
@@ -131,14 +130,14 @@ size_t dp4a_ws_bytes(int64_t M, int64_t K) {
 
 // Scratch of a path: its own arrays, then a slot of M binary32 RMSNorm factors (used only
 // when the call normalises its input).
-size_t norm_slot_offset(q8_path p, int64_t M, int64_t N, int64_t K, int splits) {
+size_t norm_slot_offset(q8_path p, int64_t M, int64_t N, int64_t K, size_t part_bytes) {
   return p == Q8_PATH_BATCH  ? batch_ws_bytes(M, K)
          : p == Q8_PATH_DP4A ? dp4a_ws_bytes(M, K)
-                             : tensor_ws_bytes(M, N, K, splits);
+                             : tensor_ws_bytes(M, N, K, part_bytes);
 }
-size_t path_ws_bytes(q8_path p, int64_t M, int64_t N, int64_t K, int splits) {
+size_t path_ws_bytes(q8_path p, int64_t M, int64_t N, int64_t K, size_t part_bytes) {
   if (p == Q8_PATH_DECODE || M == 0 || N == 0 || K == 0) return 0;
-  return norm_slot_offset(p, M, N, K, splits) + align256(static_cast<size_t>(M) * 4);
+  return norm_slot_offset(p, M, N, K, part_bytes) + align256(static_cast<size_t>(M) * 4);
 }
 
 // Library-owned scratch for (current device, stream), grown on demand.
@@ -235,7 +234,8 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
                            stream, epi, pro);
     }));
   const int splits = gemm_splits(M, N, K, dev);
-  const size_t need = path_ws_bytes(p, M, N, K, splits);
+  const size_t part_bytes = gemm_part_bytes(M, N, K, dev);
+  const size_t need = path_ws_bytes(p, M, N, K, part_bytes);
   if (library_ws) {
     if ((st = library_workspace(dev, stream, need, &ws)) != Q8_OK) return st;
   } else {
@@ -244,7 +244,7 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
     if (ws_bytes < need) return Q8_ERR_NOMEM;
   }
   if (pro.on()) {  // the rows' RMSNorm factors, read by the activation quantizer
-    float* r = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + norm_slot_offset(p, M, N, K, splits));
+    float* r = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + norm_slot_offset(p, M, N, K, part_bytes));
     cudaError_t e = launch_row_rms(x, static_cast<int>(xtype), M, K, pro.eps, r, dev, stream);
     if (e != cudaSuccess) return launch_status(e);
     pro.r = r;
@@ -379,7 +379,7 @@ size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path) {
   if (current_device(&dev) != Q8_OK) return 0;
   q8_path p;
   if (resolve_path(M, N, K, path, dev, &p) != Q8_OK) return 0;
-  return path_ws_bytes(p, M, N, K, gemm_splits(M, N, K, dev));
+  return path_ws_bytes(p, M, N, K, gemm_part_bytes(M, N, K, dev));
 }
 
 q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64_t M, int64_t N,

@@ -69,8 +69,13 @@ struct GemmParams {
   const float* xd;     // [M, nb]
   const uint16_t* Wd;  // [N, nb]
   float* y;            // [M, N]
-  float* part;         // [splits, M, N] partial outputs (split-K), or nullptr
+  float* part;         // split-K partial outputs: [splits, M, N]; in tail mode [unit, BM, BN]
   int splits;          // K split into this many ranges of whole scale windows (blockIdx.y)
+  // Tail mode (tail_splits > 0): blocks [0, main_tiles) are whole tiles (K not split);
+  // the tiles of the last, partial wave are split tail_splits ways along K, one block per
+  // (tile, range) unit, and their partial outputs are added by reduce_tail_kernel.
+  int main_tiles;
+  int tail_splits;
   int32_t* isum;       // [M, N, nb] (block-sum mode)
   int M, N, K;
   uint32_t* err;
@@ -155,15 +160,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   // [b_begin, b_end) and 64-wide stages [kb_begin, kb_end); ring slots, TMEM buffers and
   // barrier phases count from the start of the range
   const int nwin_all = (nb + kWin - 1) / kWin;
-  const int w_begin = static_cast<int>(static_cast<int64_t>(blockIdx.y) * nwin_all / p.splits);
-  const int w_end = static_cast<int>(static_cast<int64_t>(blockIdx.y + 1) * nwin_all / p.splits);
+  int tile = static_cast<int>(blockIdx.x), split = static_cast<int>(blockIdx.y), nsplit = p.splits;
+  const bool tail = !kBlockSums && p.tail_splits > 0 && tile >= p.main_tiles;
+  if (tail) {
+    const int u = tile - p.main_tiles;
+    tile = p.main_tiles + u / p.tail_splits;
+    split = u % p.tail_splits;
+    nsplit = p.tail_splits;
+  }
+  // this block stores final outputs (else partial sums for a reduction kernel)
+  const bool direct = p.splits == 1 && !tail;
+  const int w_begin = static_cast<int>(static_cast<int64_t>(split) * nwin_all / nsplit);
+  const int w_end = static_cast<int>(static_cast<int64_t>(split + 1) * nwin_all / nsplit);
   const int b_begin = w_begin * kWin;
   const int b_end = (w_end * kWin < nb) ? w_end * kWin : nb;
   const int kb_begin = b_begin / 2;
   const int kb_end = (b_end + 1) / 2;
   const int mtiles = (M + BM - 1) / BM;
-  const int m0 = (blockIdx.x % mtiles) * BM;
-  const int n0 = (blockIdx.x / mtiles) * BN;
+  const int m0 = (tile % mtiles) * BM;
+  const int n0 = (tile / mtiles) * BN;
 
   // 1024-byte aligned carve-up (128-byte swizzle atoms must sit on 1024-byte boundaries)
   const uint32_t raw = smem_u32(smem_raw);
@@ -313,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nbw = (nb - w * kWin) < kWin ? (nb - w * kWin) : kWin;
       if constexpr (!kBlockSums) {
         // the last window: bring this thread's 128 aux values towards L2 for the epilogue
-        if (kFused && w + 1 == w_end && p.part == nullptr && m_ok)
+        if (kFused && direct && w + 1 == w_end && m_ok)
           epi_prefetch(p.epi, static_cast<int64_t>(m) * N + n0 + wg * 128,
                        min(128, N - (n0 + wg * 128)));
       }
@@ -388,11 +403,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if constexpr (!kBlockSums) {
-      if (m_ok && !failed) {
-        float* yrow = (p.part ? p.part + static_cast<int64_t>(blockIdx.y) * M * N : p.y) +
+      if (m_ok && !failed && tail) {
+        // this unit's partial tile, compact: [unit][BM][BN], no bounds past N to mind
+        float* dst = p.part + (static_cast<int64_t>(blockIdx.x - p.main_tiles) * BM + row) * BN + wg * 128;
+#pragma unroll
+        for (int i = 0; i < 64; i += 2)
+          *reinterpret_cast<float4*>(dst + 2 * i) = make_float4(acc[i].x, acc[i].y, acc[i + 1].x, acc[i + 1].y);
+      } else if (m_ok && !failed) {
+        float* yrow = (p.splits > 1 ? p.part + static_cast<int64_t>(blockIdx.y) * M * N : p.y) +
                       static_cast<int64_t>(m) * N;
         const int nbase = n0 + wg * 128;
-        if (kFused && p.part == nullptr) {
+        if (kFused && direct) {
           const int64_t r0 = static_cast<int64_t>(m) * N + nbase;
           if ((N & 3) == 0 && nbase + 128 <= N) {
             // 4 chunks of 32 columns; the 8 aux loads of chunk h + 1 are in flight while
@@ -510,6 +531,42 @@ __global__ void __launch_bounds__(256) reduce_splits_scalar_kernel(const float* 
   }
 }
 
+// Tail mode: y of the tail tiles = sum over its S units' partial tiles (in unit order: the
+// result does not depend on timing), through the epilogue.  Four columns per thread.
+__global__ void __launch_bounds__(256) reduce_tail_kernel(const float* __restrict__ part, float* y,
+                                                          int M, int N, int mtiles, int main_tiles,
+                                                          int ntail, int S, const Epilogue epi) {
+  const int64_t n4 = static_cast<int64_t>(ntail) * BM * (BN / 4);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int tt = static_cast<int>(i / (BM * (BN / 4)));
+    const int rem = static_cast<int>(i - static_cast<int64_t>(tt) * BM * (BN / 4));
+    const int row = rem / (BN / 4), col = 4 * (rem % (BN / 4));
+    const int tile = main_tiles + tt;
+    const int m = (tile % mtiles) * BM + row, n = (tile / mtiles) * BN + col;
+    if (m >= M || n >= N) continue;
+    const float* src = part + (static_cast<int64_t>(tt) * S * BM + row) * BN + col;
+    float4 a = *reinterpret_cast<const float4*>(src);
+    for (int s = 1; s < S; ++s) {
+      const float4 b = *reinterpret_cast<const float4*>(src + static_cast<int64_t>(s) * BM * BN);
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    const int64_t o = static_cast<int64_t>(m) * N + n;
+    if ((N & 3) == 0 && n + 4 <= N) {
+      if (epi.plain())
+        *reinterpret_cast<float4*>(y + o) = a;
+      else
+        epi_put4(epi, y, o, epi_apply4(epi, a, epi_aux4(epi, o)));
+    } else {
+      const float v[4] = {a.x, a.y, a.z, a.w};
+      for (int c = 0; c < 4 && n + c < N; ++c) epi_store(epi, y, o + c, v[c]);
+    }
+  }
+}
+
 template <bool kBS, bool kFused = false>
 cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
                         cudaStream_t stream, int dev_id) {
@@ -527,6 +584,30 @@ cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const GemmPa
 }
 
 }  // namespace
+
+// Tail mode: when the tiles fill some whole waves of the GPU plus a partial one, the
+// partial wave's tiles are split along K so that they spread over the idle SMs (at most
+// one range per scale window).  Returns the split (0: tail mode off).
+int gemm_tail_splits(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+  if (M <= 0 || N <= 0 || K <= 0 || dev.sm_count <= 0) return 0;
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  if (tiles < dev.sm_count) return 0;  // one partial wave: uniform split-K instead
+  const int64_t tail = tiles % dev.sm_count;
+  if (tail == 0) return 0;
+  const int64_t nwin = (K / kQK + kWin - 1) / kWin;
+  int64_t s = dev.sm_count / tail;
+  if (s > nwin) s = nwin;
+  return s >= 2 ? static_cast<int>(s) : 0;
+}
+
+size_t gemm_part_bytes(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+  const int splits = gemm_splits(M, N, K, dev);
+  if (splits > 1) return static_cast<size_t>(splits) * M * N * 4;
+  const int S = gemm_tail_splits(M, N, K, dev);
+  if (S == 0) return 0;
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  return static_cast<size_t>(tiles % dev.sm_count) * S * BM * BN * 4;
+}
 
 int gemm_splits(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
   if (M <= 0 || N <= 0 || K <= 0 || dev.sm_count <= 0) return 1;
@@ -556,19 +637,36 @@ cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float
   if (isum != nullptr || splits < 1 || part == nullptr) splits = 1;  // block sums: one range
   p.splits = splits;
   p.part = splits > 1 ? part : nullptr;
+  // tail mode: needs the caller's partial buffer (sized by gemm_part_bytes); y only
+  const int64_t mtiles = (M + BM - 1) / BM;
+  const int64_t tiles0 = mtiles * ((N + BN - 1) / BN);
+  const int S = (isum == nullptr && splits == 1 && part != nullptr) ? gemm_tail_splits(M, N, K, dev) : 0;
+  const int64_t ntail = S > 0 ? tiles0 % dev.sm_count : 0;
+  p.main_tiles = static_cast<int>(tiles0 - ntail);
+  p.tail_splits = S;
+  if (S > 0) p.part = part;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.err = dev.err_word;
   p.epi = epi;
-  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int64_t tiles = tiles0 - ntail + ntail * S;  // whole tiles, then the tail's units
   if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
   if (isum) return launch_impl<true>(ta, tb, p, static_cast<int>(tiles), stream, dev.device);
   // the epilogue runs in the drain unless split-K partials take the reduce kernel's
   cudaError_t e = (splits == 1 && !epi.plain())
                       ? launch_impl<false, true>(ta, tb, p, static_cast<int>(tiles), stream, dev.device)
                       : launch_impl<false>(ta, tb, p, static_cast<int>(tiles), stream, dev.device);
-  if (e != cudaSuccess || splits == 1) return e;
+  if (e != cudaSuccess) return e;
+  if (S > 0) {
+    const int64_t n4 = ntail * BM * (BN / 4);
+    const int blocks = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, 4 * dev.sm_count));
+    reduce_tail_kernel<<<blocks, 256, 0, stream>>>(part, y, static_cast<int>(M), static_cast<int>(N),
+                                                   static_cast<int>(mtiles), p.main_tiles,
+                                                   static_cast<int>(ntail), S, epi);
+    return cudaGetLastError();
+  }
+  if (splits == 1) return e;
   const int64_t n = M * N;
   const int blocks = static_cast<int>(std::min<int64_t>((n / 4 + 255) / 256, 4 * dev.sm_count)) + 1;
   if (n % 4 == 0)

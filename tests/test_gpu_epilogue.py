@@ -190,3 +190,21 @@ def test_fused_gated_unit_full_size(q8, name, p):
     ref = O.linear_epilogue(xq_ref, xd_ref, Wq_ref, Wd_ref, gate[rows], "silu_mul", out_bf16=True)
     assert_bf16_close(got[rows], ref, f"{name} gated unit (rows {rows.tolist()})")
     assert q8.q8_device_error() == 0
+
+
+@pytest.mark.parametrize("op,bf16", [("silu_mul", True), ("add", False)])
+def test_fused_epilogue_on_the_split_tail_wave(q8, op, bf16):
+    """154 tiles on the GPU's 152 SMs: whole tiles apply the epilogue in the GEMM drain, the
+    two tail tiles (split along K) in the tail reduction; both must match the oracle."""
+    M, N, K = 129, 19556, 544
+    rng = np.random.default_rng(77)
+    W, x, xq_ref, xd_ref, Wq_ref, Wd_ref, aux = _inputs(rng, M, N, K, op)
+    Wq, Wd = q8.q8_quantize_weights(T(W))
+    out = torch.bfloat16 if bf16 else torch.float32
+    y = q8.q8_linear_fused(T(x), Wq, Wd, epi=op, aux=T(aux), out_dtype=out, path="tensor")
+    ref = O.linear_epilogue(xq_ref, xd_ref, Wq_ref, Wd_ref, aux, op, out_bf16=bf16)
+    if bf16:
+        assert_bf16_close(torch_bits(y), ref, f"tail {op} bf16")
+    else:
+        assert_close(y.cpu().numpy(), ref, f"tail {op}")
+    assert q8.q8_device_error() == 0

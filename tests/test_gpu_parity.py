@@ -249,7 +249,7 @@ def test_library_workspace_matches_caller_workspace_and_is_deterministic(q8):
 def test_outputs_stay_inside_their_buffers(q8):
     rng = np.random.default_rng(13)
     for (M, N, K, path) in ((5, 77, 256, "decode"), (131, 259, 96, "tensor"), (13, 77, 256, "batch"),
-                            (64, 3001, 512, "batch")):
+                            (64, 3001, 512, "batch"), (129, 19556, 544, "tensor")):
         W = workloads.weights(rng, N, K)
         x, _ = workloads.activations(rng, M, K)
         Wq, Wd = q8.q8_quantize_weights(T(W))
@@ -314,4 +314,24 @@ def test_dp4a_path_full_size_prefill(q8):
     ref = O.linear_codes_at(xq_ref, xd_ref, Wq_ref, Wd_ref, rows, cols)
     assert_close(y[rows, cols], ref, "dp4a prefill9b up (sampled)")
     assert np.all(np.isfinite(y))
+    assert q8.q8_device_error() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(129, 19556, 544), (300, 20480, 1056)])
+def test_tensor_path_split_tail_wave(q8, M, N, K):
+    """Shapes whose tiles fill whole waves of the GPU plus a few: the tail tiles are split
+    along K and reduced separately.  (129, 19556): 154 tiles of 128 x 256, the tail holds
+    the last, ragged column tile at both row tiles (one of them a single row); K = 544 makes
+    the two K ranges 16 and 1 blocks.  Element by element, and deterministic."""
+    rng = np.random.default_rng(M + N)
+    W = workloads.weights(rng, N, K)
+    x, _ = workloads.activations(rng, M, K, bf16=True, outlier_frac=0.02)
+    Wq_ref, Wd_ref = O.quantize_weights(W)
+    y_ref = O.linear(x, Wq_ref, Wd_ref, bf16=True)
+    Wq, Wd = q8.q8_quantize_weights(T(W))
+    y = q8.q8_linear_ex(T(x), Wq, Wd, path="tensor")
+    y2 = q8.q8_linear_ex(T(x), Wq, Wd, path="tensor")
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    assert_close(y.cpu().numpy(), y_ref, f"tensor tail M={M} N={N} K={K}")
     assert q8.q8_device_error() == 0
