@@ -392,6 +392,33 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
     return out
 
 
+def run_kv3(torch, q8, dev, steps, warmup, pk, pk_src):
+    """The 3-bit KV-cache codec on one attention layer's keys at a 256K-token context
+    (262144 tokens x 4 heads x 256 channels, bf16): encode and decode, each timed alone.
+    Algorithmic bytes per group: 256 (bf16 values) + 48 (codes) + 4 (scale)."""
+    rng = np.random.default_rng(12)
+    x_np = workloads.kv_groups(rng, **workloads.KV3_LAYER_256K)
+    x = torch.from_numpy(x_np.view(np.int16)).to(dev).view(torch.bfloat16)
+    n = x.shape[0]
+    codes = torch.empty((n, 12), dtype=torch.int32, device=dev)
+    scales = torch.empty((n,), dtype=torch.float32, device=dev)
+    out = torch.empty((n, 128), dtype=torch.bfloat16, device=dev)
+    bytes_step = n * (256 + 48 + 4)
+    res = {}
+    for name, fn in (("kv3_encode_256k", lambda: q8.q8_kv3_encode(x, codes=codes, scales=scales)),
+                     ("kv3_decode_256k", lambda: q8.q8_kv3_decode(codes, scales, torch.bfloat16, out=out))):
+        fn()
+        total, kern = time_graph_steps(torch, q8, [fn], steps, warmup, instrument=False)
+        gbs = bytes_step / kern / 1e9
+        res[name] = {"value": round(gbs, 2), "unit": "GB/s", "us_per_step": round(kern * 1e6, 3),
+                     "groups": n, "algorithmic_bytes_per_launch": bytes_step,
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": pk["hbm_gbs"],
+                                  "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                                  "peak_source": f"hbm_gbs of the {pk_src} peaks"},
+                     "steps": steps}
+    return res
+
+
 def e2e_measure(torch, q8, dev, x_np, bf16, Wqs, Wds, M, N, K, steps, warmup, bytes_step, ops_step,
                 bound, path=None):
     """End to end through the public call q8_linear / q8_linear_ex: per step the H2D copy of x
@@ -483,6 +510,10 @@ def gpu_arm(args):
                 extra[key]["note"] = ("the same unit as the plain layer (float32 y) followed by "
                                       "torch silu, multiply and bfloat16 cast; us_per_step is "
                                       "the whole step, roofline the layer's kernel alone")
+        extra.update(run_kv3(torch, q8, dev, 200, 10, pk, pk_src))
+        for k in ("kv3_encode_256k", "kv3_decode_256k"):
+            extra[k]["note"] = ("3-bit KV-cache codec (Walsh-Hadamard rotation + Lloyd-Max), "
+                                "one attention layer's keys at a 256K-token context")
     err = q8.q8_device_error()
     wname = CASES[args.workload][0]
     desc = {"decode": "decode GEMV, FFN up-projection of a dense ~9B-class layer",

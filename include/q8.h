@@ -167,6 +167,30 @@ q8_status q8_linear_fused(const void* x, q8_dtype xtype, const float* norm_weigh
                           int64_t K, q8_path path, void* workspace, size_t workspace_bytes,
                           cudaStream_t stream);
 
+/*
+ * 3-bit KV-cache codec: Walsh-Hadamard rotation + Lloyd-Max quantizer.  The post keeps a
+ * 256K-token context in a 3-bit KV cache built from these two parts, 17 GB -> 3.5 GB
+ * ("CUDA inference engine for running Qwen3.5/3.6 hybrid models on mining cards
+ * (CMP 100-210)", news.hada.io topic 29953, feature list).
+ * A group is 128 consecutive elements of a key or value vector (a 256-wide head is two
+ * groups).  Per group: codes[12] uint32, the 128 three-bit codes as a little-endian bit
+ * stream (element i at bits [3i, 3i + 3)), and one float scale: 52 bytes instead of 256
+ * (bf16), 3.25 bits per element.
+ *   encode: u = unnormalised Walsh-Hadamard transform of the group (binary32); s = the RMS
+ *           of u (pairwise sum of the squares); code_i = 4 * (u_i < 0) + the number of
+ *           thresholds t in (0.5006, 1.0500, 1.7480) with |u_i| >= t * s (the 8-level
+ *           unit-Gaussian Lloyd-Max quantizer, Max 1960); s == 0 gives codes 0.
+ *   decode: w_i = s * (+-level), levels (0.2451, 0.7560, 1.3440, 2.1520);
+ *           out = WHT(w) / 128, binary32 or bfloat16 (round to nearest even).
+ *   x [ngroups][128] of type xtype; codes [ngroups][12]; scales [ngroups];
+ *   out [ngroups][128] of type otype.  ngroups >= 0; device pointers, 16-byte aligned.
+ *   Domain: finite groups whose sum of squares stays within binary32 (|x| below ~1e18).
+ */
+q8_status q8_kv3_encode(const void* x, q8_dtype xtype, uint32_t* codes, float* scales,
+                        int64_t ngroups, cudaStream_t stream);
+q8_status q8_kv3_decode(const uint32_t* codes, const float* scales, void* out, q8_dtype otype,
+                        int64_t ngroups, cudaStream_t stream);
+
 /* Bytes of scratch q8_linear_ex needs for this shape and path (0 if none). */
 size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path);
 

@@ -32,6 +32,10 @@
  *   K6 decode: w_i = fl32(s * (+-level)), then x_i = WHT(w)_i / 128 (an exact scaling, as
  *      the unnormalised WHT applied twice is 128 times the identity), rounded to bfloat16
  *      (nearest even) when the output is bfloat16.
+ *   K7 domain: finite groups whose sum of squares stays inside the binary32 range
+ *      (|x| below about 1e18); beyond it s overflows and the decoder meets inf - inf.  Like
+ *      NaN and Inf inputs, such groups are outside the domain.  A sum that underflows to 0
+ *      is inside it (s == 0: codes 0, decoded to 0).
  *
  * Build: gcc -O2 -std=c11 -fPIC -shared -ffp-contract=off -fno-fast-math kv3_oracle.c
  *        -o libokv3.so -lm      (oracle/build.py does this)

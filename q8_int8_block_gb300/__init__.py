@@ -13,6 +13,8 @@ this package fails.
     y = q8_linear_fused(x, Wq, Wd, epi="silu_mul", aux=gate, out_dtype=torch.bfloat16)
     y = q8_linear_fused(h, Wq, Wd, norm_weight=g, norm_eps=1e-6)   # RMSNorm(h) . W^T
     xq, xd, r = q8_quantize_act_rmsnorm(h, g, 1e-6)
+    codes, scales = q8_kv3_encode(kv)                  # kv [..., 128] -> 3-bit codes + scales
+    kv_hat = q8_kv3_decode(codes, scales, torch.bfloat16)
     isum = q8_block_sums(xq, Wq, path="decode")  # int32 [M,N,K/32]
 """
 import ctypes
@@ -21,7 +23,7 @@ import os
 import torch
 
 __all__ = ["Q8Error", "q8_quantize_weights", "q8_quantize_act", "q8_quantize_act_rmsnorm",
-           "q8_linear", "q8_linear_ex",
+           "q8_linear", "q8_linear_ex", "q8_kv3_encode", "q8_kv3_decode", "KV3_GROUP",
            "q8_linear_fused", "EPILOGUES",
            "q8_linear_workspace_size", "q8_block_sums", "q8_device_error", "q8_release",
            "q8_set_timing_events", "q8_linear_noalloc", "NOALLOC_SCRATCH_BYTES",
@@ -63,6 +65,8 @@ def _load():
         "q8_linear_noalloc": [p, i32, p, p, p, i64, i64, i64, p],
         "q8_linear_fused": [p, i32, p, f32, p, p, i32, p, p, i32, i64, i64, i64, i32, p, sz, p],
         "q8_quantize_act_rmsnorm": [p, i32, p, f32, p, p, p, i64, i64, p],
+        "q8_kv3_encode": [p, i32, p, p, i64, p],
+        "q8_kv3_decode": [p, p, p, i32, i64, p],
     }
     for name, args in sigs.items():
         f = getattr(L, name)
@@ -248,6 +252,45 @@ def q8_linear_fused(x, Wq, Wd, epi="none", aux=None, y=None, out_dtype=torch.flo
                               _ptr(aux), _ptr(y), DTYPES[out_dtype], M, N, K, PATHS[path],
                               _ptr(workspace), nbytes, _stream(stream)), "q8_linear_fused")
     return y
+
+
+KV3_GROUP = 128
+
+
+def q8_kv3_encode(x, codes=None, scales=None, stream=None):
+    """3-bit KV-cache codec, encoder: x bf16/float32 [..., 128*k] (contiguous) ->
+    (codes int32 [groups, 12] holding the uint32 code words, scales float32 [groups]), one
+    group per 128 consecutive elements.  Reinterpret codes with .view(torch.int32) as needed."""
+    if x.dtype not in DTYPES:
+        raise TypeError(f"x: expected bfloat16 or float32, got {x.dtype}")
+    if not x.is_cuda or not x.is_contiguous() or x.numel() % KV3_GROUP:
+        raise ValueError("x: a contiguous CUDA tensor of whole 128-element groups")
+    n = x.numel() // KV3_GROUP
+    if codes is None:
+        codes = torch.empty((n, 12), dtype=torch.int32, device=x.device)
+    if scales is None:
+        scales = torch.empty((n,), dtype=torch.float32, device=x.device)
+    _need(codes, torch.int32, (n, 12), "codes")
+    _need(scales, torch.float32, (n,), "scales")
+    _check(_L.q8_kv3_encode(_ptr(x), DTYPES[x.dtype], _ptr(codes), _ptr(scales), n, _stream(stream)),
+           "q8_kv3_encode")
+    return codes, scales
+
+
+def q8_kv3_decode(codes, scales, out_dtype=torch.bfloat16, out=None, stream=None):
+    """3-bit KV-cache codec, decoder: (codes int32 [groups, 12], scales float32 [groups]) ->
+    out [groups, 128] of out_dtype (bfloat16 or float32)."""
+    n = codes.shape[0]
+    _need(codes, torch.int32, (n, 12), "codes")
+    _need(scales, torch.float32, (n,), "scales")
+    if out_dtype not in DTYPES:
+        raise TypeError(f"out_dtype: expected bfloat16 or float32, got {out_dtype}")
+    if out is None:
+        out = torch.empty((n, KV3_GROUP), dtype=out_dtype, device=codes.device)
+    _need(out, out_dtype, (n, KV3_GROUP), "out")
+    _check(_L.q8_kv3_decode(_ptr(codes), _ptr(scales), _ptr(out), DTYPES[out_dtype], n,
+                            _stream(stream)), "q8_kv3_decode")
+    return out
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20

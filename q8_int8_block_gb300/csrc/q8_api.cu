@@ -373,6 +373,30 @@ q8_status q8_linear_fused(const void* x, q8_dtype xtype, const float* norm_weigh
                      workspace_bytes, library_ws, stream, e, pro);
 }
 
+q8_status q8_kv3_encode(const void* x, q8_dtype xtype, uint32_t* codes, float* scales,
+                        int64_t ngroups, cudaStream_t stream) {
+  if (xtype != Q8_F32 && xtype != Q8_BF16) return Q8_ERR_DTYPE;
+  if (ngroups < 0 || static_cast<double>(ngroups) * 512 > 281474976710656.0) return Q8_ERR_SHAPE;
+  if (ngroups > 0 && (x == nullptr || codes == nullptr || scales == nullptr)) return Q8_ERR_NULL;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return Q8_ERR_ALIGN;
+  DeviceInfo dev;
+  q8_status st = current_device(&dev);
+  if (st != Q8_OK) return st;
+  return launch_status(launch_kv3_encode(x, static_cast<int>(xtype), codes, scales, ngroups, dev, stream));
+}
+
+q8_status q8_kv3_decode(const uint32_t* codes, const float* scales, void* out, q8_dtype otype,
+                        int64_t ngroups, cudaStream_t stream) {
+  if (otype != Q8_F32 && otype != Q8_BF16) return Q8_ERR_DTYPE;
+  if (ngroups < 0 || static_cast<double>(ngroups) * 512 > 281474976710656.0) return Q8_ERR_SHAPE;
+  if (ngroups > 0 && (out == nullptr || codes == nullptr || scales == nullptr)) return Q8_ERR_NULL;
+  if (!aligned16(out) || !aligned16(codes) || !aligned16(scales)) return Q8_ERR_ALIGN;
+  DeviceInfo dev;
+  q8_status st = current_device(&dev);
+  if (st != Q8_OK) return st;
+  return launch_status(launch_kv3_decode(codes, scales, out, static_cast<int>(otype), ngroups, dev, stream));
+}
+
 size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path) {
   if (check_shape(M, N, K) != Q8_OK) return 0;
   DeviceInfo dev;

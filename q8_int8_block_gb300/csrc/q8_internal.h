@@ -98,6 +98,13 @@ cudaError_t launch_dp4a_gemm(const int8_t* xq, const float* xd, const int8_t* Wq
                              const uint16_t* Wd, float* y, int32_t* isum, int64_t M, int64_t N,
                              int64_t K, cudaStream_t stream, const Epilogue& epi = Epilogue());
 
+// ---- q8_kv3.cu -------------------------------------------------------------------
+// 3-bit KV-cache codec (Walsh-Hadamard rotation + Lloyd-Max), 128-element groups.
+cudaError_t launch_kv3_encode(const void* x, int xtype, uint32_t* codes, float* scales, int64_t n,
+                              const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_kv3_decode(const uint32_t* codes, const float* scales, void* out, int otype,
+                              int64_t n, const DeviceInfo& dev, cudaStream_t stream);
+
 // ---- q8_gemm.cu -------------------------------------------------------------------
 // Tensor-core GEMM on binary16 codes: A16 [M,K] activation codes, B16 [N,K] weight codes,
 // xd [M,K/32] f32, Wd [N,K/32] binary16 bits.  Writes y [M,N] (rescaled sum) or, when

@@ -119,3 +119,17 @@ def test_rmsnorm_quantizer_rejects_bad_arguments(L):
         a = list(ok)
         a[i] = v
         assert Q(*a) == want, (i, v)
+
+
+def test_kv3_codec_rejects_bad_arguments(L):
+    E, D = L.q8_kv3_encode, L.q8_kv3_decode
+    E.argtypes = [P, ctypes.c_int, P, P, ctypes.c_int64, P]
+    D.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int64, P]
+    assert E(P(FAKE), 2, P(FAKE), P(FAKE), 4, None) == 4
+    assert E(P(FAKE), 1, P(FAKE), P(FAKE), -1, None) == 2
+    assert E(None, 1, P(FAKE), P(FAKE), 4, None) == 1
+    assert E(P(FAKE), 1, P(FAKE), P(FAKE + 4), 4, None) == 3
+    assert D(P(FAKE), P(FAKE), P(FAKE), 3, 4, None) == 4
+    assert D(P(FAKE), None, P(FAKE), 1, 4, None) == 1
+    assert D(P(FAKE + 8), P(FAKE), P(FAKE), 1, 4, None) == 3
+    assert D(P(FAKE), P(FAKE), P(FAKE), 1, 1 << 50, None) == 2

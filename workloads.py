@@ -12,6 +12,11 @@ Recipe (numpy PCG64 via default_rng):
     float32.
   * one generator per (workload, projection) for weights, and one per (workload,
     projection, M) for activations, seeded as listed in SEEDS below.
+  * KV-cache groups (the 3-bit codec): keys or values of `tokens` tokens x `heads` heads
+    x `head_dim` channels, standard_normal float32 times a per-channel gain that is 1
+    except on round(outlier_frac * head_dim) channels (the same for every token and head)
+    where it is `gain`; rounded to bfloat16; cut into 128-element groups (a 256-wide head
+    is two groups).
 """
 from dataclasses import dataclass, field
 from typing import List, Tuple
@@ -123,3 +128,24 @@ def algorithmic_bytes(M: int, N: int, K: int, x_bytes: int = 2) -> int:
 def algorithmic_ops(M: int, N: int, K: int) -> int:
     """int8-equivalent multiply-add operations (2 per MAC); block rescales excluded."""
     return 2 * M * N * K
+
+
+KV3_GROUP = 128
+
+
+def kv_groups(rng: np.random.Generator, tokens: int, heads: int, head_dim: int = 256,
+              outlier_frac: float = 0.02, gain: float = 10.0, bf16: bool = True) -> np.ndarray:
+    """Synthetic keys or values as [tokens * heads * head_dim / 128, 128] groups
+    (bfloat16 bits as uint16, or float32)."""
+    x = rng.standard_normal((tokens, heads, head_dim), dtype=np.float32)
+    cnt = int(round(outlier_frac * head_dim))
+    if cnt:
+        idx = rng.choice(head_dim, size=cnt, replace=False)
+        x[:, :, idx] *= np.float32(gain)
+    x = x.reshape(-1, KV3_GROUP)
+    return bf16_bits_from_f32(x) if bf16 else x
+
+
+# 256K-token context of the post's 3-bit KV cache: one attention layer's keys (or values),
+# 4 KV heads of 256 channels
+KV3_LAYER_256K = dict(tokens=262144, heads=4, head_dim=256)
