@@ -649,6 +649,9 @@ def parse_args(argv=None):
                     help="force a kernel family for --workload (default: the library's choice)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every point of the dense-layer sweep workload (one GPU) and exit")
+    ap.add_argument("--kv3", action="store_true",
+                    help="time only the 3-bit KV-cache codec (one layer's keys at a 256K-token "
+                         "context: encode and decode) and exit")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     a = ap.parse_args(argv)
@@ -702,6 +705,16 @@ def main(argv=None):
     args = parse_args(argv)
     if args.sweep:
         print(json.dumps(sweep_arm(args)), flush=True)
+        return
+    if args.kv3:
+        import torch
+        import __graft_entry__ as g
+        g.build()
+        import q8_int8_block_gb300 as q8
+        torch.cuda.set_device(0)
+        pk, pk_src = peaks()
+        r = run_kv3(torch, q8, torch.device("cuda", 0), args.steps, args.warmup, pk, pk_src)
+        print(json.dumps({"kv3": r, "device_error_word": q8.q8_device_error()}), flush=True)
         return
     if args.impl == "reference":
         rank, line = reference_arm(args)
