@@ -207,6 +207,8 @@ TRAFFIC_PROFILES = {  # committed ncu summaries that record DRAM bytes per launc
     "prefill9b_up": ("gemm_tc_kernel_m2048_k4096_n12288.md", ["q8_gemm.cu", "q8_ptx.cuh", "q8_epi.cuh"]),
     "decode_m16": ("batch_kernel_m16_k4096_n12288.md",
                    ["q8_batch.cu", "q8_ptx.cuh", "q8_quant_dev.cuh", "q8_epi.cuh"]),
+    "kv3_encode_256k": ("kv3_encode_kernel_256k_layer.md", ["q8_kv3.cu"]),
+    "kv3_decode_256k": ("kv3_decode_kernel_256k_layer.md", ["q8_kv3.cu"]),
 }
 
 
@@ -414,7 +416,9 @@ def run_kv3(torch, q8, dev, steps, warmup, pk, pk_src):
                      "groups": n, "algorithmic_bytes_per_launch": bytes_step,
                      "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": pk["hbm_gbs"],
                                   "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
-                                  "peak_source": f"hbm_gbs of the {pk_src} peaks"},
+                                  "peak_source": f"hbm_gbs of the {pk_src} peaks",
+                                  "kernel": "q8::kv3_" + name.split("_")[1] + "_kernel",
+                                  "traffic": profiled_traffic(*TRAFFIC_PROFILES[name])},
                      "steps": steps}
     return res
 
