@@ -381,7 +381,8 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
                            "time per step of the timed region (activation quantizer + batched "
                            "kernel, chained by programmatic dependent launch)"
                            if path == "batch" else "mean of event-node pairs around the GEMM launches")
-    prof = TRAFFIC_PROFILES.get(name)
+    # the committed captures are of the library's own choice of kernel on the plain layer
+    prof = TRAFFIC_PROFILES.get(name) if force_path is None and gated is None else None
     roof["traffic"] = profiled_traffic(*prof) if prof else None
     out = {"name": name, "M": M, "K": K, "N": N, "path": path, "unit": unit, "value": value,
            "t_max": t_max, "roofline": roof, "copies": copies, "wbytes": wbytes,

@@ -172,31 +172,47 @@ __global__ void __launch_bounds__(256) kv3_encode_kernel(const Kv3Params p) {
   }
 }
 
+// the lane's four 24-bit code chunks of group g: bits [96 c + 24 t, + 24) of its stream,
+// i.e. word 3 c + (3 t) / 4 from bit (24 t) % 32, and the next word when they cross
+__device__ __forceinline__ void load_chunks(const uint32_t* codes, int64_t g, int64_t n, int t,
+                                            uint32_t (&lo)[4], uint32_t (&hi)[4]) {
+  const int bit = 24 * t, w0 = bit >> 5, off = bit & 31;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    lo[c] = 0u;
+    hi[c] = 0u;
+    if (g < n) {
+      const uint32_t* w = codes + g * kWords + 3 * c;
+      lo[c] = __ldg(w + w0);
+      if (off > 8) hi[c] = __ldg(w + w0 + 1);
+    }
+  }
+}
+
 template <int kOType>
 __global__ void __launch_bounds__(256) kv3_decode_kernel(const Kv3Params p) {
   const int lane = threadIdx.x & 31, t = lane & 3;
   const int64_t team = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 2;
   const int64_t nteams = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 2;
   const int64_t rounds = (p.n + nteams - 1) / nteams;
+  const int off = (24 * t) & 31;
+  // software pipeline: the next group's code words and scale are in flight while this
+  // group is transformed
+  uint32_t lo[4], hi[4];
+  load_chunks(p.codes_in, team, p.n, t, lo, hi);
+  float s = team < p.n ? __ldg(p.scales_in + team) : 0.0f;
   for (int64_t it = 0; it < rounds; ++it) {
     const int64_t g = it * nteams + team;
+    const int64_t gn = g + nteams;
+    uint32_t nlo[4], nhi[4];
+    load_chunks(p.codes_in, gn, p.n, t, nlo, nhi);
+    const float ns = gn < p.n ? __ldg(p.scales_in + gn) : 0.0f;
     float v[4][kE];
-    const float s = g < p.n ? __ldg(p.scales_in + g) : 0.0f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      // bits [96 c + 24 t, + 24): word 3 c + (3 t) / 4 at offset (24 t) % 32, maybe the next
-      uint32_t chunk = 0;
-      if (g < p.n) {
-        const uint32_t* w = p.codes_in + g * kWords + 3 * c;
-        const int bit = 24 * t, w0 = bit >> 5, off = bit & 31;
-        const uint32_t lo = __ldg(w + w0);
-        const uint32_t hi = off > 8 ? __ldg(w + w0 + 1) : 0u;
-        chunk = ((lo >> off) | (off > 8 ? hi << (32 - off) : 0u)) & 0xFFFFFFu;
-      }
+      const uint32_t chunk = ((lo[c] >> off) | (off > 8 ? hi[c] << (32 - off) : 0u)) & 0xFFFFFFu;
 #pragma unroll
-      for (int e = 0; e < kE; ++e) {
-        v[c][e] = __fmul_rn(s, kv3_value(chunk >> (3 * e)));
-      }
+      for (int e = 0; e < kE; ++e) v[c][e] = __fmul_rn(s, kv3_value(chunk >> (3 * e)));
     }
     fwht_group(v, t);
     if (g < p.n) {
@@ -205,22 +221,28 @@ __global__ void __launch_bounds__(256) kv3_decode_kernel(const Kv3Params p) {
         float o[kE];
 #pragma unroll
         for (int e = 0; e < kE; ++e) o[e] = __fmul_rn(v[c][e], 0.0078125f);  // / 128, exact
-        const int64_t off = g * kD + 32 * c + 8 * t;
+        const int64_t eo = g * kD + 32 * c + 8 * t;
         if constexpr (kOType == 1) {
           uint32_t u[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 b = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
-            u[i] = *reinterpret_cast<const uint32_t*>(&b);
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+            u[i] = *reinterpret_cast<const uint32_t*>(&b2);
           }
-          __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + off), make_uint4(u[0], u[1], u[2], u[3]));
+          __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + eo), make_uint4(u[0], u[1], u[2], u[3]));
         } else {
-          float4* f = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off);
+          float4* f = reinterpret_cast<float4*>(static_cast<float*>(p.out) + eo);
           __stcs(f, make_float4(o[0], o[1], o[2], o[3]));
           __stcs(f + 1, make_float4(o[4], o[5], o[6], o[7]));
         }
       }
     }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      lo[c] = nlo[c];
+      hi[c] = nhi[c];
+    }
+    s = ns;
   }
 }
 
