@@ -191,7 +191,9 @@ q8_status q8_kv3_encode(const void* x, q8_dtype xtype, uint32_t* codes, float* s
 q8_status q8_kv3_decode(const uint32_t* codes, const float* scales, void* out, q8_dtype otype,
                         int64_t ngroups, cudaStream_t stream);
 
-/* Bytes of scratch q8_linear_ex needs for this shape and path (0 if none). */
+/* Bytes of scratch q8_linear_ex and q8_linear_fused need for this shape and path (0 if
+ * none): the path's own arrays, the GEMM's partial outputs when it splits K, and a slot
+ * for the rows' RMSNorm factors. */
 size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path);
 
 /*
