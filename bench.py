@@ -520,18 +520,14 @@ def gpu_arm(args):
             extra[k]["note"] = ("3-bit KV-cache codec (Walsh-Hadamard rotation + Lloyd-Max), "
                                 "one attention layer's keys at a 256K-token context")
     err = q8.q8_device_error()
-    wname = CASES[args.workload][0]
-    desc = {"decode": "decode GEMV, FFN up-projection of a dense ~9B-class layer",
-            "tiny": "tiny Q8_0 linear (float32 activations)",
-            "prefill9b": "prefill GEMM, 9B-class projection",
-            "prefill27b": "prefill GEMM, 27B-class projection, 1% activation channels x20"}[wname]
+    desc = workload_desc(args.workload)
     line = {
         "metric": METRIC, "value": round(r["value"], 3), "unit": r["unit"], "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(r["t_max"] / args.steps * 1e3, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
         "data": "synthetic (seeded N(0,0.02) weights quantized to Q8_0, N(0,1) activations)",
-        "config": {"workload": f"{desc}: {args.workload}", "M": r["M"], "K": r["K"], "N": r["N"],
+        "config": {"workload": desc, "M": r["M"], "K": r["K"], "N": r["N"],
                    "weights": "Q8_0 (int8 codes + binary16 scale per 32 along K)",
                    "activations": ("bf16" if r["bf16"] else "float32") +
                                   ", quantized per call inside the library",
@@ -589,6 +585,16 @@ def cpu_baseline(Wq_t, Wd_t, x_np, bf16, M, N, K, xsize, seconds):
                       f"(activation quantization + those outputs) in {dt:.1f} s"}
 
 
+def workload_desc(name):
+    """The config's workload string, the same on both arms."""
+    wname = CASES[name][0]
+    desc = {"decode": "decode GEMV, FFN up-projection of a dense ~9B-class layer",
+            "tiny": "tiny Q8_0 linear (float32 activations)",
+            "prefill9b": "prefill GEMM, 9B-class projection",
+            "prefill27b": "prefill GEMM, 27B-class projection, 1% activation channels x20"}[wname]
+    return f"{desc}: {name}"
+
+
 def reference_arm(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -630,7 +636,7 @@ def reference_arm(args):
         "ms_per_step": round(dt / args.steps * 1e3, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8",
         "data": "synthetic (seeded N(0,0.02) weights quantized to Q8_0, N(0,1) activations)",
-        "config": {"workload": f"{args.workload}", "M": M, "K": K, "N": N,
+        "config": {"workload": workload_desc(args.workload), "M": M, "K": K, "N": N,
                    "parallelism": "CPU oracle, rank 0 only"},
         "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": f"each step: the layer over {rows} of {N} output rows "
