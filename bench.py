@@ -200,6 +200,7 @@ CASES = {
     "decode_m64": ("decode", 0, 3), "tiny": ("tiny", 0, 0),
     "prefill9b_up": ("prefill9b", 0, 0), "prefill9b_down": ("prefill9b", 1, 0),
     "prefill27b_up": ("prefill27b", 0, 0), "prefill27b_down": ("prefill27b", 1, 0),
+    "gate_m128": ("sweep", 4, 3), "gate_m512": ("sweep", 4, 4),
 }
 TRAFFIC_PROFILES = {  # committed ncu summaries that record DRAM bytes per launch
     "decode_m1": ("decode_kernel_m1_k4096_n12288.md",
@@ -277,11 +278,12 @@ def time_graph_steps(torch, q8, step_fns, steps, warmup, instrument=True):
 
 
 def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=False, spec=None,
-             force_path=None, gated=None, norm=False):
+             force_path=None, gated=None, norm=False, prepared=False):
     """gated: None (the plain layer, float32 y), "fused" (q8_linear_fused: y = silu(gate) *
     x.W^T stored as bfloat16 by the GEMM's own epilogue) or "unfused" (the plain layer, then
     torch's silu, multiply and bfloat16 cast as separate kernels).  norm (with "fused"): x is
-    the un-normalised hidden state and its RMSNorm runs inside the layer's quantizer."""
+    the un-normalised hidden state and its RMSNorm runs inside the layer's quantizer.
+    prepared: the tensor-core path on weights widened once (q8_linear_prepared)."""
     wname, p, mi = spec if spec is not None else CASES[name]
     wl = workloads.WORKLOADS[wname]
     W = wl.make_weights(p)
@@ -301,14 +303,21 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
     else:
         x = torch.from_numpy(x_np).to(dev)
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
-    wsz = q8.q8_linear_workspace_size(M, N, K, force_path or "auto")
+    wsz = (q8.q8_linear_prepared_workspace_size(M, N, K) if prepared
+           else q8.q8_linear_workspace_size(M, N, K, force_path or "auto"))
     ws = torch.empty(max(wsz, 1), dtype=torch.uint8, device=dev) if wsz else None
-    if force_path:
+    if prepared:
+        path = "tensor"
+    elif force_path:
         path = force_path
     else:
         wsz_batch = q8.q8_linear_workspace_size(M, N, K, "batch") if M <= 64 else 0
         path = "decode" if wsz == 0 else ("batch" if wsz == wsz_batch else "tensor")
-    if gated is None:
+    if prepared:
+        B16s = [q8.q8_weights_to_f16(w) for w in Wqs]
+        fns = [lambda i=i: q8.q8_linear_prepared(x, B16s[i], Wds[i], y=y, workspace=ws)
+               for i in range(copies)]
+    elif gated is None:
         fns = [lambda i=i: q8.q8_linear_ex(x, Wqs[i], Wds[i], y=y, path=path, workspace=ws)
                for i in range(copies)]
     else:
@@ -382,7 +391,7 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
                            "kernel, chained by programmatic dependent launch)"
                            if path == "batch" else "mean of event-node pairs around the GEMM launches")
     # the committed captures are of the library's own choice of kernel on the plain layer
-    prof = TRAFFIC_PROFILES.get(name) if force_path is None and gated is None else None
+    prof = TRAFFIC_PROFILES.get(name) if force_path is None and gated is None and not prepared else None
     roof["traffic"] = profiled_traffic(*prof) if prof else None
     out = {"name": name, "M": M, "K": K, "N": N, "path": path, "unit": unit, "value": value,
            "t_max": t_max, "roofline": roof, "copies": copies, "wbytes": wbytes,
@@ -492,12 +501,17 @@ def gpu_arm(args):
                              ("decode_m1", 20000, "gated_fused"), ("decode_m1", 20000, "gated_unfused"),
                              ("prefill9b_up", 200, "gated_fused"), ("prefill9b_up", 200, "gated_unfused"),
                              ("decode_m1", 20000, "norm_gated_fused"),
-                             ("prefill9b_up", 200, "norm_gated_fused")):
+                             ("prefill9b_up", 200, "norm_gated_fused"),
+                             ("prefill9b_up", 200, "prepared"), ("gate_m128", 2000, None),
+                             ("gate_m128", 2000, "prepared"), ("gate_m512", 500, None),
+                             ("gate_m512", 500, "prepared")):
             norm = bool(fp) and fp.startswith("norm_")
             tag = fp[5:] if norm else fp
             gated = tag[6:] if tag and tag.startswith("gated_") else None
+            prep = fp == "prepared"
             e = run_case(torch, q8, dev, name, st, max(3, st // 50), pk, pk_src,
-                         force_path=None if gated else fp, gated=gated, norm=norm)
+                         force_path=None if (gated or prep) else fp, gated=gated, norm=norm,
+                         prepared=prep)
             key = name if fp is None else f"{name}_{fp}"
             extra[key] = {"value": round(e["value"], 3), "unit": e["unit"], "path": e["path"],
                           "us_per_step": round(e["t_max"] / st * 1e6, 3),
@@ -511,6 +525,10 @@ def gpu_arm(args):
                 if norm:
                     extra[key]["note"] = ("RMSNorm + linear + SiLU gate + bfloat16 y in one call "
                                           "(q8_linear_fused with norm_weight)")
+            if prep:
+                extra[key]["note"] = ("tensor-core path on weights widened to binary16 once "
+                                      "(q8_weights_to_f16 + q8_linear_prepared): no per-call "
+                                      "widening pass")
             if gated == "unfused":
                 extra[key]["note"] = ("the same unit as the plain layer (float32 y) followed by "
                                       "torch silu, multiply and bfloat16 cast; us_per_step is "

@@ -191,6 +191,27 @@ q8_status q8_kv3_encode(const void* x, q8_dtype xtype, uint32_t* codes, float* s
 q8_status q8_kv3_decode(const uint32_t* codes, const float* scales, void* out, q8_dtype otype,
                         int64_t ngroups, cudaStream_t stream);
 
+/*
+ * Prepared weights for the tensor-core path.  The tensor path feeds the MMA binary16
+ * copies of the int8 codes (exact: |q| <= 127); q8_linear / q8_linear_ex / q8_linear_fused
+ * widen the codes on every call (read N*K bytes, write and re-read 2*N*K).  For weights
+ * used by many prefill or medium-batch calls, widen them once and keep the copy:
+ *   q8_weights_to_f16: Wq [N,K] int8 -> B16 [N,K] binary16 bits (2 bytes per weight).
+ *   q8_linear_prepared: q8_linear_fused on the tensor-core path (any M; the batched and
+ *     decode kernels, which read the int8 codes, are faster for M <= 64) with B16 in place
+ *     of Wq; the same kernels and the same results as q8_linear_fused with
+ *     Q8_PATH_TENSOR.  workspace: NULL with workspace_bytes 0 for the library-owned
+ *     scratch, else at least q8_linear_prepared_workspace_size() bytes.
+ */
+q8_status q8_weights_to_f16(const int8_t* Wq, uint16_t* B16, int64_t N, int64_t K,
+                            cudaStream_t stream);
+q8_status q8_linear_prepared(const void* x, q8_dtype xtype, const float* norm_weight,
+                             float norm_eps, const uint16_t* B16, const uint16_t* Wd,
+                             q8_epilogue epi, const float* aux, void* y, q8_dtype ytype,
+                             int64_t M, int64_t N, int64_t K, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+size_t q8_linear_prepared_workspace_size(int64_t M, int64_t N, int64_t K);
+
 /* Bytes of scratch q8_linear_ex and q8_linear_fused need for this shape and path (0 if
  * none): the path's own arrays, the GEMM's partial outputs when it splits K, and a slot
  * for the rows' RMSNorm factors. */

@@ -13,6 +13,8 @@ this package fails.
     y = q8_linear_fused(x, Wq, Wd, epi="silu_mul", aux=gate, out_dtype=torch.bfloat16)
     y = q8_linear_fused(h, Wq, Wd, norm_weight=g, norm_eps=1e-6)   # RMSNorm(h) . W^T
     xq, xd, r = q8_quantize_act_rmsnorm(h, g, 1e-6)
+    B16 = q8_weights_to_f16(Wq)                        # once per weight matrix
+    y = q8_linear_prepared(x, B16, Wd)                 # tensor-core path, no per-call widening
     codes, scales = q8_kv3_encode(kv)                  # kv [..., 128] -> 3-bit codes + scales
     kv_hat = q8_kv3_decode(codes, scales, torch.bfloat16)
     isum = q8_block_sums(xq, Wq, path="decode")  # int32 [M,N,K/32]
@@ -24,6 +26,7 @@ import torch
 
 __all__ = ["Q8Error", "q8_quantize_weights", "q8_quantize_act", "q8_quantize_act_rmsnorm",
            "q8_linear", "q8_linear_ex", "q8_kv3_encode", "q8_kv3_decode", "KV3_GROUP",
+           "q8_weights_to_f16", "q8_linear_prepared", "q8_linear_prepared_workspace_size",
            "q8_linear_fused", "EPILOGUES",
            "q8_linear_workspace_size", "q8_block_sums", "q8_device_error", "q8_release",
            "q8_set_timing_events", "q8_linear_noalloc", "NOALLOC_SCRATCH_BYTES",
@@ -67,6 +70,8 @@ def _load():
         "q8_quantize_act_rmsnorm": [p, i32, p, f32, p, p, p, i64, i64, p],
         "q8_kv3_encode": [p, i32, p, p, i64, p],
         "q8_kv3_decode": [p, p, p, i32, i64, p],
+        "q8_weights_to_f16": [p, p, i64, i64, p],
+        "q8_linear_prepared": [p, i32, p, f32, p, p, i32, p, p, i32, i64, i64, i64, p, sz, p],
     }
     for name, args in sigs.items():
         f = getattr(L, name)
@@ -76,6 +81,8 @@ def _load():
     L.q8_set_timing_events.restype = i32
     L.q8_linear_workspace_size.argtypes = [i64, i64, i64, i32]
     L.q8_linear_workspace_size.restype = sz
+    L.q8_linear_prepared_workspace_size.argtypes = [i64, i64, i64]
+    L.q8_linear_prepared_workspace_size.restype = sz
     L.q8_device_error.argtypes = [ctypes.POINTER(i32)]
     L.q8_device_error.restype = ctypes.c_uint32
     L.q8_status_string.argtypes = [i32]
@@ -251,6 +258,51 @@ def q8_linear_fused(x, Wq, Wd, epi="none", aux=None, y=None, out_dtype=torch.flo
                               _ptr(Wq), _ptr(Wd), EPILOGUES[epi],
                               _ptr(aux), _ptr(y), DTYPES[out_dtype], M, N, K, PATHS[path],
                               _ptr(workspace), nbytes, _stream(stream)), "q8_linear_fused")
+    return y
+
+
+def q8_weights_to_f16(Wq, B16=None, stream=None):
+    """Wq int8 [N,K] -> B16 int16-stored binary16 codes [N,K], for q8_linear_prepared."""
+    N, K = Wq.shape
+    _need(Wq, torch.int8, (N, K), "Wq")
+    if B16 is None:
+        B16 = torch.empty((N, K), dtype=torch.int16, device=Wq.device)
+    _need(B16, torch.int16, (N, K), "B16")
+    _check(_L.q8_weights_to_f16(_ptr(Wq), _ptr(B16), N, K, _stream(stream)), "q8_weights_to_f16")
+    return B16
+
+
+def q8_linear_prepared_workspace_size(M, N, K) -> int:
+    return int(_L.q8_linear_prepared_workspace_size(M, N, K))
+
+
+def q8_linear_prepared(x, B16, Wd, epi="none", aux=None, y=None, out_dtype=torch.float32,
+                       workspace=None, stream=None, norm_weight=None, norm_eps=1e-6):
+    """q8_linear_fused on the tensor-core path with weights widened once by
+    q8_weights_to_f16 (no per-call widening)."""
+    if x.dtype not in DTYPES:
+        raise TypeError(f"x: expected bfloat16 or float32, got {x.dtype}")
+    if out_dtype not in DTYPES:
+        raise TypeError(f"out_dtype: expected bfloat16 or float32, got {out_dtype}")
+    _need(x, x.dtype, tuple(x.shape), "x")
+    M, K = x.shape
+    N = B16.shape[0]
+    _need(B16, torch.int16, (N, K), "B16")
+    _need(Wd, torch.int16, (N, K // QK), "Wd")
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    _need(y, out_dtype, (M, N), "y")
+    if EPILOGUES[epi] != 0:
+        if aux is None:
+            raise ValueError(f"epi {epi!r} needs aux")
+        _need(aux, torch.float32, (M, N), "aux")
+    if norm_weight is not None:
+        _need(norm_weight, torch.float32, (K,), "norm_weight")
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_L.q8_linear_prepared(_ptr(x), DTYPES[x.dtype], _ptr(norm_weight), float(norm_eps),
+                                 _ptr(B16), _ptr(Wd), EPILOGUES[epi], _ptr(aux), _ptr(y),
+                                 DTYPES[out_dtype], M, N, K, _ptr(workspace), nbytes,
+                                 _stream(stream)), "q8_linear_prepared")
     return y
 
 

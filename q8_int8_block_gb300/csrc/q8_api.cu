@@ -118,9 +118,10 @@ q8_status resolve_path(int64_t M, int64_t N, int64_t K, q8_path req, const Devic
 
 // Scratch of the tensor path: A16 [M,K] f16 codes, xd [M,K/32] f32, B16 [N,K] f16 codes, and
 // the GEMM's partial outputs (split-K, or its split tail wave: gemm_part_bytes).
-size_t tensor_ws_bytes(int64_t M, int64_t N, int64_t K, size_t part_bytes) {
+// With prepared weights (q8_linear_prepared) the B16 region is not needed.
+size_t tensor_ws_bytes(int64_t M, int64_t N, int64_t K, size_t part_bytes, bool with_b16 = true) {
   return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(M) * (K / kQK) * 4) +
-         align256(static_cast<size_t>(N) * K * 2) + align256(part_bytes);
+         (with_b16 ? align256(static_cast<size_t>(N) * K * 2) : 0) + align256(part_bytes);
 }
 
 // Scratch of the dp4a path: int8 activation codes [M,K] and their scales [M,K/32].
@@ -130,14 +131,16 @@ size_t dp4a_ws_bytes(int64_t M, int64_t K) {
 
 // Scratch of a path: its own arrays, then a slot of M binary32 RMSNorm factors (used only
 // when the call normalises its input).
-size_t norm_slot_offset(q8_path p, int64_t M, int64_t N, int64_t K, size_t part_bytes) {
+size_t norm_slot_offset(q8_path p, int64_t M, int64_t N, int64_t K, size_t part_bytes,
+                        bool with_b16 = true) {
   return p == Q8_PATH_BATCH  ? batch_ws_bytes(M, K)
          : p == Q8_PATH_DP4A ? dp4a_ws_bytes(M, K)
-                             : tensor_ws_bytes(M, N, K, part_bytes);
+                             : tensor_ws_bytes(M, N, K, part_bytes, with_b16);
 }
-size_t path_ws_bytes(q8_path p, int64_t M, int64_t N, int64_t K, size_t part_bytes) {
+size_t path_ws_bytes(q8_path p, int64_t M, int64_t N, int64_t K, size_t part_bytes,
+                     bool with_b16 = true) {
   if (p == Q8_PATH_DECODE || M == 0 || N == 0 || K == 0) return 0;
-  return norm_slot_offset(p, M, N, K, part_bytes) + align256(static_cast<size_t>(M) * 4);
+  return norm_slot_offset(p, M, N, K, part_bytes, with_b16) + align256(static_cast<size_t>(M) * 4);
 }
 
 // Library-owned scratch for (current device, stream), grown on demand.
@@ -207,7 +210,8 @@ cudaError_t timed_launch(cudaStream_t stream, F&& launch) {
 q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uint16_t* Wd,
                       float* y, int64_t M, int64_t N, int64_t K, q8_path path, void* ws,
                       size_t ws_bytes, bool library_ws, cudaStream_t stream,
-                      const Epilogue& epi = Epilogue(), Prologue pro = Prologue()) {
+                      const Epilogue& epi = Epilogue(), Prologue pro = Prologue(),
+                      const uint16_t* B16_pre = nullptr) {
   if (xtype != Q8_F32 && xtype != Q8_BF16) return Q8_ERR_DTYPE;
   if (path != Q8_PATH_AUTO && path != Q8_PATH_DECODE && path != Q8_PATH_TENSOR &&
       path != Q8_PATH_BATCH && path != Q8_PATH_DP4A)
@@ -235,7 +239,8 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
     }));
   const int splits = gemm_splits(M, N, K, dev);
   const size_t part_bytes = gemm_part_bytes(M, N, K, dev);
-  const size_t need = path_ws_bytes(p, M, N, K, part_bytes);
+  const bool with_b16 = B16_pre == nullptr;  // prepared weights need no widening scratch
+  const size_t need = path_ws_bytes(p, M, N, K, part_bytes, with_b16);
   if (library_ws) {
     if ((st = library_workspace(dev, stream, need, &ws)) != Q8_OK) return st;
   } else {
@@ -244,7 +249,8 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
     if (ws_bytes < need) return Q8_ERR_NOMEM;
   }
   if (pro.on()) {  // the rows' RMSNorm factors, read by the activation quantizer
-    float* r = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + norm_slot_offset(p, M, N, K, part_bytes));
+    float* r = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                        norm_slot_offset(p, M, N, K, part_bytes, with_b16));
     cudaError_t e = launch_row_rms(x, static_cast<int>(xtype), M, K, pro.eps, r, dev, stream);
     if (e != cudaSuccess) return launch_status(e);
     pro.r = r;
@@ -269,13 +275,13 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   uint16_t* A16 = reinterpret_cast<uint16_t*>(w8);
   float* xd = reinterpret_cast<float*>(w8 + align256(static_cast<size_t>(M) * K * 2));
-  uint16_t* B16 = reinterpret_cast<uint16_t*>(w8 + align256(static_cast<size_t>(M) * K * 2) +
-                                              align256(static_cast<size_t>(M) * (K / kQK) * 4));
-  float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(B16) +
-                                         align256(static_cast<size_t>(N) * K * 2));
+  uint8_t* after_xd = w8 + align256(static_cast<size_t>(M) * K * 2) +
+                      align256(static_cast<size_t>(M) * (K / kQK) * 4);
+  uint16_t* B16 = with_b16 ? reinterpret_cast<uint16_t*>(after_xd) : const_cast<uint16_t*>(B16_pre);
+  float* part = reinterpret_cast<float*>(after_xd + (with_b16 ? align256(static_cast<size_t>(N) * K * 2) : 0));
   cudaError_t e =
       launch_quantize(x, static_cast<int>(xtype), A16, true, xd, false, M, K, dev, stream, pro);
-  if (e == cudaSuccess) e = launch_codes_to_f16(Wq, B16, N * K, dev, stream);
+  if (e == cudaSuccess && with_b16) e = launch_codes_to_f16(Wq, B16, N * K, dev, stream);
   if (e == cudaSuccess)
     e = timed_launch(stream, [&] {
       return launch_gemm_tc(A16, B16, xd, Wd, y, nullptr, part, splits, M, N, K, dev, stream, epi);
@@ -349,28 +355,81 @@ q8_status q8_linear_ex(const void* x, q8_dtype xtype, const int8_t* Wq, const ui
   return linear_impl(x, xtype, Wq, Wd, y, M, N, K, path, workspace, workspace_bytes, false, stream);
 }
 
+}  // extern "C"
+
+namespace q8 {
+namespace {
+// The neighbours of q8_linear_fused / q8_linear_prepared, checked.
+q8_status fused_neighbours(const float* norm_weight, float norm_eps, q8_epilogue epi,
+                           const float* aux, q8_dtype ytype, int64_t M, int64_t N, Prologue* pro,
+                           Epilogue* e) {
+  if (epi != Q8_EPI_NONE && epi != Q8_EPI_ADD && epi != Q8_EPI_SILU_MUL) return Q8_ERR_DTYPE;
+  if (ytype != Q8_F32 && ytype != Q8_BF16) return Q8_ERR_DTYPE;
+  if (epi != Q8_EPI_NONE && M > 0 && N > 0 && aux == nullptr) return Q8_ERR_NULL;
+  if (!aligned16(aux) || !aligned16(norm_weight)) return Q8_ERR_ALIGN;
+  if (norm_weight != nullptr) {
+    if (!(norm_eps > 0.0f) || !std::isfinite(norm_eps)) return Q8_ERR_VALUE;
+    pro->gamma = norm_weight;
+    pro->eps = norm_eps;
+  }
+  e->aux = aux;
+  e->op = static_cast<int>(epi);
+  e->bf16 = ytype == Q8_BF16 ? 1 : 0;
+  return Q8_OK;
+}
+}  // namespace
+}  // namespace q8
+
+extern "C" {
+
 q8_status q8_linear_fused(const void* x, q8_dtype xtype, const float* norm_weight,
                           float norm_eps, const int8_t* Wq, const uint16_t* Wd, q8_epilogue epi,
                           const float* aux, void* y, q8_dtype ytype, int64_t M, int64_t N,
                           int64_t K, q8_path path, void* workspace, size_t workspace_bytes,
                           cudaStream_t stream) {
-  if (epi != Q8_EPI_NONE && epi != Q8_EPI_ADD && epi != Q8_EPI_SILU_MUL) return Q8_ERR_DTYPE;
-  if (ytype != Q8_F32 && ytype != Q8_BF16) return Q8_ERR_DTYPE;
-  if (epi != Q8_EPI_NONE && M > 0 && N > 0 && aux == nullptr) return Q8_ERR_NULL;
-  if (!aligned16(aux) || !aligned16(norm_weight)) return Q8_ERR_ALIGN;
   Prologue pro;
-  if (norm_weight != nullptr) {
-    if (!(norm_eps > 0.0f) || !std::isfinite(norm_eps)) return Q8_ERR_VALUE;
-    pro.gamma = norm_weight;
-    pro.eps = norm_eps;
-  }
   Epilogue e;
-  e.aux = aux;
-  e.op = static_cast<int>(epi);
-  e.bf16 = ytype == Q8_BF16 ? 1 : 0;
+  q8_status st = fused_neighbours(norm_weight, norm_eps, epi, aux, ytype, M, N, &pro, &e);
+  if (st != Q8_OK) return st;
   const bool library_ws = workspace == nullptr && workspace_bytes == 0;
   return linear_impl(x, xtype, Wq, Wd, static_cast<float*>(y), M, N, K, path, workspace,
                      workspace_bytes, library_ws, stream, e, pro);
+}
+
+q8_status q8_weights_to_f16(const int8_t* Wq, uint16_t* B16, int64_t N, int64_t K,
+                            cudaStream_t stream) {
+  q8_status st = check_shape(0, N, K);
+  if (st != Q8_OK) return st;
+  if (N * K > 0 && (Wq == nullptr || B16 == nullptr)) return Q8_ERR_NULL;
+  if (!aligned16(Wq) || !aligned16(B16)) return Q8_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != Q8_OK) return st;
+  if (N * K == 0) return Q8_OK;
+  return launch_status(launch_codes_to_f16(Wq, B16, N * K, dev, stream));
+}
+
+q8_status q8_linear_prepared(const void* x, q8_dtype xtype, const float* norm_weight,
+                             float norm_eps, const uint16_t* B16, const uint16_t* Wd,
+                             q8_epilogue epi, const float* aux, void* y, q8_dtype ytype,
+                             int64_t M, int64_t N, int64_t K, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  Prologue pro;
+  Epilogue e;
+  q8_status st = fused_neighbours(norm_weight, norm_eps, epi, aux, ytype, M, N, &pro, &e);
+  if (st != Q8_OK) return st;
+  if (N * K > 0 && B16 == nullptr) return Q8_ERR_NULL;
+  const bool library_ws = workspace == nullptr && workspace_bytes == 0;
+  // B16 stands in for Wq in the common checks (non-null, aligned); empty shapes return before
+  // anything reads it
+  return linear_impl(x, xtype, reinterpret_cast<const int8_t*>(B16), Wd, static_cast<float*>(y), M,
+                     N, K, Q8_PATH_TENSOR, workspace, workspace_bytes, library_ws, stream, e, pro, B16);
+}
+
+size_t q8_linear_prepared_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (check_shape(M, N, K) != Q8_OK) return 0;
+  DeviceInfo dev;
+  if (current_device(&dev) != Q8_OK) return 0;
+  return path_ws_bytes(Q8_PATH_TENSOR, M, N, K, gemm_part_bytes(M, N, K, dev), false);
 }
 
 q8_status q8_kv3_encode(const void* x, q8_dtype xtype, uint32_t* codes, float* scales,

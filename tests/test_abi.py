@@ -133,3 +133,25 @@ def test_kv3_codec_rejects_bad_arguments(L):
     assert D(P(FAKE), None, P(FAKE), 1, 4, None) == 1
     assert D(P(FAKE + 8), P(FAKE), P(FAKE), 1, 4, None) == 3
     assert D(P(FAKE), P(FAKE), P(FAKE), 1, 1 << 50, None) == 2
+
+
+def test_prepared_entry_rejects_bad_arguments(L):
+    W = L.q8_weights_to_f16
+    W.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64, P]
+    assert W(None, P(FAKE), 4, 64, None) == 1
+    assert W(P(FAKE), P(FAKE + 2), 4, 64, None) == 3
+    assert W(P(FAKE), P(FAKE), 4, 33, None) == 2
+    F = L.q8_linear_prepared
+    F.argtypes = [P, ctypes.c_int, P, ctypes.c_float, P, P, ctypes.c_int, P, P, ctypes.c_int,
+                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, ctypes.c_size_t, P]
+    ok = [P(FAKE), 1, None, 1e-6, P(FAKE), P(FAKE), 0, None, P(FAKE), 0, 2, 2, 64, None, 0, None]
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return F(*a)
+    assert call(a4=None) == 1          # no prepared weights
+    assert call(a6=5) == 4             # unknown epilogue
+    assert call(a4=P(FAKE + 8)) == 3   # misaligned prepared weights
+    assert call(a12=40) == 2
