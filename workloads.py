@@ -17,6 +17,9 @@ Recipe (numpy PCG64 via default_rng):
     except on round(outlier_frac * head_dim) channels (the same for every token and head)
     where it is `gain`; rounded to bfloat16; cut into 128-element groups (a 256-wide head
     is two groups).
+  * block-sparse attention: q, k, v standard_normal float32 rounded to bfloat16; the block
+    pattern per head and 64-token query block keeps the first key block, the two blocks
+    ending at the diagonal, and each other earlier block with probability 0.1.
 """
 from dataclasses import dataclass, field
 from typing import List, Tuple
@@ -149,3 +152,50 @@ def kv_groups(rng: np.random.Generator, tokens: int, heads: int, head_dim: int =
 # 256K-token context of the post's 3-bit KV cache: one attention layer's keys (or values),
 # 4 KV heads of 256 channels
 KV3_LAYER_256K = dict(tokens=262144, heads=4, head_dim=256)
+
+
+BSA_BLOCK = 64
+
+
+def bsa_qkv(rng: np.random.Generator, H: int, Hkv: int, T: int, d: int = 128):
+    """Synthetic queries, keys and values: standard_normal float32 rounded to bfloat16 bits,
+    q [H,T,d], k and v [Hkv,T,d]."""
+    q = bf16_bits_from_f32(rng.standard_normal((H, T, d), dtype=np.float32))
+    k = bf16_bits_from_f32(rng.standard_normal((Hkv, T, d), dtype=np.float32))
+    v = bf16_bits_from_f32(rng.standard_normal((Hkv, T, d), dtype=np.float32))
+    return q, k, v
+
+
+def bsa_mask(rng: np.random.Generator, H: int, T: int, density: float = 0.1, local: int = 2):
+    """A block-sparse causal pattern as CSR (row_ptr [H*nb+1], col_idx): per head and query
+    block qb, the first key block (the attention sink), the `local` blocks ending at qb (the
+    diagonal included), and each other earlier block with probability `density`."""
+    nb = T // BSA_BLOCK
+    row_ptr = [0]
+    cols = []
+    for _h in range(H):
+        for qb in range(nb):
+            keep = rng.random(qb + 1) < density
+            keep[0] = True
+            keep[max(0, qb - local + 1):qb + 1] = True
+            sel = np.nonzero(keep)[0]
+            cols.extend(sel.tolist())
+            row_ptr.append(len(cols))
+    return np.array(row_ptr, np.int32), np.array(cols, np.int32)
+
+
+def dense_causal_mask(H: int, T: int):
+    """Every block at or below the diagonal: plain causal attention."""
+    nb = T // BSA_BLOCK
+    row_ptr = [0]
+    cols = []
+    for _h in range(H):
+        for qb in range(nb):
+            cols.extend(range(qb + 1))
+            row_ptr.append(len(cols))
+    return np.array(row_ptr, np.int32), np.array(cols, np.int32)
+
+
+# long prefill with block-sparse attention: 32 query heads over 8 key/value heads, head
+# dim 128, 32768 tokens, about 10 % of the causal key blocks
+BSA_32K = dict(H=32, Hkv=8, T=32768, d=128, density=0.1)
