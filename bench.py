@@ -433,6 +433,42 @@ def run_kv3(torch, q8, dev, steps, warmup, pk, pk_src):
     return res
 
 
+def run_bsa(torch, q8, dev, steps, warmup, pk, pk_src):
+    """Block-sparse causal attention at a 32K-token prefill (32 query heads over 8
+    key/value heads, head dim 128, ~10 % of the causal key blocks).  Algorithmic flops:
+    4 * d per visible (query, key) pair, counted from the block lists (a listed block
+    below the diagonal holds 64 x 64 pairs, the diagonal block 64 * 65 / 2)."""
+    cfg = workloads.BSA_32K
+    rng = np.random.default_rng(13)
+    q, k, v = workloads.bsa_qkv(rng, cfg["H"], cfg["Hkv"], cfg["T"], cfg["d"])
+    rp, ci = workloads.bsa_mask(rng, cfg["H"], cfg["T"], cfg["density"])
+    nb = cfg["T"] // 64
+    rows = np.repeat(np.tile(np.arange(nb), cfg["H"]), np.diff(rp))
+    pairs = int(np.sum(np.where(ci == rows, 64 * 65 // 2, 64 * 64)))
+    flops = 4 * cfg["d"] * pairs
+    dt = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    qt, kt, vt = dt(q), dt(k), dt(v)
+    rpt, cit = torch.from_numpy(rp).to(dev), torch.from_numpy(ci).to(dev)
+    o = torch.empty((cfg["H"], cfg["T"], cfg["d"]), dtype=torch.bfloat16, device=dev)
+    fn = lambda: q8.q8_bsa_attention(qt, kt, vt, rpt, cit, out_dtype=torch.bfloat16, o=o)
+    fn()
+    total, kern = time_graph_steps(torch, q8, [fn], steps, warmup, instrument=False)
+    tf = flops / kern / 1e12
+    mma_sync_peak = 1024 * 2 * 152 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    return {"bsa_32k": {"value": round(tf, 2), "unit": "TFLOP/s", "us_per_step": round(kern * 1e6, 2),
+                        "algorithmic_flops_per_launch": flops, "visible_pairs": pairs,
+                        "block_density": round(len(ci) / (cfg["H"] * nb * (nb + 1) / 2), 4),
+                        "roofline": {"bound": "tensor", "achieved": round(tf, 2),
+                                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                                     "frac": round(tf / pk["bf16_tflops"], 4),
+                                     "peak_source": f"bf16_tflops (burst) of the {pk_src} peaks",
+                                     "mma_sync_ceiling_tflops": round(mma_sync_peak, 1),
+                                     "kernel": "q8::bsa_kernel"},
+                        "steps": steps,
+                        "note": ("block-sparse causal attention (MInference-style), mma.sync "
+                                 "bf16 tensor cores, FlashAttention-2 online softmax")}}
+
+
 def e2e_measure(torch, q8, dev, x_np, bf16, Wqs, Wds, M, N, K, steps, warmup, bytes_step, ops_step,
                 bound, path=None):
     """End to end through the public call q8_linear / q8_linear_ex: per step the H2D copy of x
@@ -534,6 +570,7 @@ def gpu_arm(args):
                                       "torch silu, multiply and bfloat16 cast; us_per_step is "
                                       "the whole step, roofline the layer's kernel alone")
         extra.update(run_kv3(torch, q8, dev, 200, 10, pk, pk_src))
+        extra.update(run_bsa(torch, q8, dev, 20, 3, pk, pk_src))
         for k in ("kv3_encode_256k", "kv3_decode_256k"):
             extra[k]["note"] = ("3-bit KV-cache codec (Walsh-Hadamard rotation + Lloyd-Max), "
                                 "one attention layer's keys at a 256K-token context")

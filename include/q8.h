@@ -192,6 +192,27 @@ q8_status q8_kv3_decode(const uint32_t* codes, const float* scales, void* out, q
                         int64_t ngroups, cudaStream_t stream);
 
 /*
+ * q8_bsa_attention -- block-sparse causal attention for long prefill.  The post speeds up
+ * long prefill with MInference-style block-sparse attention ("CUDA inference engine for
+ * running Qwen3.5/3.6 hybrid models on mining cards (CMP 100-210)", news.hada.io topic
+ * 29953, feature list).  Query t of head h attends to the keys j <= t of the 64-token key
+ * blocks listed for its 64-token query block; H query heads share Hkv key/value heads
+ * (head h reads h / (H / Hkv)); o_t = softmax(q_t . k_j / sqrt(d)) weighted sum of v_j; a
+ * query that sees no key gets 0.
+ *   q [H][T][d], k and v [Hkv][T][d]: bfloat16 bits; d = 128; T a multiple of 64.
+ *   row_ptr [H * T/64 + 1], col_idx [nnz]: int32 CSR over (head, query block) rows; the
+ *     key blocks of a row ascending, each in [0, query block] (others are skipped and set
+ *     bit 8 of the device error word).
+ *   o [H][T][d]: binary32 (otype Q8_F32) or bfloat16 (Q8_BF16).
+ * Softmax in binary32 (base-2 exponentials), products on the tensor cores with the weights
+ * rounded to bfloat16, as in FlashAttention.
+ */
+q8_status q8_bsa_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const int32_t* row_ptr, const int32_t* col_idx, int64_t nnz, void* o,
+                           q8_dtype otype, int64_t H, int64_t Hkv, int64_t T, int64_t d,
+                           cudaStream_t stream);
+
+/*
  * Prepared weights for the tensor-core path.  The tensor path feeds the MMA binary16
  * copies of the int8 codes (exact: |q| <= 127); q8_linear / q8_linear_ex / q8_linear_fused
  * widen the codes on every call (read N*K bytes, write and re-read 2*N*K).  For weights

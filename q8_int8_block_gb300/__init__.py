@@ -15,6 +15,7 @@ this package fails.
     xq, xd, r = q8_quantize_act_rmsnorm(h, g, 1e-6)
     B16 = q8_weights_to_f16(Wq)                        # once per weight matrix
     y = q8_linear_prepared(x, B16, Wd)                 # tensor-core path, no per-call widening
+    o = q8_bsa_attention(q, k, v, row_ptr, col_idx)    # block-sparse causal attention
     codes, scales = q8_kv3_encode(kv)                  # kv [..., 128] -> 3-bit codes + scales
     kv_hat = q8_kv3_decode(codes, scales, torch.bfloat16)
     isum = q8_block_sums(xq, Wq, path="decode")  # int32 [M,N,K/32]
@@ -27,6 +28,7 @@ import torch
 __all__ = ["Q8Error", "q8_quantize_weights", "q8_quantize_act", "q8_quantize_act_rmsnorm",
            "q8_linear", "q8_linear_ex", "q8_kv3_encode", "q8_kv3_decode", "KV3_GROUP",
            "q8_weights_to_f16", "q8_linear_prepared", "q8_linear_prepared_workspace_size",
+           "q8_bsa_attention",
            "q8_linear_fused", "EPILOGUES",
            "q8_linear_workspace_size", "q8_block_sums", "q8_device_error", "q8_release",
            "q8_set_timing_events", "q8_linear_noalloc", "NOALLOC_SCRATCH_BYTES",
@@ -71,6 +73,7 @@ def _load():
         "q8_kv3_encode": [p, i32, p, p, i64, p],
         "q8_kv3_decode": [p, p, p, i32, i64, p],
         "q8_weights_to_f16": [p, p, i64, i64, p],
+        "q8_bsa_attention": [p, p, p, p, p, i64, p, i32, i64, i64, i64, i64, p],
         "q8_linear_prepared": [p, i32, p, f32, p, p, i32, p, p, i32, i64, i64, i64, p, sz, p],
     }
     for name, args in sigs.items():
@@ -304,6 +307,28 @@ def q8_linear_prepared(x, B16, Wd, epi="none", aux=None, y=None, out_dtype=torch
                                  DTYPES[out_dtype], M, N, K, _ptr(workspace), nbytes,
                                  _stream(stream)), "q8_linear_prepared")
     return y
+
+
+def q8_bsa_attention(q, k, v, row_ptr, col_idx, out_dtype=torch.float32, o=None, stream=None):
+    """Block-sparse causal attention: q [H,T,128], k and v [Hkv,T,128] bfloat16; row_ptr
+    int32 [H*T/64+1], col_idx int32 [nnz] (the listed 64-token key blocks of each head's
+    64-token query block) -> o [H,T,128] of out_dtype."""
+    H, T, d = q.shape
+    Hkv = k.shape[0]
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, (H if name == "q" else Hkv, T, d), name)
+    _need(row_ptr, torch.int32, (H * (T // 64) + 1,), "row_ptr")
+    if col_idx.dtype != torch.int32 or col_idx.dim() != 1 or not col_idx.is_cuda:
+        raise ValueError("col_idx: a 1-D int32 CUDA tensor")
+    if out_dtype not in DTYPES:
+        raise TypeError(f"out_dtype: expected bfloat16 or float32, got {out_dtype}")
+    if o is None:
+        o = torch.empty((H, T, d), dtype=out_dtype, device=q.device)
+    _need(o, out_dtype, (H, T, d), "o")
+    _check(_L.q8_bsa_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(row_ptr), _ptr(col_idx),
+                               col_idx.numel(), _ptr(o), DTYPES[out_dtype], H, Hkv, T, d,
+                               _stream(stream)), "q8_bsa_attention")
+    return o
 
 
 KV3_GROUP = 128

@@ -432,6 +432,26 @@ size_t q8_linear_prepared_workspace_size(int64_t M, int64_t N, int64_t K) {
   return path_ws_bytes(Q8_PATH_TENSOR, M, N, K, gemm_part_bytes(M, N, K, dev), false);
 }
 
+q8_status q8_bsa_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const int32_t* row_ptr, const int32_t* col_idx, int64_t nnz, void* o,
+                           q8_dtype otype, int64_t H, int64_t Hkv, int64_t T, int64_t d,
+                           cudaStream_t stream) {
+  if (otype != Q8_F32 && otype != Q8_BF16) return Q8_ERR_DTYPE;
+  if (d != 128 || H < 0 || Hkv <= 0 || T < 0 || T % 64 != 0 || nnz < 0 || H % Hkv != 0 ||
+      H > 0x7FFFFFFF || T > 0x7FFFFFFF || static_cast<double>(H) * T * d * 4 > 281474976710656.0 ||
+      static_cast<double>(H) * (T / 64) >= 2147483647.0)
+    return Q8_ERR_SHAPE;
+  if (H * T > 0 && (q == nullptr || k == nullptr || v == nullptr || o == nullptr || row_ptr == nullptr ||
+                    (nnz > 0 && col_idx == nullptr)))
+    return Q8_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return Q8_ERR_ALIGN;
+  DeviceInfo dev;
+  q8_status st = current_device(&dev);
+  if (st != Q8_OK) return st;
+  return launch_status(
+      launch_bsa(q, k, v, row_ptr, col_idx, nnz, o, static_cast<int>(otype), H, Hkv, T, dev, stream));
+}
+
 q8_status q8_kv3_encode(const void* x, q8_dtype xtype, uint32_t* codes, float* scales,
                         int64_t ngroups, cudaStream_t stream) {
   if (xtype != Q8_F32 && xtype != Q8_BF16) return Q8_ERR_DTYPE;

@@ -105,6 +105,13 @@ cudaError_t launch_kv3_encode(const void* x, int xtype, uint32_t* codes, float* 
 cudaError_t launch_kv3_decode(const uint32_t* codes, const float* scales, void* out, int otype,
                               int64_t n, const DeviceInfo& dev, cudaStream_t stream);
 
+// ---- q8_bsa.cu -------------------------------------------------------------------
+// Block-sparse causal attention (64-token blocks, head dim 128, CSR block lists).
+cudaError_t launch_bsa(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       const int32_t* row_ptr, const int32_t* col_idx, int64_t nnz, void* o,
+                       int otype, int64_t H, int64_t Hkv, int64_t T, const DeviceInfo& dev,
+                       cudaStream_t stream);
+
 // ---- q8_gemm.cu -------------------------------------------------------------------
 // Tensor-core GEMM on binary16 codes: A16 [M,K] activation codes, B16 [N,K] weight codes,
 // xd [M,K/32] f32, Wd [N,K/32] binary16 bits.  Writes y [M,N] (rescaled sum) or, when

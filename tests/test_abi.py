@@ -155,3 +155,22 @@ def test_prepared_entry_rejects_bad_arguments(L):
     assert call(a6=5) == 4             # unknown epilogue
     assert call(a4=P(FAKE + 8)) == 3   # misaligned prepared weights
     assert call(a12=40) == 2
+
+
+def test_bsa_entry_rejects_bad_arguments(L):
+    F = L.q8_bsa_attention
+    F.argtypes = [P, P, P, P, P, ctypes.c_int64, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_int64, ctypes.c_int64, P]
+    ok = [P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 4, P(FAKE), 0, 4, 2, 128, 128, None]
+
+    def call(i, val):
+        a = list(ok)
+        a[i] = val
+        return F(*a)
+    assert call(7, 5) == 4            # output type
+    assert call(11, 64) == 2          # head dim other than 128
+    assert call(10, 100) == 2         # T not a multiple of 64
+    assert call(9, 3) == 2            # H not a multiple of Hkv
+    assert call(0, None) == 1
+    assert call(4, None) == 1         # nnz > 0 without col_idx
+    assert call(1, P(FAKE + 2)) == 3
