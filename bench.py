@@ -210,6 +210,7 @@ TRAFFIC_PROFILES = {  # committed ncu summaries that record DRAM bytes per launc
                    ["q8_batch.cu", "q8_ptx.cuh", "q8_quant_dev.cuh", "q8_epi.cuh"]),
     "kv3_encode_256k": ("kv3_encode_kernel_256k_layer.md", ["q8_kv3.cu"]),
     "kv3_decode_256k": ("kv3_decode_kernel_256k_layer.md", ["q8_kv3.cu"]),
+    "bsa_32k": ("bsa_kernel_32k_prefill.md", ["q8_bsa.cu", "q8_ptx.cuh"]),
 }
 
 
@@ -463,7 +464,8 @@ def run_bsa(torch, q8, dev, steps, warmup, pk, pk_src):
                                      "frac": round(tf / pk["bf16_tflops"], 4),
                                      "peak_source": f"bf16_tflops (burst) of the {pk_src} peaks",
                                      "mma_sync_ceiling_tflops": round(mma_sync_peak, 1),
-                                     "kernel": "q8::bsa_kernel"},
+                                     "kernel": "q8::bsa_kernel",
+                                     "traffic": profiled_traffic(*TRAFFIC_PROFILES["bsa_32k"])},
                         "steps": steps,
                         "note": ("block-sparse causal attention (MInference-style), mma.sync "
                                  "bf16 tensor cores, FlashAttention-2 online softmax")}}
@@ -715,6 +717,8 @@ def parse_args(argv=None):
                     help="force a kernel family for --workload (default: the library's choice)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every point of the dense-layer sweep workload (one GPU) and exit")
+    ap.add_argument("--bsa", action="store_true",
+                    help="time only block-sparse attention (32K-token prefill) and exit")
     ap.add_argument("--kv3", action="store_true",
                     help="time only the 3-bit KV-cache codec (one layer's keys at a 256K-token "
                          "context: encode and decode) and exit")
@@ -771,6 +775,16 @@ def main(argv=None):
     args = parse_args(argv)
     if args.sweep:
         print(json.dumps(sweep_arm(args)), flush=True)
+        return
+    if args.bsa:
+        import torch
+        import __graft_entry__ as g
+        g.build()
+        import q8_int8_block_gb300 as q8
+        torch.cuda.set_device(0)
+        pk, pk_src = peaks()
+        r = run_bsa(torch, q8, torch.device("cuda", 0), args.steps, args.warmup, pk, pk_src)
+        print(json.dumps({"bsa": r, "device_error_word": q8.q8_device_error()}), flush=True)
         return
     if args.kv3:
         import torch
