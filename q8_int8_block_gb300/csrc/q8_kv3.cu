@@ -35,11 +35,23 @@ constexpr int kD = 128;
 constexpr int kWords = 12;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
-// +-level of a 3-bit code (bit 2: the sign, bits 0-1: the magnitude cell)
-__device__ __forceinline__ float kv3_value(uint32_t code) {
-  const float lo = (code & 1u) ? 0.7560f : 0.2451f;
-  const float hi = (code & 1u) ? 2.1520f : 1.3440f;
-  return __uint_as_float(__float_as_uint((code & 2u) ? hi : lo) | ((code & 4u) << 29));
+// +-level of each 3-bit code (bit 2: the sign, bits 0-1: the magnitude cell); the decoder
+// copies it to shared memory and looks codes up there (one load in place of a chain of
+// selects on the integer pipe)
+__constant__ float kLevel[8] = {0.2451f,  0.7560f,  1.3440f,  2.1520f,
+                                -0.2451f, -0.7560f, -1.3440f, -2.1520f};
+
+// 0xFFFFFFFF if a >= b (ordered: false on NaN), else 0
+__device__ __forceinline__ uint32_t set_ge(float a, float b) {
+  uint32_t d;
+  asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(d) : "f"(a), "f"(b));
+  return d;
+}
+// 0xFFFFFFFF if a < b (ordered), else 0
+__device__ __forceinline__ uint32_t set_lt(float a, float b) {
+  uint32_t d;
+  asm("set.lt.u32.f32 %0, %1, %2;" : "=r"(d) : "f"(a), "f"(b));
+  return d;
 }
 
 constexpr int kE = 8;  // elements of a (c, t) chunk
@@ -153,10 +165,12 @@ __global__ void __launch_bounds__(256) kv3_encode_kernel(const Kv3Params p) {
       uint32_t bits = 0;
 #pragma unroll
       for (int e = 0; e < kE; ++e) {
+        // each true compare gives -1, so the sum is minus the code 4 neg + m (m the thresholds
+        // passed, neg the sign; -0 counts as positive); subtracted at bit 3 e
         const float a = fabsf(v[c][e]);
-        const uint32_t m = (a >= t0 ? 1u : 0u) + (a >= t1 ? 1u : 0u) + (a >= t2 ? 1u : 0u);
-        const uint32_t neg = v[c][e] < 0.0f ? 4u : 0u;  // -0 counts as positive
-        bits |= (neg | m) << (3 * e);
+        const uint32_t minus_code =
+            set_ge(a, t0) + set_ge(a, t1) + set_ge(a, t2) + 4u * set_lt(v[c][e], 0.0f);
+        bits -= minus_code << (3 * e);
       }
       chunk[c] = s == 0.0f ? 0u : bits;
     }
@@ -191,6 +205,9 @@ __device__ __forceinline__ void load_chunks(const uint32_t* codes, int64_t g, in
 
 template <int kOType>
 __global__ void __launch_bounds__(256) kv3_decode_kernel(const Kv3Params p) {
+  __shared__ float level[8];
+  if (threadIdx.x < 8) level[threadIdx.x] = kLevel[threadIdx.x];
+  __syncthreads();
   const int lane = threadIdx.x & 31, t = lane & 3;
   const int64_t team = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 2;
   const int64_t nteams = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 2;
@@ -212,7 +229,7 @@ __global__ void __launch_bounds__(256) kv3_decode_kernel(const Kv3Params p) {
     for (int c = 0; c < 4; ++c) {
       const uint32_t chunk = ((lo[c] >> off) | (off > 8 ? hi[c] << (32 - off) : 0u)) & 0xFFFFFFu;
 #pragma unroll
-      for (int e = 0; e < kE; ++e) v[c][e] = __fmul_rn(s, kv3_value(chunk >> (3 * e)));
+      for (int e = 0; e < kE; ++e) v[c][e] = __fmul_rn(s, level[(chunk >> (3 * e)) & 7u]);
     }
     fwht_group(v, t);
     if (g < p.n) {

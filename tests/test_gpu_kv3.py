@@ -37,7 +37,8 @@ def _u32(t):
 
 def _crafted(rng):
     """Zero groups, exact-zero rotations, unit vectors, large and small groups (inside the
-    binary32 range of the sum of squares), a group whose sum of squares underflows."""
+    binary32 range of the sum of squares), a group whose sum of squares underflows, and a
+    group with a negative-zero rotation output."""
     g = []
     g.append(np.zeros(128, np.float32))
     e = np.zeros(128, np.float32)
@@ -51,6 +52,10 @@ def _crafted(rng):
     g.append(rng.standard_normal(128).astype(np.float32) * np.float32(1e-15))
     g.append(rng.standard_normal(128).astype(np.float32) * np.float32(1e-30))  # s underflows to 0
     g.append(np.full(128, 3.0, np.float32))
+    z = np.zeros(128, np.float32)  # rotation output 127 is -0 while s != 0: a positive code
+    z[0] = -0.0
+    z[2] = z[3] = 5.0
+    g.append(z)
     return np.stack(g)
 
 
@@ -59,7 +64,9 @@ def test_encode_decode_bit_exact(q8, n, bf16):
     rng = np.random.default_rng(n)
     x = workloads.kv_groups(rng, n, 1, 128, outlier_frac=0.03, bf16=bf16)
     if not bf16:
-        x[: min(n, 9)] = _crafted(rng)[: min(n, 9)]
+        cr = _crafted(rng)
+        k = min(n, len(cr))
+        x[:k] = cr[:k]
     words, scales = OK.encode(x, bf16=bf16)
     c, s = q8.q8_kv3_encode(T(x))
     assert np.array_equal(_u32(c), words)

@@ -167,3 +167,19 @@ def test_exact_zeros_get_the_positive_code():
     u = H[:, 0] + H[:, 1]
     assert scales[0] == np.float32(math.sqrt(2.0))
     assert np.array_equal(kv3.codes(words)[0], np.where(u == 0, 0, 2))
+
+
+def test_negative_zero_rotation_output_gets_the_positive_code():
+    """x = -0 e_0 + 5 e_2 + 5 e_3.  The last output of the rotation is
+    ((-0 - 0) - (5 - 5)) - 0 - ... (it takes the difference at every stage, and every later
+    subtrahend is an exact +0); IEEE subtraction gives -0 - (+0) = -0, so it is a negative
+    zero while the group's RMS is not 0.  u < 0 is false for it,
+    so its code is 0 (cell 0, positive sign), like a +0."""
+    x = np.zeros((1, 128), np.float32)
+    x[0, 0] = -0.0
+    x[0, 2] = x[0, 3] = 5.0
+    u = np.asarray(kv3.fwht(x[0]), np.float32)
+    assert u[127] == 0 and np.signbit(u[127])
+    words, scales = kv3.encode(x)
+    assert scales[0] == np.sqrt(np.float32(50.0))  # 64 outputs of +-10: ss / 128 = 50
+    assert kv3.codes(words)[0][127] == 0

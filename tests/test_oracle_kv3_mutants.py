@@ -26,6 +26,7 @@ PINS = [
     lambda: P.test_unit_vector_codes_layout_and_exact_round_trip(127, 8.0),
     P.test_zero_group,
     P.test_exact_zeros_get_the_positive_code,
+    P.test_negative_zero_rotation_output_gets_the_positive_code,
     P.test_scale_is_the_rms_of_the_rotated_group,
     P.test_gaussian_distortion_is_the_lloyd_max_one,
 ]
@@ -39,6 +40,8 @@ MUTANTS = [
     ("level typo", "{0.2451f, 0.7560f, 1.3440f, 2.1520f}", "{0.2451f, 0.7650f, 1.3440f, 2.1520f}"),
     ("threshold typo", "{0.5006f, 1.0500f, 1.7480f}", "{0.5006f, 1.0050f, 1.7480f}"),
     ("sign on u <= 0", "uint32_t code = (u[i] < 0.0f ? 4u : 0u) | m;", "uint32_t code = (u[i] <= 0.0f ? 4u : 0u) | m;"),
+    ("sign from the sign bit", "uint32_t code = (u[i] < 0.0f ? 4u : 0u) | m;",
+     "uint32_t code = (signbit(u[i]) ? 4u : 0u) | m;"),
     ("threshold not scaled", "T[k] = okv3_threshold[k] * s;", "T[k] = okv3_threshold[k];"),
     ("bit offset", "int bit = 3 * i;\n        words[bit / 32] |= code << (bit % 32);",
      "int bit = 3 * i + 1;\n        words[bit / 32] |= code << (bit % 32);"),
