@@ -49,13 +49,13 @@ typedef enum q8_status {
     Q8_OK = 0,
     Q8_ERR_NULL = 1,     /* a required pointer is NULL                                 */
     Q8_ERR_SHAPE = 2,    /* M, N or K < 0, K not a multiple of 32, or a size overflows  */
-    Q8_ERR_ALIGN = 3,    /* an array pointer is not 16-byte aligned                     */
+    Q8_ERR_ALIGN = 3,    /* an array pointer is not aligned as required (16 bytes mostly) */
     Q8_ERR_DTYPE = 4,    /* unknown activation type or path selector                    */
     Q8_ERR_NOMEM = 5,    /* workspace too small, or the library could not allocate one  */
     Q8_ERR_CUDA = 6,     /* a CUDA runtime call failed                                  */
     Q8_ERR_DEVICE = 7,   /* the current device is not compute capability 10.3           */
     Q8_ERR_CAPTURE = 8,  /* the call would allocate while its stream is being captured  */
-    Q8_ERR_VALUE = 9     /* a scalar argument is outside its domain (e.g. eps <= 0)      */
+    Q8_ERR_VALUE = 9     /* an argument outside its domain (eps <= 0, aux overlapping y) */
 } q8_status;
 
 typedef enum q8_dtype {
@@ -153,8 +153,8 @@ q8_status q8_quantize_act_rmsnorm(const void* x, q8_dtype xtype, const float* ga
  * the epilogue of zero.
  * Errors: Q8_ERR_DTYPE for an unknown epilogue, output or activation type; Q8_ERR_NULL for
  * a NULL aux with an epilogue that reads it; Q8_ERR_ALIGN for aux or norm_weight not
- * 16-byte aligned; Q8_ERR_VALUE for a norm_eps that is not finite and > 0; the rest as
- * q8_linear_ex.
+ * 16-byte aligned; Q8_ERR_VALUE for a norm_eps that is not finite and > 0, or for an aux
+ * whose M*N floats overlap the bytes of y; the rest as q8_linear_ex.
  */
 typedef enum q8_epilogue {
     Q8_EPI_NONE = 0,
@@ -204,6 +204,7 @@ q8_status q8_kv3_decode(const uint32_t* codes, const float* scales, void* out, q
  *     key blocks of a row ascending, each in [0, query block] (others are skipped and set
  *     bit 8 of the device error word).
  *   o [H][T][d]: binary32 (otype Q8_F32) or bfloat16 (Q8_BF16).
+ *   q, k, v and o 16-byte aligned, row_ptr and col_idx 4-byte aligned (else Q8_ERR_ALIGN).
  * Softmax in binary32 (base-2 exponentials), products on the tensor cores with the weights
  * rounded to bfloat16, as in FlashAttention.
  */

@@ -361,12 +361,23 @@ namespace q8 {
 namespace {
 // The neighbours of q8_linear_fused / q8_linear_prepared, checked.
 q8_status fused_neighbours(const float* norm_weight, float norm_eps, q8_epilogue epi,
-                           const float* aux, q8_dtype ytype, int64_t M, int64_t N, Prologue* pro,
-                           Epilogue* e) {
+                           const float* aux, const void* y, q8_dtype ytype, int64_t M, int64_t N,
+                           int64_t K, Prologue* pro, Epilogue* e) {
   if (epi != Q8_EPI_NONE && epi != Q8_EPI_ADD && epi != Q8_EPI_SILU_MUL) return Q8_ERR_DTYPE;
   if (ytype != Q8_F32 && ytype != Q8_BF16) return Q8_ERR_DTYPE;
   if (epi != Q8_EPI_NONE && M > 0 && N > 0 && aux == nullptr) return Q8_ERR_NULL;
   if (!aligned16(aux) || !aligned16(norm_weight)) return Q8_ERR_ALIGN;
+  if (epi != Q8_EPI_NONE && M > 0 && N > 0 && y != nullptr) {
+    // aux is read through the read-only data path while y is written: the two byte ranges
+    // must be disjoint (the shape check bounds both below 2^48 bytes)
+    const q8_status st = check_shape(M, N, K);
+    if (st != Q8_OK) return st;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(aux);
+    const uintptr_t y0 = reinterpret_cast<uintptr_t>(y);
+    const uintptr_t a1 = a0 + static_cast<uintptr_t>(M * N) * 4u;
+    const uintptr_t y1 = y0 + static_cast<uintptr_t>(M * N) * (ytype == Q8_BF16 ? 2u : 4u);
+    if (a0 < y1 && y0 < a1) return Q8_ERR_VALUE;
+  }
   if (norm_weight != nullptr) {
     if (!(norm_eps > 0.0f) || !std::isfinite(norm_eps)) return Q8_ERR_VALUE;
     pro->gamma = norm_weight;
@@ -389,7 +400,7 @@ q8_status q8_linear_fused(const void* x, q8_dtype xtype, const float* norm_weigh
                           cudaStream_t stream) {
   Prologue pro;
   Epilogue e;
-  q8_status st = fused_neighbours(norm_weight, norm_eps, epi, aux, ytype, M, N, &pro, &e);
+  q8_status st = fused_neighbours(norm_weight, norm_eps, epi, aux, y, ytype, M, N, K, &pro, &e);
   if (st != Q8_OK) return st;
   const bool library_ws = workspace == nullptr && workspace_bytes == 0;
   return linear_impl(x, xtype, Wq, Wd, static_cast<float*>(y), M, N, K, path, workspace,
@@ -415,7 +426,7 @@ q8_status q8_linear_prepared(const void* x, q8_dtype xtype, const float* norm_we
                              size_t workspace_bytes, cudaStream_t stream) {
   Prologue pro;
   Epilogue e;
-  q8_status st = fused_neighbours(norm_weight, norm_eps, epi, aux, ytype, M, N, &pro, &e);
+  q8_status st = fused_neighbours(norm_weight, norm_eps, epi, aux, y, ytype, M, N, K, &pro, &e);
   if (st != Q8_OK) return st;
   if (N * K > 0 && B16 == nullptr) return Q8_ERR_NULL;
   const bool library_ws = workspace == nullptr && workspace_bytes == 0;
@@ -445,6 +456,9 @@ q8_status q8_bsa_attention(const uint16_t* q, const uint16_t* k, const uint16_t*
                     (nnz > 0 && col_idx == nullptr)))
     return Q8_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return Q8_ERR_ALIGN;
+  // the block lists are read as int32 words on the device
+  if ((reinterpret_cast<uintptr_t>(row_ptr) & 3u) != 0 || (reinterpret_cast<uintptr_t>(col_idx) & 3u) != 0)
+    return Q8_ERR_ALIGN;
   DeviceInfo dev;
   q8_status st = current_device(&dev);
   if (st != Q8_OK) return st;

@@ -92,7 +92,8 @@ def test_valid_call_without_gpu_fails_cleanly(L):
 
 def test_fused_entry_rejects_bad_arguments(L):
     F = L.q8_linear_fused
-    ok = [P(FAKE), 1, None, 1e-6, P(FAKE), P(FAKE), 1, P(FAKE), P(FAKE), 0, 2, 2, 64, 0, None, 0, None]
+    ok = [P(FAKE), 1, None, 1e-6, P(FAKE), P(FAKE), 1, P(FAKE), P(FAKE + 0x1000), 0, 2, 2, 64, 0, None,
+          0, None]
 
     def call(**kw):
         a = list(ok)
@@ -109,6 +110,12 @@ def test_fused_entry_rejects_bad_arguments(L):
     assert call(a2=P(FAKE + 4)) == 3  # misaligned norm weight
     for eps in (0.0, -1e-6, float("nan"), float("inf")):
         assert call(a2=P(FAKE), a3=eps) == 9
+    # aux (M*N floats) overlapping y: in place, bfloat16 y in place, and a partial overlap
+    # (64 x 64 floats of aux reach 16 KB past it, y starts 4 KB in)
+    assert call(a8=P(FAKE)) == 9
+    assert call(a8=P(FAKE), a9=1) == 9
+    assert call(a8=P(FAKE + 0x1000), a10=64, a11=64) == 9
+    assert call(a7=P(FAKE + 0x1000), a8=P(FAKE), a10=64, a11=64) == 9
 
 
 def test_rmsnorm_quantizer_rejects_bad_arguments(L):
@@ -174,3 +181,5 @@ def test_bsa_entry_rejects_bad_arguments(L):
     assert call(0, None) == 1
     assert call(4, None) == 1         # nnz > 0 without col_idx
     assert call(1, P(FAKE + 2)) == 3
+    assert call(3, P(FAKE + 2)) == 3   # row_ptr not on an int32 boundary
+    assert call(4, P(FAKE + 1)) == 3   # col_idx likewise
