@@ -24,8 +24,10 @@
  *
  * Conventions for every entry point:
  *   - all array pointers are DEVICE pointers owned by the caller; the library never
- *     frees or keeps them; every array pointer must be 16-byte aligned; the pointer of an
- *     empty array (zero elements) may be NULL;
+ *     frees or keeps them; every array pointer must be 16-byte aligned unless its entry
+ *     point says otherwise; the pointer of an empty array (zero elements) may be NULL;
+ *   - an output array must not overlap any input or other output of the same call (the
+ *     kernels read inputs while other blocks write outputs); only aux against y is checked;
  *   - calls are asynchronous on `stream` (0 = the legacy default stream); inputs must
  *     stay valid and outputs untouched until the stream passes the call;
  *   - arguments are checked on the host before anything is launched; on any error
