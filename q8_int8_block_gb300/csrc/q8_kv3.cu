@@ -41,19 +41,6 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 __constant__ float kLevel[8] = {0.2451f,  0.7560f,  1.3440f,  2.1520f,
                                 -0.2451f, -0.7560f, -1.3440f, -2.1520f};
 
-// 0xFFFFFFFF if a >= b (ordered: false on NaN), else 0
-__device__ __forceinline__ uint32_t set_ge(float a, float b) {
-  uint32_t d;
-  asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(d) : "f"(a), "f"(b));
-  return d;
-}
-// 0xFFFFFFFF if a < b (ordered), else 0
-__device__ __forceinline__ uint32_t set_lt(float a, float b) {
-  uint32_t d;
-  asm("set.lt.u32.f32 %0, %1, %2;" : "=r"(d) : "f"(a), "f"(b));
-  return d;
-}
-
 constexpr int kE = 8;  // elements of a (c, t) chunk
 
 // Unnormalised WHT of a group held by four lanes (v[c][e] = element 32 c + 8 t + e).
@@ -164,15 +151,22 @@ __global__ void __launch_bounds__(256) kv3_encode_kernel(const Kv3Params p) {
     for (int c = 0; c < 4; ++c) {
       uint32_t bits = 0;
 #pragma unroll
-      for (int e = 0; e < kE; ++e) {
-        // each true compare gives -1, so the sum is minus the code 4 neg + m (m the thresholds
-        // passed, neg the sign; -0 counts as positive); subtracted at bit 3 e
+      for (int e = kE - 1; e >= 0; --e) {
+        // the three bits of the code from sign bits, each shifted in at the bottom (element
+        // 7 first): the sign of v + 0 (v < 0; -0 + 0 is +0), the sign of a - t1 (a < t1),
+        // and the parity of the signs of a - t0, a - t1, a - t2 (the thresholds not passed;
+        // a - t is +0 when they are equal, so a >= t is a clear sign bit).  m counts the
+        // thresholds passed, so its bits are the complements of the last two: inverted below.
         const float a = fabsf(v[c][e]);
-        const uint32_t minus_code =
-            set_ge(a, t0) + set_ge(a, t1) + set_ge(a, t2) + 4u * set_lt(v[c][e], 0.0f);
-        bits -= minus_code << (3 * e);
+        const uint32_t sg = __float_as_uint(__fadd_rn(v[c][e], 0.0f));
+        const uint32_t d0 = __float_as_uint(__fsub_rn(a, t0));
+        const uint32_t d1 = __float_as_uint(__fsub_rn(a, t1));
+        const uint32_t d2 = __float_as_uint(__fsub_rn(a, t2));
+        bits = __funnelshift_l(sg, bits, 1);
+        bits = __funnelshift_l(d1, bits, 1);
+        bits = __funnelshift_l(d0 ^ d1 ^ d2, bits, 1);
       }
-      chunk[c] = s == 0.0f ? 0u : bits;
+      chunk[c] = s == 0.0f ? 0u : bits ^ 0x6DB6DBu;  // bits 3 e and 3 e + 1 of each code
     }
     // stream bits 96 c + 24 t: lane t < 3 forms word 3 c + t from its chunk and lane t + 1's
     const int next = (lane & ~3) | ((t + 1) & 3);
