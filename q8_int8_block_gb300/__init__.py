@@ -132,6 +132,11 @@ def _need(t, dtype, shape, name):
         raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name}: must be a contiguous CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on the current device: a pointer into another GPU's memory
+        # must not reach its kernels
+        raise ValueError(f"{name}: on {t.device}, but the current device is "
+                         f"cuda:{torch.cuda.current_device()} (use torch.cuda.device)")
 
 
 def q8_quantize_weights(W, Wq=None, Wd=None, stream=None):
@@ -318,8 +323,9 @@ def q8_bsa_attention(q, k, v, row_ptr, col_idx, out_dtype=torch.float32, o=None,
     for t, name in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, torch.bfloat16, (H if name == "q" else Hkv, T, d), name)
     _need(row_ptr, torch.int32, (H * (T // 64) + 1,), "row_ptr")
-    if col_idx.dtype != torch.int32 or col_idx.dim() != 1 or not col_idx.is_cuda:
+    if col_idx.dim() != 1:
         raise ValueError("col_idx: a 1-D int32 CUDA tensor")
+    _need(col_idx, torch.int32, (col_idx.numel(),), "col_idx")
     if out_dtype not in DTYPES:
         raise TypeError(f"out_dtype: expected bfloat16 or float32, got {out_dtype}")
     if o is None:
@@ -340,8 +346,9 @@ def q8_kv3_encode(x, codes=None, scales=None, stream=None):
     group per 128 consecutive elements.  Reinterpret codes with .view(torch.int32) as needed."""
     if x.dtype not in DTYPES:
         raise TypeError(f"x: expected bfloat16 or float32, got {x.dtype}")
-    if not x.is_cuda or not x.is_contiguous() or x.numel() % KV3_GROUP:
+    if x.numel() % KV3_GROUP:
         raise ValueError("x: a contiguous CUDA tensor of whole 128-element groups")
+    _need(x, x.dtype, tuple(x.shape), "x")
     n = x.numel() // KV3_GROUP
     if codes is None:
         codes = torch.empty((n, 12), dtype=torch.int32, device=x.device)

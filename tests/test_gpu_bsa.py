@@ -98,6 +98,20 @@ def test_empty_rows_and_bad_blocks(q8):
     assert q8.q8_device_error() == 0
 
 
+def test_binding_refuses_strided_block_lists(q8):
+    """A strided int32 view of the block list would hand the kernel the wrong words: the
+    binding refuses it before anything launches."""
+    rng = np.random.default_rng(9)
+    q, k, v = workloads.bsa_qkv(rng, 2, 2, 128)
+    rp, ci = workloads.dense_causal_mask(2, 128)
+    strided = T(np.repeat(ci, 2))[::2]
+    assert torch.equal(strided.cpu(), torch.from_numpy(ci)) and not strided.is_contiguous()
+    with pytest.raises(ValueError, match="col_idx"):
+        q8.q8_bsa_attention(T(q), T(k), T(v), T(rp), strided)
+    o = q8.q8_bsa_attention(T(q), T(k), T(v), T(rp), strided.contiguous())
+    _close(o.cpu().numpy(), OB.attention(q, k, v, rp, ci), "contiguous copy")
+
+
 def test_full_size_32k(q8):
     """32 query heads over 8 key/value heads, 32768 tokens, ~10 % of the causal blocks:
     sampled queries (the first and last of the sequence included) against the oracle."""
