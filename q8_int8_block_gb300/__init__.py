@@ -125,6 +125,13 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _key(table, key, name):
+    """table[key], or a ValueError naming the accepted keys."""
+    if key not in table:
+        raise ValueError(f"{name}: expected one of {sorted(table)}, got {key!r}")
+    return table[key]
+
+
 def _need(t, dtype, shape, name):
     if t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
@@ -216,7 +223,7 @@ def q8_linear(x, Wq, Wd, y=None, stream=None):
 
 
 def q8_linear_workspace_size(M, N, K, path="auto") -> int:
-    return int(_L.q8_linear_workspace_size(M, N, K, PATHS[path]))
+    return int(_L.q8_linear_workspace_size(M, N, K, _key(PATHS, path, "path")))
 
 
 def q8_linear_ex(x, Wq, Wd, y=None, path="auto", workspace=None, stream=None):
@@ -225,6 +232,7 @@ def q8_linear_ex(x, Wq, Wd, y=None, path="auto", workspace=None, stream=None):
     (then one is allocated here with torch)."""
     if x.dtype not in DTYPES:
         raise TypeError(f"x: expected bfloat16 or float32, got {x.dtype}")
+    path_id = _key(PATHS, path, "path")
     _need(x, x.dtype, tuple(x.shape), "x")
     M, N, K, y = _lin_check(x, Wq, Wd, y)
     need = q8_linear_workspace_size(M, N, K, path)
@@ -232,7 +240,7 @@ def q8_linear_ex(x, Wq, Wd, y=None, path="auto", workspace=None, stream=None):
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_L.q8_linear_ex(_ptr(x), DTYPES[x.dtype], _ptr(Wq), _ptr(Wd), _ptr(y), M, N, K,
-                           PATHS[path], _ptr(workspace), nbytes, _stream(stream)), "q8_linear_ex")
+                           path_id, _ptr(workspace), nbytes, _stream(stream)), "q8_linear_ex")
     return y
 
 
@@ -247,6 +255,9 @@ def q8_linear_fused(x, Wq, Wd, epi="none", aux=None, y=None, out_dtype=torch.flo
         raise TypeError(f"x: expected bfloat16 or float32, got {x.dtype}")
     if out_dtype not in DTYPES:
         raise TypeError(f"out_dtype: expected bfloat16 or float32, got {out_dtype}")
+    epi_id, path_id = _key(EPILOGUES, epi, "epi"), _key(PATHS, path, "path")
+    if epi_id != 0 and aux is None:
+        raise ValueError(f"epi {epi!r} needs aux")
     _need(x, x.dtype, tuple(x.shape), "x")
     M, K = x.shape
     N = Wq.shape[0]
@@ -255,16 +266,14 @@ def q8_linear_fused(x, Wq, Wd, epi="none", aux=None, y=None, out_dtype=torch.flo
     if y is None:
         y = torch.empty((M, N), dtype=out_dtype, device=x.device)
     _need(y, out_dtype, (M, N), "y")
-    if EPILOGUES[epi] != 0:
-        if aux is None:
-            raise ValueError(f"epi {epi!r} needs aux")
+    if epi_id != 0:
         _need(aux, torch.float32, (M, N), "aux")
     if norm_weight is not None:
         _need(norm_weight, torch.float32, (K,), "norm_weight")
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_L.q8_linear_fused(_ptr(x), DTYPES[x.dtype], _ptr(norm_weight), float(norm_eps),
-                              _ptr(Wq), _ptr(Wd), EPILOGUES[epi],
-                              _ptr(aux), _ptr(y), DTYPES[out_dtype], M, N, K, PATHS[path],
+                              _ptr(Wq), _ptr(Wd), epi_id,
+                              _ptr(aux), _ptr(y), DTYPES[out_dtype], M, N, K, path_id,
                               _ptr(workspace), nbytes, _stream(stream)), "q8_linear_fused")
     return y
 
@@ -292,6 +301,9 @@ def q8_linear_prepared(x, B16, Wd, epi="none", aux=None, y=None, out_dtype=torch
         raise TypeError(f"x: expected bfloat16 or float32, got {x.dtype}")
     if out_dtype not in DTYPES:
         raise TypeError(f"out_dtype: expected bfloat16 or float32, got {out_dtype}")
+    epi_id = _key(EPILOGUES, epi, "epi")
+    if epi_id != 0 and aux is None:
+        raise ValueError(f"epi {epi!r} needs aux")
     _need(x, x.dtype, tuple(x.shape), "x")
     M, K = x.shape
     N = B16.shape[0]
@@ -300,15 +312,13 @@ def q8_linear_prepared(x, B16, Wd, epi="none", aux=None, y=None, out_dtype=torch
     if y is None:
         y = torch.empty((M, N), dtype=out_dtype, device=x.device)
     _need(y, out_dtype, (M, N), "y")
-    if EPILOGUES[epi] != 0:
-        if aux is None:
-            raise ValueError(f"epi {epi!r} needs aux")
+    if epi_id != 0:
         _need(aux, torch.float32, (M, N), "aux")
     if norm_weight is not None:
         _need(norm_weight, torch.float32, (K,), "norm_weight")
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_L.q8_linear_prepared(_ptr(x), DTYPES[x.dtype], _ptr(norm_weight), float(norm_eps),
-                                 _ptr(B16), _ptr(Wd), EPILOGUES[epi], _ptr(aux), _ptr(y),
+                                 _ptr(B16), _ptr(Wd), epi_id, _ptr(aux), _ptr(y),
                                  DTYPES[out_dtype], M, N, K, _ptr(workspace), nbytes,
                                  _stream(stream)), "q8_linear_prepared")
     return y
@@ -397,6 +407,7 @@ def q8_linear_noalloc(x, Wq, Wd, y=None, stream=None):
 
 def q8_block_sums(xq, Wq, isum=None, path="auto", stream=None):
     """Exact int32 block sums isum [M,N,K/32] of int8 codes, by the kernel of `path`."""
+    path_id = _key(PATHS, path, "path")
     M, K = xq.shape
     N = Wq.shape[0]
     _need(xq, torch.int8, (M, K), "xq")
@@ -404,7 +415,7 @@ def q8_block_sums(xq, Wq, isum=None, path="auto", stream=None):
     if isum is None:
         isum = torch.empty((M, N, K // QK), dtype=torch.int32, device=xq.device)
     _need(isum, torch.int32, (M, N, K // QK), "isum")
-    _check(_L.q8_block_sums(_ptr(xq), _ptr(Wq), _ptr(isum), M, N, K, PATHS[path], _stream(stream)),
+    _check(_L.q8_block_sums(_ptr(xq), _ptr(Wq), _ptr(isum), M, N, K, path_id, _stream(stream)),
            "q8_block_sums")
     return isum
 
