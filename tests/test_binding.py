@@ -70,3 +70,33 @@ def test_host_tensors_never_reach_the_library(q8):
         q8.q8_bsa_attention(*(_cpu((2, 64, 128), torch.bfloat16) for _ in range(3)),
                             _cpu((3,), torch.int32), _cpu((2,), torch.int32))
 
+
+
+def test_keywords_reach_the_abi_as_their_enum_values(q8, monkeypatch):
+    """With the library replaced by a recorder (and the device checks off), every keyword
+    arrives at its C ABI argument as the value include/q8.h gives it."""
+    calls = {}
+
+    class Recorder:
+        def __getattr__(self, name):
+            def f(*args):
+                calls[name] = args
+                return 0
+            return f
+    monkeypatch.setattr(q8, "_L", Recorder())
+    monkeypatch.setattr(q8, "_need", lambda t, dtype, shape, name: None)
+    monkeypatch.setattr(q8, "_stream", lambda s: None)
+    monkeypatch.setattr(q8, "_ptr", lambda t: None if t is None else 1)
+    x = _cpu((2, 64), torch.bfloat16)
+    Wq, Wd, aux = _cpu((4, 64), torch.int8), _cpu((4, 2), torch.int16), _cpu((2, 4), torch.float32)
+    q8.q8_linear_fused(x, Wq, Wd, epi="silu_mul", aux=aux, path="tensor", out_dtype=torch.bfloat16)
+    a = calls["q8_linear_fused"]
+    assert (a[1], a[6], a[9], a[13]) == (1, 2, 1, 2)   # xtype bf16, SILU_MUL, ytype bf16, TENSOR
+    q8.q8_linear_prepared(x, _cpu((4, 64), torch.int16), Wd, epi="add", aux=aux)
+    assert calls["q8_linear_prepared"][6] == 1          # Q8_EPI_ADD
+    q8.q8_linear_ex(x.float(), Wq, Wd, path="batch")
+    assert calls["q8_linear_ex"][1] == 0 and calls["q8_linear_ex"][8] == 3   # f32 x, Q8_PATH_BATCH
+    q8.q8_block_sums(_cpu((2, 64), torch.int8), Wq, path="dp4a")
+    assert calls["q8_block_sums"][6] == 4               # Q8_PATH_DP4A
+    q8.q8_linear_workspace_size(2, 4, 64, "decode")
+    assert calls["q8_linear_workspace_size"] == (2, 4, 64, 1)
