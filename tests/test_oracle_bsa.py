@@ -8,7 +8,10 @@ from the oracle itself.
   grouped-query head mapping;
 - a two-key closed form fixes the softmax and its 1/sqrt(d) scale;
 - a sharp softmax (queries scaled by 64) returns the value row of the best visible key;
-- masked blocks and future tokens are invisible; heads sharing a key/value head agree.
+- masked blocks and future tokens are invisible; heads sharing a key/value head agree;
+- against a library routine: PyTorch's scaled_dot_product_attention in binary64 on the
+  CPU, plain causal for the dense mask and with the block-and-causal visibility written out
+  as an explicit boolean mask for a sparse one.
 """
 import math
 
@@ -138,3 +141,48 @@ def test_heads_sharing_a_kv_head_agree():
     o = bsa.attention(q, k, v, rp1, ci1)
     assert np.array_equal(o[0], o[1])
     assert not np.array_equal(o[0], o[2])
+
+
+def _visibility(row_ptr, col_idx, H, T):
+    """[H, T, T] booleans: query t of head h sees key j (listed block, j <= t)."""
+    nb = T // B
+    m = np.zeros((H, T, T), bool)
+    for h in range(H):
+        for qb in range(nb):
+            for kb in col_idx[row_ptr[h * nb + qb]:row_ptr[h * nb + qb + 1]]:
+                m[h, qb * B:(qb + 1) * B, kb * B:(kb + 1) * B] = True
+    return m & np.tril(np.ones((T, T), bool))
+
+
+def _sdpa(q, k, v, mask=None):
+    """torch's scaled_dot_product_attention in binary64 on the CPU (scale 1/sqrt(d)), each
+    key/value head repeated for the query heads that share it."""
+    torch = pytest.importorskip("torch")
+    g = q.shape[0] // k.shape[0]
+    tq = torch.from_numpy(_f(q))
+    tk = torch.from_numpy(_f(k)).repeat_interleave(g, 0)
+    tv = torch.from_numpy(_f(v)).repeat_interleave(g, 0)
+    if mask is None:
+        o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True)
+    else:
+        o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=torch.from_numpy(mask))
+    return o.numpy()
+
+
+def _agree(o, ref):
+    # the oracle rounds a binary64 result once to binary32
+    assert np.allclose(o, ref, rtol=2.0 ** -23, atol=1e-12 * np.max(np.abs(ref)))
+
+
+def test_dense_causal_mask_is_library_causal_attention():
+    q, k, v, _, _ = _case(10, H=4, Hkv=2, T=192)
+    rp, ci = workloads.dense_causal_mask(4, 192)
+    _agree(bsa.attention(q, k, v, rp, ci), _sdpa(q, k, v))
+
+
+def test_block_sparse_is_library_attention_under_the_block_mask():
+    q, k, v, rp, ci = _case(11, H=4, Hkv=2, T=512, density=0.3)
+    mask = _visibility(rp, ci, 4, 512)
+    assert mask.any(axis=2).all()          # every query sees itself: no empty softmax
+    assert all(not np.array_equal(mask[0], mask[h]) for h in range(1, 4))   # per-head lists
+    _agree(bsa.attention(q, k, v, rp, ci), _sdpa(q, k, v, mask))

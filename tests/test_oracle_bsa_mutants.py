@@ -25,6 +25,8 @@ PINS = [
     P.test_sharp_softmax_picks_the_best_key,
     P.test_masked_blocks_and_future_tokens_are_invisible,
     P.test_heads_sharing_a_kv_head_agree,
+    P.test_dense_causal_mask_is_library_causal_attention,
+    P.test_block_sparse_is_library_attention_under_the_block_mask,
 ]
 
 MUTANTS = [
