@@ -591,8 +591,12 @@ def gpu_arm(args):
                    "kernel_path": r["path"], "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {r['copies']} rotating weight copies "
                          f"({r['copies'] * r['wbytes'] / 1e6:.0f} MB > 2 x L2)",
-                   "timing": "CUDA graph replays, CUDA events; main kernel timed by event nodes "
-                             "around each launch"},
+                   "timing": "CUDA graph replays timed by CUDA events; " +
+                             ("the GEMM kernel timed by event nodes around each launch"
+                              if r["path"] in ("tensor", "dp4a") else
+                              "kernel time = the timed region's time per step (the streaming "
+                              "kernel, chained to its neighbours by programmatic dependent "
+                              "launch; event nodes would serialize the overlapping launches)")},
         "roofline": r["roofline"],
         "clocks": r["clocks"],
         "e2e": r["e2e"],
