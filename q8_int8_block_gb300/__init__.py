@@ -139,11 +139,23 @@ def _need(t, dtype, shape, name):
         raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name}: must be a contiguous CUDA tensor")
-    if t.device.index != torch.cuda.current_device():
-        # the library launches on the current device: a pointer into another GPU's memory
-        # must not reach its kernels
-        raise ValueError(f"{name}: on {t.device}, but the current device is "
-                         f"cuda:{torch.cuda.current_device()} (use torch.cuda.device)")
+
+
+def _on_device(**tensors):
+    """Every tensor given (None skipped) is a contiguous CUDA tensor on the current device:
+    the library launches there, so a pointer into host memory or another GPU's memory must
+    not reach its kernels.  One device query per call."""
+    d = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name}: must be a contiguous CUDA tensor")
+        if d is None:
+            d = torch.cuda.current_device()
+        if t.get_device() != d:
+            raise ValueError(f"{name}: on {t.device}, but the current device is cuda:{d} "
+                             "(use torch.cuda.device)")
 
 
 def q8_quantize_weights(W, Wq=None, Wd=None, stream=None):
@@ -156,6 +168,7 @@ def q8_quantize_weights(W, Wq=None, Wd=None, stream=None):
         Wd = torch.empty((N, K // QK), dtype=torch.int16, device=W.device)
     _need(Wq, torch.int8, (N, K), "Wq")
     _need(Wd, torch.int16, (N, K // QK), "Wd")
+    _on_device(W=W, Wq=Wq, Wd=Wd)
     _check(_L.q8_quantize_weights(_ptr(W), _ptr(Wq), _ptr(Wd), N, K, _stream(stream)),
            "q8_quantize_weights")
     return Wq, Wd
@@ -173,6 +186,7 @@ def q8_quantize_act(x, xq=None, xd=None, stream=None):
         xd = torch.empty((M, K // QK), dtype=torch.float32, device=x.device)
     _need(xq, torch.int8, (M, K), "xq")
     _need(xd, torch.float32, (M, K // QK), "xd")
+    _on_device(x=x, xq=xq, xd=xd)
     _check(_L.q8_quantize_act(_ptr(x), DTYPES[x.dtype], _ptr(xq), _ptr(xd), M, K, _stream(stream)),
            "q8_quantize_act")
     return xq, xd
@@ -196,6 +210,7 @@ def q8_quantize_act_rmsnorm(x, gamma, eps, xq=None, xd=None, r=None, stream=None
     _need(xq, torch.int8, (M, K), "xq")
     _need(xd, torch.float32, (M, K // QK), "xd")
     _need(r, torch.float32, (M,), "r")
+    _on_device(x=x, gamma=gamma, xq=xq, xd=xd, r=r)
     _check(_L.q8_quantize_act_rmsnorm(_ptr(x), DTYPES[x.dtype], _ptr(gamma), float(eps), _ptr(xq),
                                       _ptr(xd), _ptr(r), M, K, _stream(stream)),
            "q8_quantize_act_rmsnorm")
@@ -217,6 +232,7 @@ def q8_linear(x, Wq, Wd, y=None, stream=None):
     """y float32 [M,N] = Q8_0 linear of bf16 x [M,K] (library-owned scratch)."""
     _need(x, torch.bfloat16, tuple(x.shape), "x")
     M, N, K, y = _lin_check(x, Wq, Wd, y)
+    _on_device(x=x, Wq=Wq, Wd=Wd, y=y)
     _check(_L.q8_linear(_ptr(x), _ptr(Wq), _ptr(Wd), _ptr(y), M, N, K, _stream(stream)),
            "q8_linear")
     return y
@@ -239,6 +255,7 @@ def q8_linear_ex(x, Wq, Wd, y=None, path="auto", workspace=None, stream=None):
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _on_device(x=x, Wq=Wq, Wd=Wd, y=y, workspace=workspace)
     _check(_L.q8_linear_ex(_ptr(x), DTYPES[x.dtype], _ptr(Wq), _ptr(Wd), _ptr(y), M, N, K,
                            path_id, _ptr(workspace), nbytes, _stream(stream)), "q8_linear_ex")
     return y
@@ -271,6 +288,7 @@ def q8_linear_fused(x, Wq, Wd, epi="none", aux=None, y=None, out_dtype=torch.flo
     if norm_weight is not None:
         _need(norm_weight, torch.float32, (K,), "norm_weight")
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _on_device(x=x, norm_weight=norm_weight, Wq=Wq, Wd=Wd, aux=aux, y=y, workspace=workspace)
     _check(_L.q8_linear_fused(_ptr(x), DTYPES[x.dtype], _ptr(norm_weight), float(norm_eps),
                               _ptr(Wq), _ptr(Wd), epi_id,
                               _ptr(aux), _ptr(y), DTYPES[out_dtype], M, N, K, path_id,
@@ -285,6 +303,7 @@ def q8_weights_to_f16(Wq, B16=None, stream=None):
     if B16 is None:
         B16 = torch.empty((N, K), dtype=torch.int16, device=Wq.device)
     _need(B16, torch.int16, (N, K), "B16")
+    _on_device(Wq=Wq, B16=B16)
     _check(_L.q8_weights_to_f16(_ptr(Wq), _ptr(B16), N, K, _stream(stream)), "q8_weights_to_f16")
     return B16
 
@@ -317,6 +336,7 @@ def q8_linear_prepared(x, B16, Wd, epi="none", aux=None, y=None, out_dtype=torch
     if norm_weight is not None:
         _need(norm_weight, torch.float32, (K,), "norm_weight")
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _on_device(x=x, norm_weight=norm_weight, B16=B16, Wd=Wd, aux=aux, y=y, workspace=workspace)
     _check(_L.q8_linear_prepared(_ptr(x), DTYPES[x.dtype], _ptr(norm_weight), float(norm_eps),
                                  _ptr(B16), _ptr(Wd), epi_id, _ptr(aux), _ptr(y),
                                  DTYPES[out_dtype], M, N, K, _ptr(workspace), nbytes,
@@ -341,6 +361,7 @@ def q8_bsa_attention(q, k, v, row_ptr, col_idx, out_dtype=torch.float32, o=None,
     if o is None:
         o = torch.empty((H, T, d), dtype=out_dtype, device=q.device)
     _need(o, out_dtype, (H, T, d), "o")
+    _on_device(q=q, k=k, v=v, row_ptr=row_ptr, col_idx=col_idx, o=o)
     _check(_L.q8_bsa_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(row_ptr), _ptr(col_idx),
                                col_idx.numel(), _ptr(o), DTYPES[out_dtype], H, Hkv, T, d,
                                _stream(stream)), "q8_bsa_attention")
@@ -366,6 +387,7 @@ def q8_kv3_encode(x, codes=None, scales=None, stream=None):
         scales = torch.empty((n,), dtype=torch.float32, device=x.device)
     _need(codes, torch.int32, (n, 12), "codes")
     _need(scales, torch.float32, (n,), "scales")
+    _on_device(x=x, codes=codes, scales=scales)
     _check(_L.q8_kv3_encode(_ptr(x), DTYPES[x.dtype], _ptr(codes), _ptr(scales), n, _stream(stream)),
            "q8_kv3_encode")
     return codes, scales
@@ -382,6 +404,7 @@ def q8_kv3_decode(codes, scales, out_dtype=torch.bfloat16, out=None, stream=None
     if out is None:
         out = torch.empty((n, KV3_GROUP), dtype=out_dtype, device=codes.device)
     _need(out, out_dtype, (n, KV3_GROUP), "out")
+    _on_device(codes=codes, scales=scales, out=out)
     _check(_L.q8_kv3_decode(_ptr(codes), _ptr(scales), _ptr(out), DTYPES[out_dtype], n,
                             _stream(stream)), "q8_kv3_decode")
     return out
@@ -400,6 +423,7 @@ def q8_linear_noalloc(x, Wq, Wd, y=None, stream=None):
         raise TypeError(f"x: expected bfloat16 or float32, got {x.dtype}")
     _need(x, x.dtype, tuple(x.shape), "x")
     M, N, K, y = _lin_check(x, Wq, Wd, y)
+    _on_device(x=x, Wq=Wq, Wd=Wd, y=y)
     _check(_L.q8_linear_noalloc(_ptr(x), DTYPES[x.dtype], _ptr(Wq), _ptr(Wd), _ptr(y), M, N, K,
                                 _stream(stream)), "q8_linear_noalloc")
     return y
@@ -415,6 +439,7 @@ def q8_block_sums(xq, Wq, isum=None, path="auto", stream=None):
     if isum is None:
         isum = torch.empty((M, N, K // QK), dtype=torch.int32, device=xq.device)
     _need(isum, torch.int32, (M, N, K // QK), "isum")
+    _on_device(xq=xq, Wq=Wq, isum=isum)
     _check(_L.q8_block_sums(_ptr(xq), _ptr(Wq), _ptr(isum), M, N, K, path_id, _stream(stream)),
            "q8_block_sums")
     return isum

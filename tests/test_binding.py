@@ -72,6 +72,16 @@ def test_host_tensors_never_reach_the_library(q8):
 
 
 
+def test_every_tensor_argument_is_checked_before_the_call(q8):
+    """The per-call check refuses host tensors and strided views, including a caller's
+    workspace (which no shape check covers), and skips absent optional tensors."""
+    q8._on_device(aux=None, norm_weight=None)
+    with pytest.raises(ValueError, match="workspace"):
+        q8._on_device(workspace=torch.zeros(1024, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="y"):
+        q8._on_device(y=torch.zeros((4, 8))[:, ::2])
+
+
 def test_keywords_reach_the_abi_as_their_enum_values(q8, monkeypatch):
     """With the library replaced by a recorder (and the device checks off), every keyword
     arrives at its C ABI argument as the value include/q8.h gives it."""
@@ -85,6 +95,7 @@ def test_keywords_reach_the_abi_as_their_enum_values(q8, monkeypatch):
             return f
     monkeypatch.setattr(q8, "_L", Recorder())
     monkeypatch.setattr(q8, "_need", lambda t, dtype, shape, name: None)
+    monkeypatch.setattr(q8, "_on_device", lambda **tensors: None)
     monkeypatch.setattr(q8, "_stream", lambda s: None)
     monkeypatch.setattr(q8, "_ptr", lambda t: None if t is None else 1)
     x = _cpu((2, 64), torch.bfloat16)
