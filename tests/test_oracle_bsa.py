@@ -186,3 +186,14 @@ def test_block_sparse_is_library_attention_under_the_block_mask():
     assert mask.any(axis=2).all()          # every query sees itself: no empty softmax
     assert all(not np.array_equal(mask[0], mask[h]) for h in range(1, 4))   # per-head lists
     _agree(bsa.attention(q, k, v, rp, ci), _sdpa(q, k, v, mask))
+
+
+def test_sampled_queries_equal_the_full_output():
+    """attention_at (the sampled form the full-size GPU test uses) returns, bit for bit, the
+    rows of the full output at the sampled (head, token) pairs."""
+    q, k, v, rp, ci = _case(12, H=4, Hkv=2, T=256, density=0.3)
+    o = bsa.attention(q, k, v, rp, ci)
+    rng = np.random.default_rng(12)
+    heads = rng.integers(0, 4, 40)
+    toks = rng.integers(0, 256, 40)
+    assert np.array_equal(bsa.attention_at(q, k, v, rp, ci, heads, toks), o[heads, toks])
