@@ -23,7 +23,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -97,7 +96,10 @@ def peaks():
     try:
         with open(path) as f:
             p = json.load(f)
-        return {k: float(p[k]) for k in FALLBACK}, "measured"
+        out = {k: float(p[k]) for k in FALLBACK}
+        if "sm_max_mhz" in p:
+            out["sm_max_mhz"] = float(p["sm_max_mhz"])
+        return out, "measured"
     except Exception:
         return dict(FALLBACK), "fallback"
 
@@ -168,19 +170,22 @@ def kernel_source_sha(files):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(summary_md, sources):
-    """DRAM bytes per launch recorded by an ncu capture, if that capture was taken on the
-    current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", summary_md)
+def recorded_traffic(name):
+    """DRAM bytes per launch from the committed ncu capture record of workload `name`
+    (profiles/traffic.json), if that capture was taken on the current kernel sources (else
+    None: the kernel has changed since the counters were taken)."""
     try:
-        txt = open(path).read()
-    except OSError:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)["records"][name]
+    except (OSError, KeyError, ValueError):
         return None
-    m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", txt)
-    m_b = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9.eE+]+)", txt)
-    if not m_sha or not m_b or m_sha.group(1) != kernel_source_sha(sources):
+    if rec.get("source_sha256_16") != kernel_source_sha(rec["sources"]):
         return None
-    return float(m_b.group(1))
+    return float(rec["dram_bytes_per_launch"])
+
+
+def sm_count(torch):
+    return int(torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count)
 
 
 # ----------------------------------------------------------------------------------- #
@@ -202,38 +207,46 @@ CASES = {
     "prefill27b_up": ("prefill27b", 0, 0), "prefill27b_down": ("prefill27b", 1, 0),
     "gate_m128": ("sweep", 4, 3), "gate_m512": ("sweep", 4, 4),
 }
-TRAFFIC_PROFILES = {  # committed ncu summaries that record DRAM bytes per launch
-    "decode_m1": ("decode_kernel_m1_k4096_n12288.md",
-                  ["q8_decode.cu", "q8_ptx.cuh", "q8_quant_dev.cuh", "q8_epi.cuh"]),
-    "prefill9b_up": ("gemm_tc_kernel_m2048_k4096_n12288.md", ["q8_gemm.cu", "q8_ptx.cuh", "q8_epi.cuh"]),
-    "decode_m16": ("batch_kernel_m16_k4096_n12288.md",
-                   ["q8_batch.cu", "q8_ptx.cuh", "q8_quant_dev.cuh", "q8_epi.cuh"]),
-    "kv3_encode_256k": ("kv3_encode_kernel_256k_layer.md", ["q8_kv3.cu"]),
-    "kv3_decode_256k": ("kv3_decode_kernel_256k_layer.md", ["q8_kv3.cu"]),
-    "bsa_32k": ("bsa_kernel_32k_prefill.md", ["q8_bsa.cu", "q8_ptx.cuh"]),
-}
+_WEIGHTS = {}
+
+
+def quantized_weights(torch, q8, dev, wname, p):
+    """Q8_0 weights (codes, binary16 scales) of projection p of a workload, quantized by the
+    library on the device; the most recent shapes are kept so that cases sharing a projection
+    draw and quantize it once."""
+    key = (wname, p)
+    if key not in _WEIGHTS:
+        if len(_WEIGHTS) >= 4:
+            _WEIGHTS.pop(next(iter(_WEIGHTS)))
+        W = workloads.WORKLOADS[wname].make_weights(p)
+        _WEIGHTS[key] = q8.q8_quantize_weights(torch.from_numpy(W).to(dev))
+        del W
+    return _WEIGHTS[key]
 
 
 def time_graph_steps(torch, q8, step_fns, steps, warmup, instrument=True):
-    """Captures one CUDA graph holding whole rotations of step_fns, runs `warmup` steps, then times
-    exactly `steps` steps: whole replays plus a replay of a graph holding the remainder.
-    Returns (seconds for the timed steps, mean seconds of the main kernel), all from CUDA
-    events on the launching stream.  With `instrument`, the library records event nodes
-    around each step's main kernel and the mean is over the last len(step_fns) launches;
-    without it (one kernel per step, consecutive launches overlapping through programmatic
-    dependent launch, which event nodes between them would serialize), the main kernel's
-    time per launch is the timed region's time per step."""
-    # one graph holds a whole number of rotations and at least 48 steps, so the chain of
-    # overlapping launches breaks only at replay boundaries, rarely
-    reps = max(1, -(-min(48, steps) // len(step_fns)))
-    step_fns = list(step_fns) * reps
-    R = len(step_fns)
+    """Runs `warmup` untimed steps, then times exactly `steps` steps, all as replays of CUDA
+    graphs that rotate over step_fns (one step per weight copy).  Up to 48 steps the timed
+    region is one replay of a graph holding exactly `steps` steps; longer runs replay a graph
+    of whole rotations (at least 48 steps) and then one holding the remainder.  Every graph
+    the timed region replays has been replayed during the warm-up (a graph's first launch
+    also uploads it).  Returns (seconds for the timed steps, mean seconds of the main kernel),
+    all from CUDA events on the launching stream.  With `instrument`, the library records
+    event nodes around each step's main kernel and the mean is over the launches of one
+    graph; without it (one kernel per step, consecutive launches overlapping through
+    programmatic dependent launch, which event nodes between them would serialize), the main
+    kernel's time per launch is the timed region's time per step."""
+    if steps <= 48:
+        R = steps
+    else:
+        R = len(step_fns) * max(1, -(-48 // len(step_fns)))
+    fns = [step_fns[i % len(step_fns)] for i in range(R)]
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(R)]
     stops = [torch.cuda.Event(enable_timing=True) for _ in range(R)]
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        for f in step_fns[:len(step_fns) // reps]:  # eager once (attributes, workspace)
+        for f in step_fns:  # eager once (attributes, workspace)
             f()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
@@ -242,7 +255,7 @@ def time_graph_steps(torch, q8, step_fns, steps, warmup, instrument=True):
     try:
         full = torch.cuda.CUDAGraph()
         with torch.cuda.graph(full):
-            for f in step_fns:
+            for f in fns:
                 f()
         rem = steps % R
         part = None
@@ -251,12 +264,14 @@ def time_graph_steps(torch, q8, step_fns, steps, warmup, instrument=True):
                 q8.q8_set_timing_events(starts, stops)
             part = torch.cuda.CUDAGraph()
             with torch.cuda.graph(part):
-                for f in step_fns[:rem]:
+                for f in fns[:rem]:
                     f()
     finally:
         q8.q8_set_timing_events()
-    for _ in range((warmup + R - 1) // R):
+    for _ in range(max(1, -(-warmup // R))):
         full.replay()
+    if part is not None:
+        part.replay()
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
@@ -272,7 +287,8 @@ def time_graph_steps(torch, q8, step_fns, steps, warmup, instrument=True):
     barrier()
     total = ev0.elapsed_time(ev1) / 1e3
     if instrument:
-        kern = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, stops)) / 1e3
+        n = rem if part is not None else R
+        kern = statistics.mean(a.elapsed_time(b) for a, b in zip(starts[:n], stops[:n])) / 1e3
     else:
         kern = total / steps
     return total, kern
@@ -287,12 +303,10 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
     prepared: the tensor-core path on weights widened once (q8_linear_prepared)."""
     wname, p, mi = spec if spec is not None else CASES[name]
     wl = workloads.WORKLOADS[wname]
-    W = wl.make_weights(p)
+    Wq0, Wd0 = quantized_weights(torch, q8, dev, wname, p)
     x_np, _ = wl.make_act(p, mi)
     M, K = x_np.shape
-    N = W.shape[0]
-    Wq0, Wd0 = q8.q8_quantize_weights(torch.from_numpy(W).to(dev))
-    del W
+    N = Wq0.shape[0]
     wbytes = N * K + 2 * N * (K // 32)
     copies = max(2, -(-(2 * l2_bytes(torch)) // wbytes))
     Wqs = [Wq0] + [Wq0.clone() for _ in range(copies - 1)]
@@ -375,13 +389,14 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
     if path == "dp4a":
         # CUDA-core integer path: peak from unit counts, 64 dp4a per clock per SM (measured),
         # 4 int8 MACs each, at the maximum SM clock
-        dp4a_peak = 64 * 4 * 2 * 152 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        sms = sm_count(torch)
+        dp4a_peak = 64 * 4 * 2 * sms * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         roof = {"bound": "alu", "achieved": round(ops_step / kern / 1e12, 2),
                 "peak": round(dp4a_peak, 1), "unit": "TOPS",
                 "frac": round(ops_step / kern / 1e12 / dp4a_peak, 4),
                 "algorithmic_flops_per_launch": ops_step,
-                "peak_source": "dp4a: 64 per clock per SM (microbenchmark) x 4 MACs x 2 ops x "
-                               "152 SMs x maximum SM clock"}
+                "peak_source": f"dp4a: 64 per clock per SM (microbenchmark) x 4 MACs x 2 ops x "
+                               f"{sms} SMs x maximum SM clock"}
     roof["kernel"] = {"decode": "q8::decode_kernel", "batch": "q8::batch_kernel",
                       "dp4a": "q8::dp4a_gemm_kernel"}.get(path, "q8::gemm_tc_kernel")
     roof["kernel_us"] = round(kern * 1e6, 3)
@@ -392,9 +407,10 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
                            "kernel, chained by programmatic dependent launch)"
                            if path == "batch" else "mean of event-node pairs around the GEMM launches")
     # the committed captures are of the library's own choice of kernel on the plain layer
-    prof = TRAFFIC_PROFILES.get(name) if force_path is None and gated is None and not prepared else None
-    roof["traffic"] = profiled_traffic(*prof) if prof else None
+    roof["traffic"] = (recorded_traffic(name) if force_path is None and gated is None and not prepared
+                       else None)
     out = {"name": name, "M": M, "K": K, "N": N, "path": path, "unit": unit, "value": value,
+           "steps": steps,
            "t_max": t_max, "roofline": roof, "copies": copies, "wbytes": wbytes,
            "launches_per_step": {"decode": 1, "batch": 2, "dp4a": 2}.get(path, 3), "clocks": clk_summary,
            "bytes_step": bytes_step, "xsize": xsize, "bf16": wl.bf16}
@@ -429,7 +445,7 @@ def run_kv3(torch, q8, dev, steps, warmup, pk, pk_src):
                                   "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
                                   "peak_source": f"hbm_gbs of the {pk_src} peaks",
                                   "kernel": "q8::kv3_" + name.split("_")[1] + "_kernel",
-                                  "traffic": profiled_traffic(*TRAFFIC_PROFILES[name])},
+                                  "traffic": recorded_traffic(name)},
                      "steps": steps}
     return res
 
@@ -455,7 +471,7 @@ def run_bsa(torch, q8, dev, steps, warmup, pk, pk_src):
     fn()
     total, kern = time_graph_steps(torch, q8, [fn], steps, warmup, instrument=False)
     tf = flops / kern / 1e12
-    mma_sync_peak = 1024 * 2 * 152 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    mma_sync_peak = 1024 * 2 * sm_count(torch) * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
     return {"bsa_32k": {"value": round(tf, 2), "unit": "TFLOP/s", "us_per_step": round(kern * 1e6, 2),
                         "algorithmic_flops_per_launch": flops, "visible_pairs": pairs,
                         "block_density": round(len(ci) / (cfg["H"] * nb * (nb + 1) / 2), 4),
@@ -465,7 +481,7 @@ def run_bsa(torch, q8, dev, steps, warmup, pk, pk_src):
                                      "peak_source": f"bf16_tflops (burst) of the {pk_src} peaks",
                                      "mma_sync_ceiling_tflops": round(mma_sync_peak, 1),
                                      "kernel": "q8::bsa_kernel",
-                                     "traffic": profiled_traffic(*TRAFFIC_PROFILES["bsa_32k"])},
+                                     "traffic": recorded_traffic("bsa_32k")},
                         "steps": steps,
                         "note": ("block-sparse causal attention (MInference-style), mma.sync "
                                  "bf16 tensor cores, FlashAttention-2 online softmax")}}
@@ -518,6 +534,82 @@ def e2e_measure(torch, q8, dev, x_np, bf16, Wqs, Wds, M, N, K, steps, warmup, by
             "api": "q8_int8_block_gb300.q8_linear (C ABI q8_linear), host-timed"}
 
 
+def int8_library_reference(torch, dev, M=2048, K=4096, N=12288, steps=20):
+    """Speed reference only (not this library's path): the int8 x int8 -> int32 GEMM of
+    PyTorch's torch._int_mm (a vendor-library int8 GEMM) on the 9B up-projection shape, in
+    int8 TOPS.  It tells what the GPU's int8 GEMM route delivers; None if unavailable."""
+    try:
+        g = torch.Generator(device=dev)
+        g.manual_seed(5)
+        a = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev, generator=g)
+        b = torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev, generator=g).t()
+        for _ in range(3):
+            torch._int_mm(a, b)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            torch._int_mm(a, b)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / steps
+        return {"tops": round(2 * M * N * K / t / 1e12, 1), "us": round(t * 1e6, 1),
+                "shape": f"M={M} K={K} N={N}", "what": "torch._int_mm (library int8 GEMM), "
+                "speed reference only"}
+    except Exception as e:  # noqa: BLE001
+        return {"unavailable": f"{type(e).__name__}: {str(e)[:80]}"}
+
+
+# The configurations measured in every default run, after the headline: (case name, steps).
+CONFIG_CASES = (("tiny", 20000), ("decode_m4", 20000), ("decode_m16", 20000), ("decode_m64", 20000),
+                ("prefill9b_up", 200), ("prefill9b_down", 200), ("prefill27b_up", 20),
+                ("prefill27b_down", 20))
+
+
+def compact(e):
+    """[value of the whole call, unit, roofline frac of the main kernel, us per call, us of the
+    main kernel, path]"""
+    return [round(e["value"], 2 if e["value"] < 1000 else 1), e["unit"], e["roofline"]["frac"],
+            round(e["t_max"] / e["steps"] * 1e6, 2), e["roofline"]["kernel_us"], e["path"]]
+
+
+def sweep_points(torch, q8, dev, pk, pk_src, budget_s=1.0):
+    """Every (projection shape, M) point of the dense-layer sweep workload, timed like the
+    headline (graph replays, rotating weight copies > 2 x L2), with the whole call's fraction
+    of max(bytes / HBM peak, ops / tensor peak)."""
+    wl = workloads.WORKLOADS["sweep"]
+    points, seen = [], set()
+    for p, proj in enumerate(wl.projections):
+        if (proj.K, proj.N) in seen:  # q, k, v, o share one shape; so do gate and up
+            continue
+        seen.add((proj.K, proj.N))
+        for mi, M in enumerate(wl.Ms):
+            ops = workloads.algorithmic_ops(M, proj.N, proj.K)
+            b = workloads.algorithmic_bytes(M, proj.N, proj.K, x_bytes=2)
+            t_roof = max(b / (pk["hbm_gbs"] * 1e9), ops / (pk["bf16_tflops"] * 1e12))
+            steps = int(max(20, min(2000, budget_s / max(t_roof * 4, 1e-9))))
+            r = run_case(torch, q8, dev, f"sweep_{proj.name}_m{M}", steps, max(3, steps // 20), pk,
+                         pk_src, spec=("sweep", p, mi))
+            t = r["t_max"] / steps
+            points.append({"projection": proj.name, "K": proj.K, "N": proj.N, "M": M,
+                           "path": r["path"], "us_per_call": round(t * 1e6, 3),
+                           "GBps": round(b / t / 1e9, 1), "TOPS": round(ops / t / 1e12, 2),
+                           "bound": "hbm" if b / (pk["hbm_gbs"] * 1e9) >= ops / (pk["bf16_tflops"] * 1e12)
+                           else "tensor",
+                           "roofline_frac": round(t_roof / t, 4),
+                           "kernel_frac": r["roofline"]["frac"]})
+    return points
+
+
+def sweep_compact(points):
+    """{"M": [...], "<proj> KxN": [whole-call roofline fraction per M]}"""
+    out = {"M": sorted({pt["M"] for pt in points})}
+    for pt in points:
+        key = f"{pt['projection']} {pt['K']}>{pt['N']}"
+        out.setdefault(key, []).append(pt["roofline_frac"])
+    return out
+
+
 def gpu_arm(args):
     import torch
     rank, world, local = dist_env()
@@ -531,11 +623,9 @@ def gpu_arm(args):
     dev = torch.device("cuda", local)
     r = run_case(torch, q8, dev, args.workload, args.steps, args.warmup, pk, pk_src, clocks=True,
                  e2e=True, force_path=None if args.path == "auto" else args.path)
-    extra = {}
+    extra, configs = {}, {}
     if not args.no_extra and args.workload == "decode_m1":
-        for name, st, fp in (("decode_m4", 20000, None), ("decode_m16", 20000, None),
-                             ("decode_m64", 20000, None), ("prefill9b_up", 200, None),
-                             ("prefill9b_down", 200, None), ("prefill9b_up", 50, "dp4a"),
+        for name, st, fp in (("prefill9b_up", 50, "dp4a"),
                              ("decode_m1", 20000, "gated_fused"), ("decode_m1", 20000, "gated_unfused"),
                              ("prefill9b_up", 200, "gated_fused"), ("prefill9b_up", 200, "gated_unfused"),
                              ("decode_m1", 20000, "norm_gated_fused"),
@@ -576,6 +666,19 @@ def gpu_arm(args):
         for k in ("kv3_encode_256k", "kv3_decode_256k"):
             extra[k]["note"] = ("3-bit KV-cache codec (Walsh-Hadamard rotation + Lloyd-Max), "
                                 "one attention layer's keys at a 256K-token context")
+        # every configured workload, compact: the prefill half of the metric with the rest
+        configs["legend"] = ("[value of the whole call, unit, roofline frac of the main kernel, "
+                             "us per call, us of the main kernel, path]; peaks: hbm "
+                             f"{pk['hbm_gbs']} GB/s, tensor {pk['bf16_tflops']} TFLOP/s ({pk_src})")
+        configs["decode_m1"] = compact(dict(r, steps=args.steps))
+        for name, st in CONFIG_CASES:
+            e = run_case(torch, q8, dev, name, st, max(3, st // 50), pk, pk_src)
+            configs[name] = compact(dict(e, steps=st))
+            extra.setdefault("configs_roofline", {})[name] = e["roofline"]
+        pts = sweep_points(torch, q8, dev, pk, pk_src)
+        extra["sweep_points"] = pts
+        configs["sweep_call_frac"] = sweep_compact(pts)
+        configs["int8_library_ref"] = int8_library_reference(torch, dev)
     err = q8.q8_device_error()
     desc = workload_desc(args.workload)
     line = {
@@ -608,6 +711,8 @@ def gpu_arm(args):
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(r["Wq0"], r["Wd0"], r["x_np"], r["bf16"], r["M"], r["N"],
                                             r["K"], r["xsize"], args.cpu_seconds)
+    if configs:
+        line["configs"] = configs  # last: the end of the line holds every config's summary
     return rank, line
 
 
@@ -738,41 +843,21 @@ def parse_args(argv=None):
 
 def sweep_arm(args):
     """Every (projection, M) point of the dense-layer sweep workload, each timed like the
-    headline workload (graph replays, rotating weight copies > 2 x L2), with its roofline
-    fraction against max(bytes / HBM, ops / tensor peak).  One JSON line with all points."""
+    headline workload, with its roofline fraction against max(bytes / HBM, ops / tensor
+    peak).  One JSON line with all points."""
     import torch
     torch.cuda.set_device(0)
     import __graft_entry__ as g
     g.build()
     import q8_int8_block_gb300 as q8
     pk, pk_src = peaks()
-    dev = torch.device("cuda", 0)
-    wl = workloads.WORKLOADS["sweep"]
-    points = []
-    seen = set()
-    for p, proj in enumerate(wl.projections):
-        if (proj.K, proj.N) in seen:  # q, k, v, o share one shape
-            continue
-        seen.add((proj.K, proj.N))
-        for mi, M in enumerate(wl.Ms):
-            ops = workloads.algorithmic_ops(M, proj.N, proj.K)
-            steps = max(20, min(2000, int(2e12 / max(ops, 1))))
-            r = run_case(torch, q8, dev, f"sweep_{proj.name}_m{M}", steps, max(3, steps // 20), pk,
-                         pk_src, spec=("sweep", p, mi))
-            b = workloads.algorithmic_bytes(M, proj.N, proj.K, x_bytes=r["xsize"])
-            t = r["t_max"] / steps
-            t_roof = max(b / (pk["hbm_gbs"] * 1e9), ops / (pk["bf16_tflops"] * 1e12))
-            points.append({"projection": proj.name, "K": proj.K, "N": proj.N, "M": M,
-                           "path": r["path"], "us_per_call": round(t * 1e6, 3),
-                           "GBps": round(b / t / 1e9, 1), "TOPS": round(ops / t / 1e12, 2),
-                           "bound": "hbm" if b / (pk["hbm_gbs"] * 1e9) >= ops / (pk["bf16_tflops"] * 1e12)
-                           else "tensor",
-                           "roofline_frac": round(t_roof / t, 4)})
+    pts = sweep_points(torch, q8, torch.device("cuda", 0), pk, pk_src)
     return {"metric": METRIC, "sweep": "dense-layer sweep, hidden 5120 (q/k/v/o 5120x5120, "
             "gate/up 5120x17408, down 17408x5120, GDN in-proj 5120x10240)",
             "time": "whole call per step (all kernels of the path), CUDA graph replays",
             "peaks": {k: pk[k] for k in ("hbm_gbs", "bf16_tflops")}, "peak_source": pk_src,
-            "points": points, "device_error_word": q8.q8_device_error()}
+            "points": pts, "call_frac": sweep_compact(pts),
+            "device_error_word": q8.q8_device_error()}
 
 
 def main(argv=None):

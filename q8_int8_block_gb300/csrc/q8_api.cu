@@ -589,18 +589,25 @@ q8_status q8_set_timing_events(cudaEvent_t* starts, cudaEvent_t* stops, int coun
 }
 
 void q8_release(void) {
-  std::lock_guard<std::mutex> lock(g_mu);
-  int cur = -1;
-  cudaGetDevice(&cur);
-  for (auto& kv : g_ws) {
-    if (kv.second.ptr != nullptr) {
-      cudaSetDevice(kv.first.first);
-      cudaFree(kv.second.ptr);
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int cur = -1;
+    cudaGetDevice(&cur);
+    for (auto& kv : g_ws) {
+      if (kv.second.ptr != nullptr) {
+        cudaSetDevice(kv.first.first);
+        cudaFree(kv.second.ptr);
+      }
     }
+    g_ws.clear();
+    if (cur >= 0) cudaSetDevice(cur);
+    // device addresses (the error word) belong to the context they were looked up in
+    for (DeviceInfo& d : g_dev) d = DeviceInfo();
   }
-  g_ws.clear();
-  if (cur >= 0) cudaSetDevice(cur);
-  forget_kernel_attributes();  // a later context (e.g. after cudaDeviceReset) starts afresh
+  // a later context (e.g. after cudaDeviceReset) starts afresh
+  forget_kernel_attributes();
+  forget_noalloc_scratch();
+  forget_tensor_maps();
 }
 
 const char* q8_version(void) { return "0.1.0"; }
@@ -613,6 +620,8 @@ std::mutex g_attr_mu;
 std::map<std::pair<const void*, int>, size_t> g_smem_set;
 std::map<std::pair<const void*, int>, int> g_regs;
 }  // namespace
+
+int device_info(DeviceInfo* out) { return static_cast<int>(current_device(out)); }
 
 cudaError_t ensure_smem(const void* fn, size_t bytes, int device) {
   std::lock_guard<std::mutex> lock(g_attr_mu);

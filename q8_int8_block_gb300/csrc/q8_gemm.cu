@@ -31,6 +31,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
 
 #include "q8_epi.cuh"
@@ -486,8 +487,8 @@ EncodeTiledFn get_encode_fn() {
 }
 
 // 2-D binary16 matrix [rows, cols] (cols contiguous), box = box_rows x 64 columns, 128B swizzle.
-bool make_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
-                   uint32_t box_rows) {
+bool encode_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {cols, rows};
@@ -497,6 +498,41 @@ bool make_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t co
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Encoded tensor maps, keyed by everything the encoding depends on (address, shape, box),
+// so a cached map is always the one a fresh encoding would give.  Bounded: cleared when full.
+struct TmapKey {
+  const void* ptr;
+  uint64_t rows, cols;
+  uint32_t box_rows;
+  bool operator<(const TmapKey& o) const {
+    if (ptr != o.ptr) return ptr < o.ptr;
+    if (rows != o.rows) return rows < o.rows;
+    if (cols != o.cols) return cols < o.cols;
+    return box_rows < o.box_rows;
+  }
+};
+std::mutex g_tmap_mu;
+std::map<TmapKey, CUtensorMap> g_tmaps;
+constexpr size_t kTmapCacheMax = 4096;
+
+bool make_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows) {
+  const TmapKey key{ptr, rows, cols, box_rows};
+  {
+    std::lock_guard<std::mutex> lock(g_tmap_mu);
+    auto it = g_tmaps.find(key);
+    if (it != g_tmaps.end()) {
+      *map = it->second;
+      return true;
+    }
+  }
+  if (!encode_tmap_f16(map, ptr, rows, cols, box_rows)) return false;
+  std::lock_guard<std::mutex> lock(g_tmap_mu);
+  if (g_tmaps.size() >= kTmapCacheMax) g_tmaps.clear();
+  g_tmaps[key] = *map;
+  return true;
 }
 
 // y = sum over s of part[s] (fixed order: the result does not depend on timing).
@@ -584,6 +620,11 @@ cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const GemmPa
 }
 
 }  // namespace
+
+void forget_tensor_maps() {
+  std::lock_guard<std::mutex> lock(g_tmap_mu);
+  g_tmaps.clear();
+}
 
 // Tail mode: when the tiles fill some whole waves of the GPU plus a partial one, the
 // partial wave's tiles are split along K so that they spread over the idle SMs (at most

@@ -50,6 +50,14 @@ cudaError_t ensure_smem(const void* fn, size_t bytes, int device);
 cudaError_t kernel_regs(const void* fn, int device, int* regs);
 // Drops both caches (q8_release: a later context starts afresh).
 void forget_kernel_attributes();
+// The current device's checked info (compute capability 10.3, SM count, shared-memory
+// limit, the device address of the library's error word), filled on first use per device.
+// Returns 0 (Q8_OK) or a q8_status code.
+int device_info(DeviceInfo* out);
+
+// ---- q8_noalloc.cu ----------------------------------------------------------------
+// Drops the cached device addresses of the static scratch array (q8_release).
+void forget_noalloc_scratch();
 
 // ---- q8_quant.cu ------------------------------------------------------------------
 // Quantizes `rows` rows of K values (xtype 0 = f32, 1 = bf16 bits) into codes and scales.
@@ -128,6 +136,8 @@ cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float
                            const uint16_t* Wd, float* y, int32_t* isum, float* part, int splits,
                            int64_t M, int64_t N, int64_t K, const DeviceInfo& dev,
                            cudaStream_t stream, const Epilogue& epi = Epilogue());
+// Drops the cache of encoded TMA tensor maps (q8_release).
+void forget_tensor_maps();
 // y = op(0, aux) for K == 0 (an empty sum), M*N outputs.
 cudaError_t launch_epilogue_only(const Epilogue& epi, float* y, int64_t n, cudaStream_t stream);
 

@@ -21,13 +21,17 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[Q8_NOALLOC_SCRATCH_BY
 
 constexpr int kMaxDev = 64;
 std::mutex g_na_mu;
-void* g_na_ptr[kMaxDev] = {};
-int g_na_sms[kMaxDev] = {};
-int g_na_smem[kMaxDev] = {};
+void* g_na_ptr[kMaxDev] = {};  // the array's device address, per device (nullptr: not looked up)
 
 size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
+
+void forget_noalloc_scratch() {
+  std::lock_guard<std::mutex> lock(g_na_mu);
+  for (void*& p : g_na_ptr) p = nullptr;
+}
+
 }  // namespace q8
 
 using namespace q8;
@@ -51,39 +55,32 @@ extern "C" q8_status q8_linear_noalloc(const void* x, q8_dtype xtype, const int8
   if (need_d > static_cast<double>(Q8_NOALLOC_SCRATCH_BYTES)) return Q8_ERR_NOMEM;
   if (M == 0 || N == 0) return Q8_OK;
 
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDev) return Q8_ERR_CUDA;
+  // the library's checked device info: compute capability, SM count, shared-memory limit,
+  // and the device error word that the kernels' bounded waits report into
   DeviceInfo di;
+  const int st = device_info(&di);
+  if (st != Q8_OK) return static_cast<q8_status>(st);
+  if (di.device >= kMaxDev) return Q8_ERR_DEVICE;
+  void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_na_mu);
-    if (g_na_ptr[dev] == nullptr) {
-      // one-time set-up on this device (with it current): the array's device address
-      int major = 0, minor = 0;
-      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&g_na_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&g_na_smem[dev], cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-              cudaSuccess)
-        return Q8_ERR_CUDA;
-      if (major != 10 || minor != 3) return Q8_ERR_DEVICE;
+    if (g_na_ptr[di.device] == nullptr) {
+      // one-time set-up on this device (it is current): the array's device address
       void* ptr = nullptr;
-      e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
       if (e != cudaSuccess || ptr == nullptr) return Q8_ERR_CUDA;
-      g_na_ptr[dev] = ptr;
+      g_na_ptr[di.device] = ptr;
     }
-    di.device = dev;
-    di.sm_count = g_na_sms[dev];
-    di.max_smem_optin = g_na_smem[dev];
-    di.err_word = nullptr;  // bounded waits still end; they report nothing here
+    scratch = g_na_ptr[di.device];
   }
+  cudaError_t e;
   if (K == 0) {
     e = cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 4, stream);
     return e == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
   }
   // Every byte of scratch a call reads is written by that call first (codes and scales of
   // all M rows and all N weight rows), so nothing has to be cleared between calls.
-  uint8_t* base = static_cast<uint8_t*>(g_na_ptr[dev]);
+  uint8_t* base = static_cast<uint8_t*>(scratch);
   uint16_t* A16 = reinterpret_cast<uint16_t*>(base);
   float* xd = reinterpret_cast<float*>(base + up256(static_cast<size_t>(M) * K * 2));
   uint16_t* B16 = reinterpret_cast<uint16_t*>(base + up256(static_cast<size_t>(M) * K * 2) +
