@@ -757,7 +757,8 @@ def workload_desc(name):
     desc = {"decode": "decode GEMV, FFN up-projection of a dense ~9B-class layer",
             "tiny": "tiny Q8_0 linear (float32 activations)",
             "prefill9b": "prefill GEMM, 9B-class projection",
-            "prefill27b": "prefill GEMM, 27B-class projection, 1% activation channels x20"}[wname]
+            "prefill27b": "prefill GEMM, 27B-class projection, 1% activation channels x20",
+            "sweep": "dense-layer sweep point, hidden-5120 hybrid layer"}[wname]
     return f"{desc}: {name}"
 
 
