@@ -184,6 +184,28 @@ def recorded_traffic(name):
     return float(rec["dram_bytes_per_launch"])
 
 
+def measured_rates():
+    """Per-SM unit rates measured by bench_rates.py on this GPU type (committed record), or
+    None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "rates_gb300.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def unit_peak(torch, pk, key, ops_per_unit, fallback):
+    """Peak in T-ops/s of a unit rate (per clock per SM) x ops per unit x SMs x maximum SM
+    clock; the rate from the measured record, else `fallback`.  Returns (peak, source)."""
+    rec = measured_rates()
+    rate, src = fallback, "assumed rate"
+    if rec and key in rec.get("rates", {}):
+        rate, src = rec["rates"][key], "bench_rates.py record"
+    sms = sm_count(torch)
+    return rate * ops_per_unit * sms * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12, (
+        f"{rate} {key} ({src}) x {ops_per_unit} ops x {sms} SMs x maximum SM clock")
+
+
 def sm_count(torch):
     return int(torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count)
 
@@ -389,14 +411,18 @@ def run_case(torch, q8, dev, name, steps, warmup, pk, pk_src, clocks=False, e2e=
     if path == "dp4a":
         # CUDA-core integer path: peak from unit counts, 64 dp4a per clock per SM (measured),
         # 4 int8 MACs each, at the maximum SM clock
-        sms = sm_count(torch)
-        dp4a_peak = 64 * 4 * 2 * sms * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        dp4a_peak, dp4a_src = unit_peak(torch, pk, "dp4a_per_clk_sm", 8, 64.0)
         roof = {"bound": "alu", "achieved": round(ops_step / kern / 1e12, 2),
                 "peak": round(dp4a_peak, 1), "unit": "TOPS",
                 "frac": round(ops_step / kern / 1e12 / dp4a_peak, 4),
                 "algorithmic_flops_per_launch": ops_step,
-                "peak_source": f"dp4a: 64 per clock per SM (microbenchmark) x 4 MACs x 2 ops x "
-                               f"{sms} SMs x maximum SM clock"}
+                "peak_source": "dp4a: " + dp4a_src}
+    if path == "tensor":
+        # the GPU's int8 tensor path (mma.sync s8, what an int8 GEMM runs on here), for reference
+        i8, i8_src = unit_peak(torch, pk, "imma_mac_per_clk_sm", 2, 252.0)
+        roof["int8_mma_sync_peak_tops"] = round(i8, 1)
+        roof["int8_equivalent_tops"] = round(ops_step / kern / 1e12, 2)
+        roof["frac_of_int8_mma_sync_peak"] = round(ops_step / kern / 1e12 / i8, 3)
     roof["kernel"] = {"decode": "q8::decode_kernel", "batch": "q8::batch_kernel",
                       "dp4a": "q8::dp4a_gemm_kernel"}.get(path, "q8::gemm_tc_kernel")
     roof["kernel_us"] = round(kern * 1e6, 3)
@@ -471,7 +497,7 @@ def run_bsa(torch, q8, dev, steps, warmup, pk, pk_src):
     fn()
     total, kern = time_graph_steps(torch, q8, [fn], steps, warmup, instrument=False)
     tf = flops / kern / 1e12
-    mma_sync_peak = 1024 * 2 * sm_count(torch) * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    mma_sync_peak, _ = unit_peak(torch, pk, "hmma_mac_per_clk_sm", 2, 1024.0)
     return {"bsa_32k": {"value": round(tf, 2), "unit": "TFLOP/s", "us_per_step": round(kern * 1e6, 2),
                         "algorithmic_flops_per_launch": flops, "visible_pairs": pairs,
                         "block_density": round(len(ci) / (cfg["H"] * nb * (nb + 1) / 2), 4),
