@@ -7,6 +7,7 @@ than the library.  Usage: python -m q8_int8_block_gb300.build [--force] [--jobs 
 import concurrent.futures as cf
 import glob
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -45,12 +46,46 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
+# Kernels whose warp roles resize their registers with setmaxnreg: the split is exact only for
+# the register count the kernel was written for (the constant named here, in the same file).
+# The build reads ptxas's report and stops if the compiled count differs, rather than leave
+# the library to refuse every launch of that kernel at run time.
+REG_PINS = {"q8_gemm.cu": ("gemm_tc_kernel", "kLaunchRegs")}
+
+
+def _check_reg_pin(src: str, ptxas_report: str) -> None:
+    name = os.path.basename(src)
+    if name not in REG_PINS:
+        return
+    kernel, const = REG_PINS[name]
+    m = re.search(r"constexpr int " + const + r" = (\d+);", open(src).read())
+    if not m:
+        raise RuntimeError(f"{name}: constant {const} not found")
+    want = int(m.group(1))
+    current, seen = None, 0
+    for line in ptxas_report.splitlines():
+        e = re.search(r"Compiling entry function '([^']+)'", line)
+        if e:
+            current = e.group(1)
+            continue
+        u = re.search(r"Used (\d+) registers", line)
+        if u and current and kernel in current:
+            seen += 1
+            if int(u.group(1)) != want:
+                raise RuntimeError(f"{name}: {current} compiled to {u.group(1)} registers per thread, "
+                                   f"but its setmaxnreg split assumes {const} = {want}")
+    if seen == 0:
+        raise RuntimeError(f"{name}: no ptxas register report for {kernel}")
+
+
 def _compile(src: str, extra) -> str:
     obj = os.path.join(OBJ, os.path.basename(src) + ".o")
-    cmd = [nvcc()] + ARCH + CFLAGS + list(extra) + ["-c", src, "-o", obj]
+    verbose = ["-Xptxas", "-v"] if os.path.basename(src) in REG_PINS else []
+    cmd = [nvcc()] + ARCH + CFLAGS + verbose + list(extra) + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
+    _check_reg_pin(src, r.stdout + r.stderr)
     return obj
 
 
