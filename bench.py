@@ -693,9 +693,8 @@ def gpu_arm(args):
             extra[k]["note"] = ("3-bit KV-cache codec (Walsh-Hadamard rotation + Lloyd-Max), "
                                 "one attention layer's keys at a 256K-token context")
         # every configured workload, compact: the prefill half of the metric with the rest
-        configs["legend"] = ("[value of the whole call, unit, roofline frac of the main kernel, "
-                             "us per call, us of the main kernel, path]; peaks: hbm "
-                             f"{pk['hbm_gbs']} GB/s, tensor {pk['bf16_tflops']} TFLOP/s ({pk_src})")
+        configs["legend"] = ("[call value, unit, kernel roofline frac, us/call, kernel us, path]; "
+                             f"peaks {pk['hbm_gbs']} GB/s, {pk['bf16_tflops']} TFLOP/s ({pk_src})")
         configs["decode_m1"] = compact(dict(r, steps=args.steps))
         for name, st in CONFIG_CASES:
             e = run_case(torch, q8, dev, name, st, max(3, st // 50), pk, pk_src)
@@ -704,7 +703,9 @@ def gpu_arm(args):
         pts = sweep_points(torch, q8, dev, pk, pk_src)
         extra["sweep_points"] = pts
         configs["sweep_call_frac"] = sweep_compact(pts)
-        configs["int8_library_ref"] = int8_library_reference(torch, dev)
+        ref = int8_library_reference(torch, dev)
+        extra["int8_library_ref"] = ref
+        configs["int8_library_ref_tops"] = ref.get("tops")
     err = q8.q8_device_error()
     desc = workload_desc(args.workload)
     line = {
