@@ -117,7 +117,7 @@ q8_status resolve_path(int64_t M, int64_t N, int64_t K, q8_path req, const Devic
 }
 
 // Scratch of the tensor path: A16 [M,K] f16 codes, xd [M,K/32] f32, B16 [N,K] f16 codes, and
-// the GEMM's partial outputs (split-K, or its split tail wave: gemm_part_bytes).
+// the GEMM's partial outputs (split-K, or its stream-K partial tiles: gemm_part_bytes).
 // With prepared weights (q8_linear_prepared) the B16 region is not needed.
 size_t tensor_ws_bytes(int64_t M, int64_t N, int64_t K, size_t part_bytes, bool with_b16 = true) {
   return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(M) * (K / kQK) * 4) +

@@ -12,8 +12,11 @@
 // accumulator).  Each Q8_0 block gets its own TMEM accumulator (two K=16 MMAs starting
 // from zero), so the value read back is exactly the int32 block sum isum[m,n,b].
 //
-// Design (one CTA per 128 x 256 output tile, 384 threads = 3 warpgroups; the control
-// warpgroup hands registers to the two drain warpgroups with setmaxnreg):
+// Design (384 threads = 3 warpgroups per CTA, one CTA per SM; the control warpgroup hands
+// registers to the two drain warpgroups with setmaxnreg).  A CTA works through one to three
+// segments, each a 128 x 256 output tile over a range of K: a whole tile, a split-K range
+// of one, or (stream-K, for a partial last wave) an equal run of scale windows that may
+// cross tile boundaries (see gemm_schedule).  The pipelines run on across segments.
 //   warp 0     TMA producer: A (activation codes, 128 x 64 binary16) and B (weight codes,
 //              256 x 64 binary16) tiles with 128-byte swizzle into a 3-stage ring;
 //   warp 1     TMEM owner and MMA issuer: per 32-K block, 2 x tcgen05.mma
@@ -25,12 +28,15 @@
 //              the block sums of their TMEM lanes 16 columns at a time and the column
 //              scales from shared memory, both one chunk ahead, then
 //              y_acc += (xd * Wd) * isum in binary32 registers (packed f32x2 multiply,
-//              scalar fused multiply-add); release the TMEM buffer; finally store y.
+//              scalar fused multiply-add); release the TMEM buffer; at a segment's end
+//              store y, or a partial tile that a reduction kernel adds.  The CTA's last
+//              segment is staged in the then idle operand ring and written by TMA stores.
 // Block-sum mode (for checking) stores the TMEM block sums as int32 instead.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstring>
 #include <map>
 #include <mutex>
 
@@ -65,6 +71,8 @@ constexpr uint32_t kWinDw = kWin * BN * 4;  // Wd of the tile's columns, f32   (
 constexpr uint32_t kWinDx = kWin * BM * 4;  // xd of the tile's rows, f32      (8 KB)
 constexpr size_t kSmemBytes = 1024 /*align*/ + kStages * (kStageA + kStageB) +
                               kWinSlots * (kWinDw + kWinDx);
+// The CTA's last results are staged in the operand ring, 16 KB per drain warp.
+static_assert(kDrainWarps * 32 * 128 * 4 <= kStages * (kStageA + kStageB), "output staging");
 
 // Output tile t -> its first row (token) and column (weight row): token tile fastest, so the
 // CTAs resident at one time share a few weight slabs of B.  (A grouped order that keeps A
@@ -79,18 +87,67 @@ struct GemmParams {
   const float* xd;     // [M, nb]
   const uint16_t* Wd;  // [N, nb]
   float* y;            // [M, N]
-  float* part;         // split-K partial outputs: [splits, M, N]; in tail mode [unit, BM, BN]
+  float* part;         // split-K partial outputs: [splits, M, N]; stream-K: [2 sk_ctas, BM, BN]
   int splits;          // K split into this many ranges of whole scale windows (blockIdx.y)
-  // Tail mode (tail_splits > 0): blocks [0, main_tiles) are whole tiles (K not split);
-  // the tiles of the last, partial wave are split tail_splits ways along K, one block per
-  // (tile, range) unit, and their partial outputs are added by reduce_tail_kernel.
-  int main_tiles;
-  int tail_splits;
+  // Stream-K (sk_ctas > 0): the scale windows of tiles [0, sk_tiles), sk_windows of them in
+  // tile order, are cut into sk_ctas equal contiguous runs, one per CTA [0, sk_ctas) (see
+  // cta_segments); the CTAs after them take one whole tile each, tiles [sk_tiles, ...).  A
+  // run that covers only part of a tile stores a partial tile, and reduce_sk_kernel adds a
+  // tile's partials.  The runs come first so that they start together on an idle GPU and the
+  // whole tiles after them even out the SMs' finishing times.
+  int sk_ctas;
+  int sk_tiles;
+  int sk_windows;
   int32_t* isum;       // [M, N, nb] (block-sum mode)
   int M, N, K;
+  int tma_y;           // whole-K tiles are stored through tmY (binary32 y, box 32 x 32)
+  int tma_part;        // partial tiles are stored through tmP (binary32, 3-D, box 32 x 32 x 1):
+                       // stream-K [2 sk_ctas][BM][BN] at (column, row, slot), split-K
+                       // [splits][M][N] at (n, m, split)
   uint32_t* err;
-  Epilogue epi;        // fused output step (applied by the split-K reduction when splitting)
+  Epilogue epi;        // fused output step (applied by the reduction where K is split)
 };
+
+// A CTA's work: up to kMaxSegs segments, each one output tile over a range of its scale
+// windows.  A stream-K run is shorter than two tiles, so it touches at most three.
+constexpr int kMaxSegs = 3;
+struct Seg {
+  int tile;
+  int w0, w1;  // scale windows [w0, w1) of the tile's K
+  int slot;    // >= 0: partial tile slot of a stream-K run; -1: whole K of the tile
+};
+
+// Stream-K: run j of G covers windows [start(j), start(j + 1)) of the W in the stream-K
+// tiles, start(j) = floor(j W / G).  A partial first segment of run j takes partial-tile
+// slot 2 j, a partial last one slot 2 j + 1.
+__host__ __device__ __forceinline__ int sk_start(int j, int W, int G) {
+  return static_cast<int>(static_cast<int64_t>(j) * W / G);
+}
+
+__device__ int cta_segments(const GemmParams& p, int nwin, Seg* seg) {
+  const int bid = static_cast<int>(blockIdx.x);
+  if (bid >= p.sk_ctas) {
+    const int s = static_cast<int>(blockIdx.y), ns = p.splits;  // split-K range s of ns
+    seg[0].tile = p.sk_tiles + (bid - p.sk_ctas);
+    seg[0].w0 = static_cast<int>(static_cast<int64_t>(s) * nwin / ns);
+    seg[0].w1 = static_cast<int>(static_cast<int64_t>(s + 1) * nwin / ns);
+    seg[0].slot = -1;
+    return 1;
+  }
+  const int j = bid;
+  const int a = sk_start(j, p.sk_windows, p.sk_ctas);
+  const int e = sk_start(j + 1, p.sk_windows, p.sk_ctas);
+  int n = 0;
+  for (int t = a / nwin; t * nwin < e && n < kMaxSegs; ++t, ++n) {
+    const int w0 = max(a, t * nwin) - t * nwin;
+    const int w1 = min(e, (t + 1) * nwin) - t * nwin;
+    seg[n].tile = t;
+    seg[n].w0 = w0;
+    seg[n].w1 = w1;
+    seg[n].slot = (w0 == 0 && w1 == nwin) ? -1 : (n == 0 ? 2 * j : 2 * j + 1);
+  }
+  return n;
+}
 
 // Fill one window of scales: Wd of the tile's 256 columns and xd of its 128 rows, blocks
 // [16 w, 16 w + 16) (zero past the ends), as f32 [block][column] and [block][row].
@@ -152,9 +209,12 @@ __device__ __forceinline__ void stage_scales(const GemmParams& p, int w, int m0,
 
 // kFused: the drain's final store applies the epilogue (residual, SiLU gate, bfloat16 y);
 // the plain layer is a separate instantiation so that it carries none of that code.
-template <bool kBlockSums, bool kFused>
+// kSK: the launch has stream-K runs, whose CTAs walk several segments; without it every CTA
+// has exactly one, known at compile time.
+template <bool kBlockSums, bool kFused, bool kSK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmP,
                    const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
@@ -162,32 +222,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t sfull_bar[kWinSlots], sempty_bar[kWinSlots];
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
+  __shared__ Seg segs[kMaxSegs];
+  __shared__ int nseg_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = p.M, N = p.N, K = p.K;
   const int nb = K / kQK;
-  // split-K: this CTA takes scale windows [w_begin, w_end) of the K range, i.e. Q8_0 blocks
-  // [b_begin, b_end) and 64-wide stages [kb_begin, kb_end); ring slots, TMEM buffers and
-  // barrier phases count from the start of the range
-  const int nwin_all = (nb + kWin - 1) / kWin;
-  int tile = static_cast<int>(blockIdx.x), split = static_cast<int>(blockIdx.y), nsplit = p.splits;
-  const bool tail = !kBlockSums && p.tail_splits > 0 && tile >= p.main_tiles;
-  if (tail) {
-    const int u = tile - p.main_tiles;
-    tile = p.main_tiles + u / p.tail_splits;
-    split = u % p.tail_splits;
-    nsplit = p.tail_splits;
-  }
-  // this block stores final outputs (else partial sums for a reduction kernel)
-  const bool direct = p.splits == 1 && !tail;
-  const int w_begin = static_cast<int>(static_cast<int64_t>(split) * nwin_all / nsplit);
-  const int w_end = static_cast<int>(static_cast<int64_t>(split + 1) * nwin_all / nsplit);
-  const int b_begin = w_begin * kWin;
-  const int b_end = (w_end * kWin < nb) ? w_end * kWin : nb;
-  const int kb_begin = b_begin / 2;
-  const int kb_end = (b_end + 1) / 2;
-  int m0, n0;
-  tile_origin(tile, (M + BM - 1) / BM, &m0, &n0);
+  const int nwin = (nb + kWin - 1) / kWin;
+  const int mtiles = (M + BM - 1) / BM;
+  // Every role walks the CTA's segments in order.  Segment s covers Q8_0 blocks
+  // [16 w0, min(16 w1, nb)) of its tile, i.e. 64-wide stages [8 w0, (b_end + 1) / 2); the
+  // operand ring, the TMEM buffers, the scale ring and their barrier phases count on across
+  // segments, so the pipelines do not drain between them.
 
   // 1024-byte aligned carve-up (128-byte swizzle atoms must sit on 1024-byte boundaries)
   const uint32_t raw = smem_u32(smem_raw);
@@ -199,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    nseg_s = cta_segments(p, nwin, segs);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
@@ -220,24 +267,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_slot;
+  const int nseg = kSK ? nseg_s : 1;
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     if (warp == 0) {
       // ------------------------------- TMA producer -----------------------------------
       if (lane == 0) {
-        int issued = 0;
-        for (int kb = kb_begin; kb < kb_end; ++kb) {
-          const int i = kb - kb_begin;
-          const int s = i % kStages;
-          if (!mbar_wait(&empty_bar[s], ((i / kStages) & 1) ^ 1, &abort_flag)) {
-            report_error(p.err, kErrWaitTimeout, &abort_flag);
-            break;
+        int issued = 0;  // stages, all segments
+        bool ok = true;
+        for (int sg = 0; sg < nseg && ok; ++sg) {
+          const Seg S = segs[sg];
+          int m0, n0;
+          tile_origin(S.tile, mtiles, &m0, &n0);
+          const int kb_end = (min(S.w1 * kWin, nb) + 1) / 2;
+          for (int kb = S.w0 * (kWin / 2); kb < kb_end; ++kb) {
+            const int s = issued % kStages;
+            if (!mbar_wait(&empty_bar[s], ((issued / kStages) & 1) ^ 1, &abort_flag)) {
+              report_error(p.err, kErrWaitTimeout, &abort_flag);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full_bar[s], kStageA + kStageB);
+            tma_load_2d(sA + s * kStageA, &tmA, &full_bar[s], kb * BK, m0);
+            tma_load_2d(sB + s * kStageB, &tmB, &full_bar[s], kb * BK, n0);
+            ++issued;
           }
-          mbar_arrive_expect_tx(&full_bar[s], kStageA + kStageB);
-          tma_load_2d(sA + s * kStageA, &tmA, &full_bar[s], kb * BK, m0);
-          tma_load_2d(sB + s * kStageB, &tmB, &full_bar[s], kb * BK, n0);
-          ++issued;
         }
         for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
           if (!mbar_wait(&full_bar[i % kStages], (i / kStages) & 1, nullptr)) {
@@ -249,40 +304,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------- MMA issuer -------------------------------------
       if (lane == 0) {
         constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+        int i = 0;  // stages consumed, all segments
+        int g = 0;  // blocks issued, all segments: TMEM buffer g & 1, phase (g >> 1) & 1
         int last_stage = -1;
-        for (int kb = kb_begin; kb < kb_end; ++kb) {
-          const int i = kb - kb_begin;
-          const int s = i % kStages;
-          if (!mbar_wait(&full_bar[s], (i / kStages) & 1, &abort_flag)) {
-            report_error(p.err, kErrWaitTimeout, &abort_flag);
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + s * kStageA);
-          const uint32_t b0 = smem_u32(sB + s * kStageB);
-          const int nblk = (b_end - 2 * kb) < 2 ? (b_end - 2 * kb) : 2;
-          bool ok = true;
-          for (int j = 0; j < nblk; ++j) {
-            const int blk = 2 * kb + j - b_begin;  // block of the range
-            const int buf = blk & 1;
-            if (!mbar_wait(&tempty_bar[buf], ((blk >> 1) & 1) ^ 1, &abort_flag)) {
+        bool ok = true;
+        for (int sg = 0; sg < nseg && ok; ++sg) {
+          const Seg S = segs[sg];
+          const int b_end = min(S.w1 * kWin, nb);
+          for (int kb = S.w0 * (kWin / 2); kb < (b_end + 1) / 2 && ok; ++kb, ++i) {
+            const int s = i % kStages;
+            if (!mbar_wait(&full_bar[s], (i / kStages) & 1, &abort_flag)) {
               report_error(p.err, kErrWaitTimeout, &abort_flag);
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
+            const uint32_t a0 = smem_u32(sA + s * kStageA);
+            const uint32_t b0 = smem_u32(sB + s * kStageB);
+            const int nblk = min(b_end - 2 * kb, 2);
+            for (int j = 0; j < nblk; ++j, ++g) {
+              const int buf = g & 1;
+              if (!mbar_wait(&tempty_bar[buf], ((g >> 1) & 1) ^ 1, &abort_flag)) {
+                report_error(p.err, kErrWaitTimeout, &abort_flag);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              const uint32_t koff = static_cast<uint32_t>((2 * j + kk) * 32);  // 16 f16 = 32 B
-              mma_f16_ss(d, sdesc_k_sw128(a0 + koff), sdesc_k_sw128(b0 + koff), idesc,
-                         kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < 2; ++kk) {
+                const uint32_t koff = static_cast<uint32_t>((2 * j + kk) * 32);  // 16 f16 = 32 B
+                mma_f16_ss(d, sdesc_k_sw128(a0 + koff), sdesc_k_sw128(b0 + koff), idesc,
+                           kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&tfull_bar[buf]);
             }
-            mma_commit(&tfull_bar[buf]);
+            mma_commit(&empty_bar[s]);
+            last_stage = i;
           }
-          mma_commit(&empty_bar[s]);
-          last_stage = i;
-          if (!ok) break;
         }
         // do not leave while MMAs are still reading shared memory / writing TMEM
         if (last_stage >= 0 &&
@@ -292,15 +351,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if constexpr (!kBlockSums) {
       // ------------------------------- scale producer (warps 2-3) ---------------------
       const int t = threadIdx.x - 64;  // 0..63
-      for (int w = w_begin; w < w_end; ++w) {
-        const int u = w - w_begin;
-        const int slot = u % kWinSlots;
-        if (!mbar_wait(&sempty_bar[slot], ((u / kWinSlots) & 1) ^ 1, &abort_flag)) {
-          report_error(p.err, kErrWaitTimeout, &abort_flag);
-          break;
+      int u = 0;  // windows staged, all segments
+      bool ok = true;
+      for (int sg = 0; sg < nseg && ok; ++sg) {
+        const Seg S = segs[sg];
+        int m0, n0;
+        tile_origin(S.tile, mtiles, &m0, &n0);
+        for (int w = S.w0; w < S.w1; ++w, ++u) {
+          const int slot = u % kWinSlots;
+          if (!mbar_wait(&sempty_bar[slot], ((u / kWinSlots) & 1) ^ 1, &abort_flag)) {
+            report_error(p.err, kErrWaitTimeout, &abort_flag);
+            ok = false;
+            break;
+          }
+          stage_scales(p, w, m0, n0, nb, sW + slot * kWin * BN, sX + slot * kWin * BM, t);
+          mbar_arrive(&sfull_bar[slot]);  // release: the stores above are visible to waiters
         }
-        stage_scales(p, w, m0, n0, nb, sW + slot * kWin * BN, sX + slot * kWin * BM, t);
-        mbar_arrive(&sfull_bar[slot]);  // release: the stores above are visible to waiters
       }
     }
   } else {
@@ -314,158 +380,219 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const int m = m0 + row;
-    const bool m_ok = m < M;
     float2 acc[kBlockSums ? 1 : 64];
-    if constexpr (!kBlockSums) {
-#pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
-    }
     bool failed = false;
-    for (int w = w_begin; w < w_end && !failed; ++w) {
-      const int u = w - w_begin;
-      const int slot = u % kWinSlots;
-      const float* dws = sW + slot * kWin * BN + wg * 128;
-      const float* dxs = sX + slot * kWin * BM;
+    int u = 0;  // windows consumed, all segments
+    int g = 0;  // blocks drained, all segments
+    for (int sg = 0; sg < nseg && !failed; ++sg) {
+      // (the segment's fields are read from shared memory where they are used, so that
+      // the tile's origin is not held in registers through the accumulation)
+      const int w1 = segs[sg].w1;
       if constexpr (!kBlockSums) {
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sfull_bar[slot], (u / kWinSlots) & 1, &abort_flag))) {
-          if (lane == 0) report_error(p.err, kErrWaitTimeout, &abort_flag);
-          failed = true;
-          break;
-        }
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
       }
-      const int nbw = (nb - w * kWin) < kWin ? (nb - w * kWin) : kWin;
-      if constexpr (!kBlockSums) {
-        // the last window: bring this thread's 128 aux values towards L2 for the epilogue
-        if (kFused && direct && w + 1 == w_end && m_ok)
-          epi_prefetch(p.epi, static_cast<int64_t>(m) * N + n0 + wg * 128,
-                       min(128, N - (n0 + wg * 128)));
-      }
-#pragma unroll 1
-      for (int bb = 0; bb < nbw; ++bb) {
-        const int blk = w * kWin + bb;  // absolute block (block-sum output index)
-        const int lb = blk - b_begin;   // block of the range: TMEM buffer and phase
-        const int buf = lb & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull_bar[buf], (lb >> 1) & 1, &abort_flag))) {
-          if (lane == 0) report_error(p.err, kErrWaitTimeout, &abort_flag);
-          failed = true;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                               static_cast<uint32_t>(buf * BN + wg * 128);
-        const float* dwb = dws + bb * BN;
-        float dx = 0.0f;
-        if constexpr (!kBlockSums) dx = dxs[bb * BM + row];
-        const float2 dx2 = make_float2(dx, dx);
-        uint32_t r[2][16];
-        float4 wv[2][4];
-        tmem_ld_32x32b_x16(taddr, r[0]);
+      for (int w = segs[sg].w0; w < w1 && !failed; ++w, ++u) {
+        const int slot = u % kWinSlots;
+        const float* dws = sW + slot * kWin * BN + wg * 128;
+        const float* dxs = sX + slot * kWin * BM;
         if constexpr (!kBlockSums) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) wv[0][i] = *reinterpret_cast<const float4*>(dwb + 4 * i);
-        }
-        tmem_ld_wait_regs(r[0]);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          if (c + 1 < 8) {
-            tmem_ld_32x32b_x16(taddr + (c + 1) * 16, r[(c + 1) & 1]);
-            if constexpr (!kBlockSums) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                wv[(c + 1) & 1][i] = *reinterpret_cast<const float4*>(dwb + (c + 1) * 16 + 4 * i);
-            }
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sfull_bar[slot], (u / kWinSlots) & 1, &abort_flag))) {
+            if (lane == 0) report_error(p.err, kErrWaitTimeout, &abort_flag);
+            failed = true;
+            break;
           }
-          const uint32_t* rc = r[c & 1];
-          if constexpr (kBlockSums) {
-            if (m_ok) {
+        }
+        const int nbw = min(nb - w * kWin, kWin);
+        if constexpr (kFused) {
+          // the last window: bring this thread's 128 aux values towards L2 for the epilogue
+          const Seg S = segs[sg];
+          int m0, n0;
+          tile_origin(S.tile, mtiles, &m0, &n0);
+          if (S.slot < 0 && p.splits == 1 && w + 1 == w1 && m0 + row < M)
+            epi_prefetch(p.epi, static_cast<int64_t>(m0 + row) * N + n0 + wg * 128,
+                         min(128, N - (n0 + wg * 128)));
+        }
+#pragma unroll 1
+        for (int bb = 0; bb < nbw; ++bb, ++g) {
+          const int blk = w * kWin + bb;  // block of the tile's K (block-sum output index)
+          const int buf = g & 1;
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull_bar[buf], (g >> 1) & 1, &abort_flag))) {
+            if (lane == 0) report_error(p.err, kErrWaitTimeout, &abort_flag);
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                 static_cast<uint32_t>(buf * BN + wg * 128);
+          const float* dwb = dws + bb * BN;
+          float dx = 0.0f;
+          if constexpr (!kBlockSums) dx = dxs[bb * BM + row];
+          const float2 dx2 = make_float2(dx, dx);
+          uint32_t r[2][16];
+          float4 wv[2][4];
+          tmem_ld_32x32b_x16(taddr, r[0]);
+          if constexpr (!kBlockSums) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int n = n0 + wg * 128 + c * 16 + i;
-                if (n < N)
-                  p.isum[(static_cast<int64_t>(m) * N + n) * nb + blk] =
-                      __float2int_rn(__uint_as_float(rc[i]));
+            for (int i = 0; i < 4; ++i) wv[0][i] = *reinterpret_cast<const float4*>(dwb + 4 * i);
+          }
+          tmem_ld_wait_regs(r[0]);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            if (c + 1 < 8) {
+              tmem_ld_32x32b_x16(taddr + (c + 1) * 16, r[(c + 1) & 1]);
+              if constexpr (!kBlockSums) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  wv[(c + 1) & 1][i] = *reinterpret_cast<const float4*>(dwb + (c + 1) * 16 + 4 * i);
               }
             }
-          } else {
+            const uint32_t* rc = r[c & 1];
+            if constexpr (kBlockSums) {
+              int m0, n0;
+              tile_origin(segs[sg].tile, mtiles, &m0, &n0);
+              const int m = m0 + row;
+              if (m < M) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float4 w4 = wv[c & 1][i];
-              const float2 c0 = __fmul2_rn(dx2, make_float2(w4.x, w4.y));
-              const float2 c1 = __fmul2_rn(dx2, make_float2(w4.z, w4.w));
-              const int a = (c * 16 + 4 * i) >> 1;
-              acc[a].x = fmaf(c0.x, __uint_as_float(rc[4 * i]), acc[a].x);
-              acc[a].y = fmaf(c0.y, __uint_as_float(rc[4 * i + 1]), acc[a].y);
-              acc[a + 1].x = fmaf(c1.x, __uint_as_float(rc[4 * i + 2]), acc[a + 1].x);
-              acc[a + 1].y = fmaf(c1.y, __uint_as_float(rc[4 * i + 3]), acc[a + 1].y);
+                for (int i = 0; i < 16; ++i) {
+                  const int n = n0 + wg * 128 + c * 16 + i;
+                  if (n < N)
+                    p.isum[(static_cast<int64_t>(m) * N + n) * nb + blk] =
+                        __float2int_rn(__uint_as_float(rc[i]));
+                }
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float4 w4 = wv[c & 1][i];
+                const float2 c0 = __fmul2_rn(dx2, make_float2(w4.x, w4.y));
+                const float2 c1 = __fmul2_rn(dx2, make_float2(w4.z, w4.w));
+                const int a = (c * 16 + 4 * i) >> 1;
+                acc[a].x = fmaf(c0.x, __uint_as_float(rc[4 * i]), acc[a].x);
+                acc[a].y = fmaf(c0.y, __uint_as_float(rc[4 * i + 1]), acc[a].y);
+                acc[a + 1].x = fmaf(c1.x, __uint_as_float(rc[4 * i + 2]), acc[a + 1].x);
+                acc[a + 1].y = fmaf(c1.y, __uint_as_float(rc[4 * i + 3]), acc[a + 1].y);
+              }
             }
+            if (c + 1 < 8) tmem_ld_wait_regs(r[(c + 1) & 1]);
           }
-          if (c + 1 < 8) tmem_ld_wait_regs(r[(c + 1) & 1]);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty_bar[buf]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+        if constexpr (!kBlockSums) {
+          __syncwarp();
+          if (lane == 0 && !failed) mbar_arrive(&sempty_bar[slot]);
+        }
       }
       if constexpr (!kBlockSums) {
-        __syncwarp();
-        if (lane == 0 && !failed) mbar_arrive(&sempty_bar[slot]);
-      }
-    }
-    if constexpr (!kBlockSums) {
-      if (m_ok && !failed && tail) {
-        // this unit's partial tile, compact: [unit][BM][BN], no bounds past N to mind
-        float* dst = p.part + (static_cast<int64_t>(blockIdx.x - p.main_tiles) * BM + row) * BN + wg * 128;
+        const Seg S = segs[sg];
+        int m0, n0;
+        tile_origin(S.tile, mtiles, &m0, &n0);
+        const int m = m0 + row;
+        const bool m_ok = m < M;
+        // this segment stores final outputs (else partial sums for a reduction kernel)
+        const bool direct = S.slot < 0 && p.splits == 1;
+        // The CTA's last segment is stored by TMA: y of a whole-K tile (plain output), or a
+        // partial tile.  The operand ring is idle by then (every MMA has completed and no load
+        // is left), so each drain warp stages its 32 rows x 128 columns there as four 32 x 32
+        // boxes in the 128-byte swizzled layout (16-byte chunk c of row r at position
+        // c ^ (r % 8): the warp's shared-memory stores hit distinct banks), and one lane
+        // writes them as whole 128-byte lines, instead of 32 rows' scattered 16-byte pieces.
+        // (partial tiles take this path only without stream-K: with it, the extra code in
+        // the drain measurably slowed the accumulation loop of the stream-K kernels)
+        const bool tma = sg + 1 == nseg && (direct ? (!kFused && p.tma_y) : (!kSK && p.tma_part));
+        if (tma && !failed) {
+          float* stg = reinterpret_cast<float*>(base) + (warp - 4) * (32 * 128);
+          // box origin: (column, row[, plane]) in the target tensor
+          int x = n0 + wg * 128, yr = m0 + quad * 32, z = static_cast<int>(blockIdx.y);
+          bool rows_in = yr < M;
+          if (S.slot >= 0) {
+            x = wg * 128;
+            yr = quad * 32;
+            z = S.slot;
+            rows_in = true;
+          }
+          const int x_end = S.slot >= 0 ? BN : N;
 #pragma unroll
-        for (int i = 0; i < 64; i += 2)
-          *reinterpret_cast<float4*>(dst + 2 * i) = make_float4(acc[i].x, acc[i].y, acc[i + 1].x, acc[i + 1].y);
-      } else if (m_ok && !failed) {
-        float* yrow = (p.splits > 1 ? p.part + static_cast<int64_t>(blockIdx.y) * M * N : p.y) +
-                      static_cast<int64_t>(m) * N;
-        const int nbase = n0 + wg * 128;
-        if (kFused && direct) {
-          const int64_t r0 = static_cast<int64_t>(m) * N + nbase;
-          if ((N & 3) == 0 && nbase + 128 <= N) {
-            // 4 chunks of 32 columns; the 8 aux loads of chunk h + 1 are in flight while
-            // chunk h is computed and stored
-            float4 a[2][8];
+          for (int q = 0; q < 4; ++q) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) a[0][q] = epi_aux4(p.epi, r0 + 4 * q);
+            for (int k = 0; k < 8; ++k) {
+              const int i = 16 * q + 2 * k;
+              *reinterpret_cast<float4*>(stg + q * 1024 + lane * 32 + ((k ^ (lane & 7)) * 4)) =
+                  make_float4(acc[i].x, acc[i].y, acc[i + 1].x, acc[i + 1].y);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && rows_in) {
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              if (h + 1 < 4) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) a[(h + 1) & 1][q] = epi_aux4(p.epi, r0 + 32 * (h + 1) + 4 * q);
-              }
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                const int i = 16 * h + 2 * q;  // columns 2i .. 2i + 3 of the slice
-                const float4 v = make_float4(acc[i].x, acc[i].y, acc[i + 1].x, acc[i + 1].y);
-                epi_put4(p.epi, p.y, r0 + 32 * h + 4 * q, epi_apply4(p.epi, v, a[h & 1][q]));
+            for (int q = 0; q < 4; ++q) {
+              if (x + 32 * q < x_end) {
+                if (direct)
+                  tma_store_2d(&tmY, stg + q * 1024, x + 32 * q, yr);
+                else
+                  tma_store_3d(&tmP, stg + q * 1024, x + 32 * q, yr, z);
               }
             }
+            bulk_commit_group();
+          }
+        } else if (m_ok && !failed && S.slot >= 0) {
+          // a stream-K partial tile, compact: [slot][BM][BN], no bounds past N to mind
+          float* dst = p.part + (static_cast<int64_t>(S.slot) * BM + row) * BN + wg * 128;
+#pragma unroll
+          for (int i = 0; i < 64; i += 2)
+            *reinterpret_cast<float4*>(dst + 2 * i) = make_float4(acc[i].x, acc[i].y, acc[i + 1].x, acc[i + 1].y);
+        } else if (m_ok && !failed) {
+          float* yrow = (p.splits > 1 ? p.part + static_cast<int64_t>(blockIdx.y) * M * N : p.y) +
+                        static_cast<int64_t>(m) * N;
+          const int nbase = n0 + wg * 128;
+          if (kFused && direct) {
+            const int64_t r0 = static_cast<int64_t>(m) * N + nbase;
+            if ((N & 3) == 0 && nbase + 128 <= N) {
+              // 4 chunks of 32 columns; the 8 aux loads of chunk h + 1 are in flight while
+              // chunk h is computed and stored
+              float4 a[2][8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) a[0][q] = epi_aux4(p.epi, r0 + 4 * q);
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                if (h + 1 < 4) {
+#pragma unroll
+                  for (int q = 0; q < 8; ++q) a[(h + 1) & 1][q] = epi_aux4(p.epi, r0 + 32 * (h + 1) + 4 * q);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const int i = 16 * h + 2 * q;  // columns 2i .. 2i + 3 of the slice
+                  const float4 v = make_float4(acc[i].x, acc[i].y, acc[i + 1].x, acc[i + 1].y);
+                  epi_put4(p.epi, p.y, r0 + 32 * h + 4 * q, epi_apply4(p.epi, v, a[h & 1][q]));
+                }
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 64; ++i) {
+                if (nbase + 2 * i < N) epi_store(p.epi, p.y, r0 + 2 * i, acc[i].x);
+                if (nbase + 2 * i + 1 < N) epi_store(p.epi, p.y, r0 + 2 * i + 1, acc[i].y);
+              }
+            }
+          } else if ((N & 3) == 0 && nbase + 128 <= N) {
+#pragma unroll
+            for (int i = 0; i < 64; i += 2)
+              *reinterpret_cast<float4*>(yrow + nbase + 2 * i) =
+                  make_float4(acc[i].x, acc[i].y, acc[i + 1].x, acc[i + 1].y);
           } else {
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
-              if (nbase + 2 * i < N) epi_store(p.epi, p.y, r0 + 2 * i, acc[i].x);
-              if (nbase + 2 * i + 1 < N) epi_store(p.epi, p.y, r0 + 2 * i + 1, acc[i].y);
+              if (nbase + 2 * i < N) yrow[nbase + 2 * i] = acc[i].x;
+              if (nbase + 2 * i + 1 < N) yrow[nbase + 2 * i + 1] = acc[i].y;
             }
-          }
-        } else if ((N & 3) == 0 && nbase + 128 <= N) {
-#pragma unroll
-          for (int i = 0; i < 64; i += 2)
-            *reinterpret_cast<float4*>(yrow + nbase + 2 * i) =
-                make_float4(acc[i].x, acc[i].y, acc[i + 1].x, acc[i + 1].y);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            if (nbase + 2 * i < N) yrow[nbase + 2 * i] = acc[i].x;
-            if (nbase + 2 * i + 1 < N) yrow[nbase + 2 * i + 1] = acc[i].y;
           }
         }
       }
     }
   }
 
+  if (warp >= 4 && lane == 0) bulk_wait_all();  // this warp's TMA stores have completed
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -494,28 +621,39 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D binary16 matrix [rows, cols] (cols contiguous), box = box_rows x 64 columns, 128B swizzle.
-bool encode_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
-                     uint32_t box_rows) {
+// The kinds of tensor map the GEMM uses, all [planes][rows][cols] with cols contiguous and the
+// 128-byte swizzle: the binary16 operands (2-D, box box_rows x 64 columns) and the binary32
+// outputs the drain stores from its staged boxes (box 32 x 32: y 2-D, partial tiles 3-D).
+enum TmapKind : uint32_t { kTmapF16Operand = 0, kTmapF32Out = 1, kTmapF32Planes = 2 };
+
+bool encode_tmap(CUtensorMap* map, TmapKind kind, const void* ptr, uint64_t planes, uint64_t rows,
+                 uint64_t cols, uint32_t box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const bool f16 = kind == kTmapF16Operand;
+  const uint64_t esz = f16 ? 2 : 4;
+  const cuuint64_t dims[3] = {cols, rows, planes};
+  const cuuint64_t strides[2] = {cols * esz, rows * cols * esz};
+  const cuuint32_t box[3] = {f16 ? static_cast<cuuint32_t>(BK) : 32u, box_rows, 1u};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+             kind == kTmapF32Planes ? 3 : 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Encoded tensor maps, keyed by everything the encoding depends on (address, shape, box),
-// so a cached map is always the one a fresh encoding would give.  Bounded: cleared when full.
+// Encoded tensor maps, keyed by everything the encoding depends on (kind, address, shape,
+// box), so a cached map is always the one a fresh encoding would give.  Bounded: cleared
+// when full.
 struct TmapKey {
+  uint32_t kind;
   const void* ptr;
-  uint64_t rows, cols;
+  uint64_t planes, rows, cols;
   uint32_t box_rows;
   bool operator<(const TmapKey& o) const {
+    if (kind != o.kind) return kind < o.kind;
     if (ptr != o.ptr) return ptr < o.ptr;
+    if (planes != o.planes) return planes < o.planes;
     if (rows != o.rows) return rows < o.rows;
     if (cols != o.cols) return cols < o.cols;
     return box_rows < o.box_rows;
@@ -525,9 +663,9 @@ std::mutex g_tmap_mu;
 std::map<TmapKey, CUtensorMap> g_tmaps;
 constexpr size_t kTmapCacheMax = 4096;
 
-bool make_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
-                   uint32_t box_rows) {
-  const TmapKey key{ptr, rows, cols, box_rows};
+bool make_tmap(CUtensorMap* map, TmapKind kind, const void* ptr, uint64_t planes, uint64_t rows,
+               uint64_t cols, uint32_t box_rows) {
+  const TmapKey key{kind, ptr, planes, rows, cols, box_rows};
   {
     std::lock_guard<std::mutex> lock(g_tmap_mu);
     auto it = g_tmaps.find(key);
@@ -536,7 +674,7 @@ bool make_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t co
       return true;
     }
   }
-  if (!encode_tmap_f16(map, ptr, rows, cols, box_rows)) return false;
+  if (!encode_tmap(map, kind, ptr, planes, rows, cols, box_rows)) return false;
   std::lock_guard<std::mutex> lock(g_tmap_mu);
   if (g_tmaps.size() >= kTmapCacheMax) g_tmaps.clear();
   g_tmaps[key] = *map;
@@ -575,48 +713,54 @@ __global__ void __launch_bounds__(256) reduce_splits_scalar_kernel(const float* 
   }
 }
 
-// Tail mode: y of the tail tiles = sum over its S units' partial tiles (in unit order: the
-// result does not depend on timing), through the epilogue.  Four columns per thread.
-__global__ void __launch_bounds__(256) reduce_tail_kernel(const float* __restrict__ part, float* y,
-                                                          int M, int N, int mtiles, int main_tiles,
-                                                          int ntail, int S, const Epilogue epi) {
-  const int64_t n4 = static_cast<int64_t>(ntail) * BM * (BN / 4);
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int tt = static_cast<int>(i / (BM * (BN / 4)));
-    const int rem = static_cast<int>(i - static_cast<int64_t>(tt) * BM * (BN / 4));
-    const int row = rem / (BN / 4), col = 4 * (rem % (BN / 4));
-    const int tile = main_tiles + tt;
-    int m0, n0;
-    tile_origin(tile, mtiles, &m0, &n0);
+// Stream-K fix-up.  The stream-K region holds more tiles than there are runs, so every run
+// is longer than a tile, run boundaries are at least a tile apart, and a tile holds at most
+// one of them: a split tile has exactly two partials, the end of run j - 1 and the start of
+// run j.  CTA (j - 1, r) takes the boundary between runs j - 1 and j and, if that boundary
+// falls inside a tile, adds the tile's two partials (in that order: the result does not
+// depend on timing) for its rows [32 r, 32 r + 32) and stores them through the epilogue.
+constexpr int kFixRows = 32;
+__global__ void __launch_bounds__(256) reduce_sk_kernel(const float* __restrict__ part, float* y,
+                                                        int M, int N, int mtiles, int nwin, int G,
+                                                        int W, const Epilogue epi) {
+  const int j = static_cast<int>(blockIdx.x) + 1;
+  const int w = sk_start(j, W, G);
+  if (w % nwin == 0) return;  // on a tile boundary: both tiles were stored whole
+  const int ts = w / nwin;
+  const int s_lo = (sk_start(j - 1, W, G) / nwin == ts) ? 2 * (j - 1) : 2 * (j - 1) + 1;
+  const int s_hi = 2 * j;
+  int m0, n0;
+  tile_origin(ts, mtiles, &m0, &n0);
+  const float* lo = part + static_cast<int64_t>(s_lo) * BM * BN;
+  const float* hi = part + static_cast<int64_t>(s_hi) * BM * BN;
+#pragma unroll 4
+  for (int k = 0; k < kFixRows * (BN / 4) / 256; ++k) {
+    const int idx = k * 256 + static_cast<int>(threadIdx.x);
+    const int row = static_cast<int>(blockIdx.y) * kFixRows + idx / (BN / 4);
+    const int col = 4 * (idx % (BN / 4));
     const int m = m0 + row, n = n0 + col;
     if (m >= M || n >= N) continue;
-    const float* src = part + (static_cast<int64_t>(tt) * S * BM + row) * BN + col;
-    float4 a = *reinterpret_cast<const float4*>(src);
-    for (int s = 1; s < S; ++s) {
-      const float4 b = *reinterpret_cast<const float4*>(src + static_cast<int64_t>(s) * BM * BN);
-      a.x += b.x;
-      a.y += b.y;
-      a.z += b.z;
-      a.w += b.w;
-    }
+    const float4 a = *reinterpret_cast<const float4*>(lo + row * BN + col);
+    const float4 b = *reinterpret_cast<const float4*>(hi + row * BN + col);
+    const float4 v = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
     const int64_t o = static_cast<int64_t>(m) * N + n;
     if ((N & 3) == 0 && n + 4 <= N) {
       if (epi.plain())
-        *reinterpret_cast<float4*>(y + o) = a;
+        *reinterpret_cast<float4*>(y + o) = v;
       else
-        epi_put4(epi, y, o, epi_apply4(epi, a, epi_aux4(epi, o)));
+        epi_put4(epi, y, o, epi_apply4(epi, v, epi_aux4(epi, o)));
     } else {
-      const float v[4] = {a.x, a.y, a.z, a.w};
-      for (int c = 0; c < 4 && n + c < N; ++c) epi_store(epi, y, o + c, v[c]);
+      const float e[4] = {v.x, v.y, v.z, v.w};
+      for (int c = 0; c < 4 && n + c < N; ++c) epi_store(epi, y, o + c, e[c]);
     }
   }
 }
 
-template <bool kBS, bool kFused = false>
-cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
-                        cudaStream_t stream, int dev_id) {
-  auto fn = gemm_tc_kernel<kBS, kFused>;
+template <bool kBS, bool kFused = false, bool kSK = false>
+cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& yt,
+                        const CUtensorMap& pt, const GemmParams& p, int grid, cudaStream_t stream,
+                        int dev_id) {
+  auto fn = gemm_tc_kernel<kBS, kFused, kSK>;
   // setmaxnreg.inc waits until the registers exist: the split above is exact only if the
   // kernel was compiled for kLaunchRegs per thread.  Refuse to launch otherwise.
   int regs = 0;
@@ -625,7 +769,7 @@ cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const GemmPa
   if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   e = ensure_smem(reinterpret_cast<const void*>(fn), kSmemBytes, dev_id);
   if (e != cudaSuccess) return e;
-  fn<<<dim3(grid, p.splits), kThreads, kSmemBytes, stream>>>(a, b, p);
+  fn<<<dim3(grid, p.splits), kThreads, kSmemBytes, stream>>>(a, b, yt, pt, p);
   return cudaGetLastError();
 }
 
@@ -636,38 +780,48 @@ void forget_tensor_maps() {
   g_tmaps.clear();
 }
 
-// Tail mode: when the tiles fill some whole waves of the GPU plus a partial one, the
-// partial wave's tiles are split along K so that they spread over the idle SMs (at most
-// one range per scale window).  Returns the split (0: tail mode off).
-int gemm_tail_splits(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
-  if (M <= 0 || N <= 0 || K <= 0 || dev.sm_count <= 0) return 0;
+namespace {
+// How the output tiles are spread over the GPU's SMs (one CTA per SM at a time):
+//  - fewer tiles than SMs: every tile is split along K into `splits` ranges of whole scale
+//    windows, one CTA each (uniform split-K, partials [splits, M, N]);
+//  - a whole number of waves: one CTA per tile;
+//  - otherwise stream-K: the tiles of one full wave plus the partial one (sk_tiles, fewer
+//    than two waves) are shared out as equal runs of scale windows over one CTA per SM,
+//    launched first; the other waves' tiles (dp_tiles) follow as whole tiles.
+struct Schedule {
+  int splits = 1;
+  int64_t dp_tiles = 0;
+  int sk_ctas = 0;
+  int64_t sk_tiles = 0;
+  int64_t nwin = 0;
+};
+
+Schedule gemm_schedule(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+  Schedule sc;
+  if (M <= 0 || N <= 0 || K <= 0 || dev.sm_count <= 0) return sc;
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  if (tiles < dev.sm_count) return 0;  // one partial wave: uniform split-K instead
-  const int64_t tail = tiles % dev.sm_count;
-  if (tail == 0) return 0;
-  const int64_t nwin = (K / kQK + kWin - 1) / kWin;
-  int64_t s = dev.sm_count / tail;
-  if (s > nwin) s = nwin;
-  return s >= 2 ? static_cast<int>(s) : 0;
+  const int64_t G = dev.sm_count;
+  sc.nwin = (K / kQK + kWin - 1) / kWin;
+  sc.dp_tiles = tiles;
+  if (tiles < G) {
+    sc.splits = static_cast<int>(std::max<int64_t>(1, std::min(G / tiles, sc.nwin)));
+  } else if (tiles % G != 0) {
+    sc.sk_tiles = G + tiles % G;
+    sc.dp_tiles = tiles - sc.sk_tiles;
+    sc.sk_ctas = static_cast<int>(G);
+  }
+  return sc;
+}
+}  // namespace
+
+int gemm_splits(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+  return gemm_schedule(M, N, K, dev).splits;
 }
 
 size_t gemm_part_bytes(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
-  const int splits = gemm_splits(M, N, K, dev);
-  if (splits > 1) return static_cast<size_t>(splits) * M * N * 4;
-  const int S = gemm_tail_splits(M, N, K, dev);
-  if (S == 0) return 0;
-  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  return static_cast<size_t>(tiles % dev.sm_count) * S * BM * BN * 4;
-}
-
-int gemm_splits(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
-  if (M <= 0 || N <= 0 || K <= 0 || dev.sm_count <= 0) return 1;
-  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int64_t nwin = (K / kQK + kWin - 1) / kWin;
-  if (tiles >= dev.sm_count) return 1;
-  int64_t s = dev.sm_count / tiles;
-  if (s > nwin) s = nwin;
-  return s < 1 ? 1 : static_cast<int>(s);
+  const Schedule sc = gemm_schedule(M, N, K, dev);
+  if (sc.splits > 1) return static_cast<size_t>(sc.splits) * M * N * 4;
+  return static_cast<size_t>(2) * sc.sk_ctas * BM * BN * 4;
 }
 
 cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float* xd,
@@ -677,8 +831,8 @@ cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float
   if (M == 0 || N == 0) return cudaSuccess;
   if (K == 0) return cudaErrorInvalidValue;  // the API handles K == 0 without a launch
   CUtensorMap ta, tb;
-  if (!make_tmap_f16(&ta, A16, static_cast<uint64_t>(M), static_cast<uint64_t>(K), BM) ||
-      !make_tmap_f16(&tb, B16, static_cast<uint64_t>(N), static_cast<uint64_t>(K), BN))
+  if (!make_tmap(&ta, kTmapF16Operand, A16, 1, static_cast<uint64_t>(M), static_cast<uint64_t>(K), BM) ||
+      !make_tmap(&tb, kTmapF16Operand, B16, 1, static_cast<uint64_t>(N), static_cast<uint64_t>(K), BN))
     return cudaErrorInvalidValue;
   GemmParams p;
   p.xd = xd;
@@ -688,33 +842,53 @@ cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float
   if (isum != nullptr || splits < 1 || part == nullptr) splits = 1;  // block sums: one range
   p.splits = splits;
   p.part = splits > 1 ? part : nullptr;
-  // tail mode: needs the caller's partial buffer (sized by gemm_part_bytes); y only
+  // stream-K needs the caller's partial buffer (sized by gemm_part_bytes); y only
+  const Schedule sc = gemm_schedule(M, N, K, dev);
+  const bool sk = isum == nullptr && splits == 1 && part != nullptr && sc.sk_ctas > 0;
   const int64_t mtiles = (M + BM - 1) / BM;
   const int64_t tiles0 = mtiles * ((N + BN - 1) / BN);
-  const int S = (isum == nullptr && splits == 1 && part != nullptr) ? gemm_tail_splits(M, N, K, dev) : 0;
-  const int64_t ntail = S > 0 ? tiles0 % dev.sm_count : 0;
-  p.main_tiles = static_cast<int>(tiles0 - ntail);
-  p.tail_splits = S;
-  if (S > 0) p.part = part;
+  p.sk_ctas = sk ? sc.sk_ctas : 0;
+  p.sk_tiles = static_cast<int>(sk ? sc.sk_tiles : 0);
+  p.sk_windows = static_cast<int>(sk ? sc.sk_tiles * sc.nwin : 0);
+  if (sk) p.part = part;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.err = dev.err_word;
   p.epi = epi;
-  const int64_t tiles = tiles0 - ntail + ntail * S;  // whole tiles, then the tail's units
-  if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  if (isum) return launch_impl<true>(ta, tb, p, static_cast<int>(tiles), stream, dev.device);
+  // TMA stores: y (plain binary32 output) and the partial tiles, where the rows are 16-byte
+  // multiples on 16-byte aligned bases
+  CUtensorMap ty, tp;
+  std::memset(&ty, 0, sizeof(ty));
+  std::memset(&tp, 0, sizeof(tp));
+  const bool rows16 = (N % 4) == 0;
+  p.tma_y = isum == nullptr && splits == 1 && epi.plain() && rows16 &&
+            (reinterpret_cast<uintptr_t>(y) % 16) == 0 &&
+            make_tmap(&ty, kTmapF32Out, y, 1, static_cast<uint64_t>(M), static_cast<uint64_t>(N), 32);
+  const bool part_ok = part != nullptr && (reinterpret_cast<uintptr_t>(part) % 16) == 0;
+  if (sk)
+    p.tma_part = part_ok && make_tmap(&tp, kTmapF32Planes, part, 2 * static_cast<uint64_t>(sc.sk_ctas), BM, BN, 32);
+  else
+    p.tma_part = splits > 1 && part_ok && rows16 &&
+                 make_tmap(&tp, kTmapF32Planes, part, static_cast<uint64_t>(splits),
+                           static_cast<uint64_t>(M), static_cast<uint64_t>(N), 32);
+  const int64_t ctas = sk ? sc.dp_tiles + sc.sk_ctas : tiles0;
+  if (tiles0 > 0x7FFFFFFF || (sk && sc.sk_tiles * sc.nwin > 0x7FFFFFFF)) return cudaErrorInvalidValue;
+  if (isum) return launch_impl<true>(ta, tb, ty, tp, p, static_cast<int>(ctas), stream, dev.device);
   // the epilogue runs in the drain unless split-K partials take the reduce kernel's
-  cudaError_t e = (splits == 1 && !epi.plain())
-                      ? launch_impl<false, true>(ta, tb, p, static_cast<int>(tiles), stream, dev.device)
-                      : launch_impl<false>(ta, tb, p, static_cast<int>(tiles), stream, dev.device);
+  const int grid = static_cast<int>(ctas);
+  cudaError_t e;
+  if (splits == 1 && !epi.plain())
+    e = sk ? launch_impl<false, true, true>(ta, tb, ty, tp, p, grid, stream, dev.device)
+           : launch_impl<false, true, false>(ta, tb, ty, tp, p, grid, stream, dev.device);
+  else
+    e = sk ? launch_impl<false, false, true>(ta, tb, ty, tp, p, grid, stream, dev.device)
+           : launch_impl<false, false, false>(ta, tb, ty, tp, p, grid, stream, dev.device);
   if (e != cudaSuccess) return e;
-  if (S > 0) {
-    const int64_t n4 = ntail * BM * (BN / 4);
-    const int blocks = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, 4 * dev.sm_count));
-    reduce_tail_kernel<<<blocks, 256, 0, stream>>>(part, y, static_cast<int>(M), static_cast<int>(N),
-                                                   static_cast<int>(mtiles), p.main_tiles,
-                                                   static_cast<int>(ntail), S, epi);
+  if (sk && sc.sk_ctas > 1) {
+    reduce_sk_kernel<<<dim3(sc.sk_ctas - 1, BM / kFixRows), 256, 0, stream>>>(
+        part, y, static_cast<int>(M), static_cast<int>(N), static_cast<int>(mtiles),
+        static_cast<int>(sc.nwin), sc.sk_ctas, p.sk_windows, epi);
     return cudaGetLastError();
   }
   if (splits == 1) return e;

@@ -127,8 +127,8 @@ cudaError_t launch_bsa(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 // K ranges (of whole 16-block scale windows) the GEMM splits into when the output has fewer
 // 128 x 256 tiles than the GPU has SMs; 1 otherwise.
 int gemm_splits(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
-// Bytes of partial outputs launch_gemm_tc needs in `part` (uniform split-K, or the split
-// tail wave), 0 if none.
+// Bytes of partial outputs launch_gemm_tc needs in `part` (uniform split-K, or the stream-K
+// runs' partial tiles), 0 if none.
 size_t gemm_part_bytes(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
 // With splits > 1, part [splits, M, N] f32 receives the partial outputs and a second kernel
 // adds them (in a fixed order) into y.
