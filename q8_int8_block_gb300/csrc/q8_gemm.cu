@@ -47,6 +47,35 @@
 namespace q8 {
 namespace {
 
+// ---- TMA stores and named barriers (used by this file only) ------------------------
+// 2-D / 3-D tile store from shared memory, completed through the issuing thread's bulk
+// groups; the parts of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src,
+                                             int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* smem_src,
+                                             int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until this thread's committed bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;  // two Q8_0 blocks per pipeline stage (one 128-byte swizzle row)
@@ -404,15 +433,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const int nbw = min(nb - w * kWin, kWin);
-        if constexpr (kFused) {
-          // the last window: bring this thread's 128 aux values towards L2 for the epilogue
-          const Seg S = segs[sg];
-          int m0, n0;
-          tile_origin(S.tile, mtiles, &m0, &n0);
-          if (S.slot < 0 && p.splits == 1 && w + 1 == w1 && m0 + row < M)
-            epi_prefetch(p.epi, static_cast<int64_t>(m0 + row) * N + n0 + wg * 128,
-                         min(128, N - (n0 + wg * 128)));
-        }
 #pragma unroll 1
         for (int bb = 0; bb < nbw; ++bb, ++g) {
           const int blk = w * kWin + bb;  // block of the tile's K (block-sum output index)

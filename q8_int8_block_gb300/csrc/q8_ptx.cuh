@@ -123,11 +123,6 @@ __device__ __forceinline__ bool wg_barrier_any(int barrier_id, bool pred) {
   return out != 0;
 }
 
-// Named barrier over `count` threads (a multiple of 32), id 1..15 (0 is __syncthreads).
-__device__ __forceinline__ void named_barrier_sync(int barrier_id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(barrier_id), "r"(count) : "memory");
-}
-
 __device__ __forceinline__ void report_error(uint32_t* err_word, uint32_t bits,
                                              volatile int* abort_flag) {
   if (err_word != nullptr) atomicOr(err_word, bits);
@@ -149,38 +144,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
-}
-
-// 2-D tile store from shared memory, completed through the issuing thread's bulk groups;
-// the parts of the box outside the tensor are not written.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src,
-                                             int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
-               : "memory");
-}
-
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* smem_src,
-                                             int32_t x, int32_t y, int32_t z) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-
-// Waits until this thread's committed bulk stores have finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Waits until this thread's committed bulk stores have completed.
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Contiguous bulk copy: both addresses 16-byte aligned, bytes a multiple of 16.

@@ -192,11 +192,13 @@ def test_fused_gated_unit_full_size(q8, name, p):
     assert q8.q8_device_error() == 0
 
 
-@pytest.mark.parametrize("op,bf16", [("silu_mul", True), ("add", False)])
-def test_fused_epilogue_on_the_split_tail_wave(q8, op, bf16):
-    """154 tiles on the GPU's 152 SMs: whole tiles apply the epilogue in the GEMM drain, the
-    two tail tiles (split along K) in the tail reduction; both must match the oracle."""
-    M, N, K = 129, 19556, 544
+@pytest.mark.parametrize("op,bf16,M,N,K", [("silu_mul", True, 129, 19556, 544),
+                                           ("add", False, 129, 19556, 544),
+                                           ("silu_mul", True, 300, 26000, 544)])
+def test_fused_epilogue_on_stream_k(q8, op, bf16, M, N, K):
+    """Partial last waves (154 and 306 tiles on the GPU's 152 SMs): tiles that one CTA covers
+    whole apply the epilogue in the GEMM drain, tiles that two stream-K runs share in the
+    reduction of their partials; both must match the oracle."""
     rng = np.random.default_rng(77)
     W, x, xq_ref, xd_ref, Wq_ref, Wd_ref, aux = _inputs(rng, M, N, K, op)
     Wq, Wd = q8.q8_quantize_weights(T(W))
@@ -204,7 +206,7 @@ def test_fused_epilogue_on_the_split_tail_wave(q8, op, bf16):
     y = q8.q8_linear_fused(T(x), Wq, Wd, epi=op, aux=T(aux), out_dtype=out, path="tensor")
     ref = O.linear_epilogue(xq_ref, xd_ref, Wq_ref, Wd_ref, aux, op, out_bf16=bf16)
     if bf16:
-        assert_bf16_close(torch_bits(y), ref, f"tail {op} bf16")
+        assert_bf16_close(torch_bits(y), ref, f"stream-K {op} bf16")
     else:
-        assert_close(y.cpu().numpy(), ref, f"tail {op}")
+        assert_close(y.cpu().numpy(), ref, f"stream-K {op}")
     assert q8.q8_device_error() == 0

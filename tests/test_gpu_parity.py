@@ -317,12 +317,16 @@ def test_dp4a_path_full_size_prefill(q8):
     assert q8.q8_device_error() == 0
 
 
-@pytest.mark.parametrize("M,N,K", [(129, 19556, 544), (300, 20480, 1056)])
-def test_tensor_path_split_tail_wave(q8, M, N, K):
-    """Shapes whose tiles fill whole waves of the GPU plus a few: the tail tiles are split
-    along K and reduced separately.  (129, 19556): 154 tiles of 128 x 256, the tail holds
-    the last, ragged column tile at both row tiles (one of them a single row); K = 544 makes
-    the two K ranges 16 and 1 blocks.  Element by element, and deterministic."""
+@pytest.mark.parametrize("M,N,K", [(129, 19556, 544), (300, 20480, 1056), (129, 32768, 544),
+                                   (300, 26000, 544)])
+def test_tensor_path_stream_k(q8, M, N, K):
+    """Shapes whose 128 x 256 tiles fill a partial last wave of the GPU: the tiles of that wave
+    and one full wave are shared out as equal runs of scale windows, one per SM, and a run
+    that splits a tile stores a partial that a second kernel adds.  (129, 19556): 154 tiles,
+    the last, ragged column tile at both row tiles (one of them a single row); K = 544 is
+    17 blocks, two windows of 16 and 1 blocks.  (129, 32768): 256 tiles, runs of 3.4 windows
+    that touch up to three tiles.  (300, 26000): 306 tiles, runs over 154 of them followed by
+    152 whole tiles.  Element by element, and deterministic."""
     rng = np.random.default_rng(M + N)
     W = workloads.weights(rng, N, K)
     x, _ = workloads.activations(rng, M, K, bf16=True, outlier_frac=0.02)
@@ -333,5 +337,5 @@ def test_tensor_path_split_tail_wave(q8, M, N, K):
     y2 = q8.q8_linear_ex(T(x), Wq, Wd, path="tensor")
     torch.cuda.synchronize()
     assert torch.equal(y, y2)
-    assert_close(y.cpu().numpy(), y_ref, f"tensor tail M={M} N={N} K={K}")
+    assert_close(y.cpu().numpy(), y_ref, f"tensor stream-K M={M} N={N} K={K}")
     assert q8.q8_device_error() == 0

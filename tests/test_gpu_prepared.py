@@ -1,7 +1,7 @@
 """The prepared-weights path (q8_weights_to_f16 + q8_linear_prepared): the widened codes are
 the exact binary16 values of the int8 codes, and the layer gives the same bits as
 q8_linear_fused on the tensor-core path (the same kernels on the same values), with and
-without split-K, on the split tail wave, and with the fused neighbours; and matches the
+without split-K, on a stream-K partial wave, and with the fused neighbours; and matches the
 oracle within the layer tolerance."""
 import numpy as np
 import pytest
