@@ -118,7 +118,10 @@ q8_status resolve_path(int64_t M, int64_t N, int64_t K, q8_path req, const Devic
 
 // Scratch of the tensor path: A16 [M,K] f16 codes, xd [M,K/32] f32, B16 [N,K] f16 codes, and
 // the GEMM's partial outputs (split-K, or its stream-K partial tiles: gemm_part_bytes).
-// With prepared weights (q8_linear_prepared) the B16 region is not needed.
+// With prepared weights (q8_linear_prepared) the B16 region is not needed, nor up to
+// kInt8WeightsMaxM tokens, where the GEMM reads the int8 codes and widens them itself.
+constexpr int64_t kInt8WeightsMaxM = 128;
+bool tensor_widens(int64_t M, bool prepared) { return !prepared && M > kInt8WeightsMaxM; }
 size_t tensor_ws_bytes(int64_t M, int64_t N, int64_t K, size_t part_bytes, bool with_b16 = true) {
   return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(M) * (K / kQK) * 4) +
          (with_b16 ? align256(static_cast<size_t>(N) * K * 2) : 0) + align256(part_bytes);
@@ -239,7 +242,12 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
     }));
   const int splits = gemm_splits(M, N, K, dev);
   const size_t part_bytes = gemm_part_bytes(M, N, K, dev);
-  const bool with_b16 = B16_pre == nullptr;  // prepared weights need no widening scratch
+  // Up to one 128-token tile the GEMM reads each weight once: it takes the int8 codes and
+  // widens them in shared memory, in place of a separate pass that reads N K bytes and
+  // writes and re-reads 2 N K.  Larger M widens once per call (the in-GEMM widening costs
+  // more there than the pass).  Prepared weights need neither.
+  const bool b8 = B16_pre == nullptr && !tensor_widens(M, false);
+  const bool with_b16 = tensor_widens(M, B16_pre != nullptr);
   const size_t need = path_ws_bytes(p, M, N, K, part_bytes, with_b16);
   if (library_ws) {
     if ((st = library_workspace(dev, stream, need, &ws)) != Q8_OK) return st;
@@ -284,7 +292,8 @@ q8_status linear_impl(const void* x, q8_dtype xtype, const int8_t* Wq, const uin
   if (e == cudaSuccess && with_b16) e = launch_codes_to_f16(Wq, B16, N * K, dev, stream);
   if (e == cudaSuccess)
     e = timed_launch(stream, [&] {
-      return launch_gemm_tc(A16, B16, xd, Wd, y, nullptr, part, splits, M, N, K, dev, stream, epi);
+      return b8 ? launch_gemm_tc(A16, Wq, true, xd, Wd, y, nullptr, part, splits, M, N, K, dev, stream, epi)
+                : launch_gemm_tc(A16, B16, false, xd, Wd, y, nullptr, part, splits, M, N, K, dev, stream, epi);
     });
   return launch_status(e);
 }
@@ -496,7 +505,7 @@ size_t q8_linear_workspace_size(int64_t M, int64_t N, int64_t K, q8_path path) {
   if (current_device(&dev) != Q8_OK) return 0;
   q8_path p;
   if (resolve_path(M, N, K, path, dev, &p) != Q8_OK) return 0;
-  return path_ws_bytes(p, M, N, K, gemm_part_bytes(M, N, K, dev));
+  return path_ws_bytes(p, M, N, K, gemm_part_bytes(M, N, K, dev), tensor_widens(M, false));
 }
 
 q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64_t M, int64_t N,
@@ -534,7 +543,7 @@ q8_status q8_block_sums(const int8_t* xq, const int8_t* Wq, int32_t* isum, int64
   cudaError_t e = launch_codes_to_f16(xq, A16, M * K, dev, stream);
   if (e == cudaSuccess) e = launch_codes_to_f16(Wq, B16, N * K, dev, stream);
   if (e == cudaSuccess)
-    e = launch_gemm_tc(A16, B16, nullptr, nullptr, nullptr, isum, nullptr, 1, M, N, K, dev, stream);
+    e = launch_gemm_tc(A16, B16, false, nullptr, nullptr, nullptr, isum, nullptr, 1, M, N, K, dev, stream);
   return launch_status(e);
 }
 

@@ -100,6 +100,16 @@ constexpr uint32_t kWinDw = kWin * BN * 4;  // Wd of the tile's columns, f32   (
 constexpr uint32_t kWinDx = kWin * BM * 4;  // xd of the tile's rows, f32      (8 KB)
 constexpr size_t kSmemBytes = 1024 /*align*/ + kStages * (kStageA + kStageB) +
                               kWinSlots * (kWinDw + kWinDx);
+// int8-weight variant (kConv): the weight codes arrive by TMA as int8 ([256 rows][64 bytes]
+// per stage) and the scale warps widen them into a 2-slot ring of binary16 B tiles in the
+// MMA's layout.  A keeps its kStages ring.
+constexpr uint32_t kStageB8 = BN * BK;      // 16 KB of int8 codes
+constexpr int kFSlots = 2;                  // binary16 B tiles ready for the MMA
+constexpr size_t kSmemBytesConv = 1024 + kStages * (kStageA + kStageB8) + kFSlots * kStageB +
+                                  kWinSlots * (kWinDw + kWinDx);
+static_assert(kSmemBytesConv <= 232448, "shared memory per CTA (int8-weight variant)");
+static_assert(kDrainWarps * 32 * 128 * 4 <= kStages * (kStageA + kStageB8) + kFSlots * kStageB,
+              "output staging (int8-weight variant)");
 // The CTA's last results are staged in the operand ring, 16 KB per drain warp.
 static_assert(kDrainWarps * 32 * 128 * 4 <= kStages * (kStageA + kStageB), "output staging");
 
@@ -178,6 +188,26 @@ __device__ int cta_segments(const GemmParams& p, int nwin, Seg* seg) {
   return n;
 }
 
+// 16 int8 codes -> 16 binary16 values, exactly: a byte biased to u = q + 128 becomes the low
+// byte of the binary16 pattern 0x64uu, whose value is 1024 + u, and 1024 + u - 1152 = q.
+__device__ __forceinline__ void codes16_to_f16(uint4 in, uint4* lo, uint4* hi) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  uint32_t o[8];
+  const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t t = w[i] ^ 0x80808080u;
+    uint32_t a = __byte_perm(t, 0x64646464u, 0x5150);  // codes 0, 1 of the word
+    uint32_t b = __byte_perm(t, 0x64646464u, 0x5352);  // codes 2, 3
+    __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+    __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+    o[2 * i] = *reinterpret_cast<uint32_t*>(&ha);
+    o[2 * i + 1] = *reinterpret_cast<uint32_t*>(&hb);
+  }
+  *lo = make_uint4(o[0], o[1], o[2], o[3]);
+  *hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 // Fill one window of scales: Wd of the tile's 256 columns and xd of its 128 rows, blocks
 // [16 w, 16 w + 16) (zero past the ends), as f32 [block][column] and [block][row].
 __device__ __forceinline__ void stage_scales(const GemmParams& p, int w, int m0, int n0, int nb,
@@ -239,8 +269,9 @@ __device__ __forceinline__ void stage_scales(const GemmParams& p, int w, int m0,
 // kFused: the drain's final store applies the epilogue (residual, SiLU gate, bfloat16 y);
 // the plain layer is a separate instantiation so that it carries none of that code.
 // kSK: the launch has stream-K runs, whose CTAs walk several segments; without it every CTA
-// has exactly one, known at compile time.
-template <bool kBlockSums, bool kFused, bool kSK>
+// has exactly one, known at compile time.  kConv: B is given as the int8 weight codes
+// (tmB over Wq [N, K] bytes) and widened in shared memory by the scale warps.
+template <bool kBlockSums, bool kFused, bool kSK, bool kConv>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmP,
@@ -249,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2];
   __shared__ uint64_t sfull_bar[kWinSlots], sempty_bar[kWinSlots];
+  __shared__ uint64_t cfull_bar[kFSlots], cempty_bar[kFSlots];  // kConv: widened B tiles
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
   __shared__ Seg segs[kMaxSegs];
@@ -268,8 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023) & ~1023u) - raw);
   uint8_t* sA = base;
-  uint8_t* sB = base + kStages * kStageA;
-  float* sW = reinterpret_cast<float*>(sB + kStages * kStageB);  // [slot][kWin][BN]
+  uint8_t* sB = base + kStages * kStageA;  // kConv: the int8 tiles, [stage][BN][BK bytes]
+  uint8_t* sF = sB + kStages * kStageB8;   // kConv: the widened binary16 tiles
+  float* sW = reinterpret_cast<float*>(kConv ? sF + kFSlots * kStageB
+                                             : sB + kStages * kStageB);  // [slot][kWin][BN]
   float* sX = sW + kWinSlots * kWin * BN;                          // [slot][kWin][BM]
 
   if (threadIdx.x == 0) {
@@ -277,7 +311,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     nseg_s = cta_segments(p, nwin, segs);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      // kConv: a stage is free once the MMA has read A (commit) and both scale warps have
+      // read the int8 codes
+      mbar_init(&empty_bar[s], kConv ? 3 : 1);
+    }
+    if constexpr (kConv) {
+      for (int f = 0; f < kFSlots; ++f) {
+        mbar_init(&cfull_bar[f], 2);
+        mbar_init(&cempty_bar[f], 1);
+      }
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
@@ -317,9 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full_bar[s], kStageA + kStageB);
+            mbar_arrive_expect_tx(&full_bar[s], kStageA + (kConv ? kStageB8 : kStageB));
             tma_load_2d(sA + s * kStageA, &tmA, &full_bar[s], kb * BK, m0);
-            tma_load_2d(sB + s * kStageB, &tmB, &full_bar[s], kb * BK, n0);
+            tma_load_2d(sB + s * (kConv ? kStageB8 : kStageB), &tmB, &full_bar[s], kb * BK, n0);
             ++issued;
           }
         }
@@ -347,9 +389,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
+            const int f = i % kFSlots;
+            if constexpr (kConv) {
+              if (!mbar_wait(&cfull_bar[f], (i / kFSlots) & 1, &abort_flag)) {
+                report_error(p.err, kErrWaitTimeout, &abort_flag);
+                ok = false;
+                break;
+              }
+            }
             tc_fence_after();
             const uint32_t a0 = smem_u32(sA + s * kStageA);
-            const uint32_t b0 = smem_u32(sB + s * kStageB);
+            const uint32_t b0 = kConv ? smem_u32(sF + f * kStageB) : smem_u32(sB + s * kStageB);
             const int nblk = min(b_end - 2 * kb, 2);
             for (int j = 0; j < nblk; ++j, ++g) {
               const int buf = g & 1;
@@ -369,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_commit(&tfull_bar[buf]);
             }
             mma_commit(&empty_bar[s]);
+            if constexpr (kConv) mma_commit(&cempty_bar[f]);
             last_stage = i;
           }
         }
@@ -380,13 +431,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if constexpr (!kBlockSums) {
       // ------------------------------- scale producer (warps 2-3) ---------------------
       const int t = threadIdx.x - 64;  // 0..63
-      int u = 0;  // windows staged, all segments
+      int u = 0;   // windows staged, all segments
+      int ci = 0;  // kConv: stages widened, all segments
       bool ok = true;
       for (int sg = 0; sg < nseg && ok; ++sg) {
         const Seg S = segs[sg];
         int m0, n0;
         tile_origin(S.tile, mtiles, &m0, &n0);
-        for (int w = S.w0; w < S.w1; ++w, ++u) {
+        for (int w = S.w0; w < S.w1 && ok; ++w, ++u) {
           const int slot = u % kWinSlots;
           if (!mbar_wait(&sempty_bar[slot], ((u / kWinSlots) & 1) ^ 1, &abort_flag)) {
             report_error(p.err, kErrWaitTimeout, &abort_flag);
@@ -395,6 +447,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           stage_scales(p, w, m0, n0, nb, sW + slot * kWin * BN, sX + slot * kWin * BM, t);
           mbar_arrive(&sfull_bar[slot]);  // release: the stores above are visible to waiters
+          if constexpr (kConv) {
+            // Widen the window's stages of int8 weight codes into binary16 B tiles in the
+            // MMA's 128-byte swizzled layout (row r at 128 r, 16-byte chunk j at j ^ (r % 8)).
+            // Thread t takes 16-byte chunk t % 4 of rows t / 4, t / 4 + 16, ...: the 8 threads
+            // of a quarter warp read 128 contiguous bytes and write 8 distinct bank groups.
+            const int kb_end = min((w + 1) * (kWin / 2), (min(S.w1 * kWin, nb) + 1) / 2);
+            for (int kb = w * (kWin / 2); kb < kb_end; ++kb, ++ci) {
+              const int s8 = ci % kStages, f = ci % kFSlots;
+              if (!mbar_wait(&full_bar[s8], (ci / kStages) & 1, &abort_flag) ||
+                  !mbar_wait(&cempty_bar[f], ((ci / kFSlots) & 1) ^ 1, &abort_flag)) {
+                report_error(p.err, kErrWaitTimeout, &abort_flag);
+                ok = false;
+                break;
+              }
+              const uint8_t* src = sB + s8 * kStageB8;
+              uint8_t* dst = sF + f * kStageB;
+              const int c = t & 3;
+#pragma unroll 2
+              for (int r = t >> 2; r < BN; r += kScaleThreads / 4) {
+                uint4 lo, hi;
+                codes16_to_f16(*reinterpret_cast<const uint4*>(src + r * BK + c * 16), &lo, &hi);
+                *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c) ^ (r & 7)) * 16)) = lo;
+                *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c + 1) ^ (r & 7)) * 16)) = hi;
+              }
+              fence_proxy_async_smem();  // the tensor core reads these stores
+              __syncwarp();
+              if (lane == 0) {
+                mbar_arrive(&cfull_bar[f]);
+                mbar_arrive(&empty_bar[s8]);  // the int8 codes of the stage are read
+              }
+            }
+          }
         }
       }
     }
@@ -641,24 +725,29 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// The kinds of tensor map the GEMM uses, all [planes][rows][cols] with cols contiguous and the
-// 128-byte swizzle: the binary16 operands (2-D, box box_rows x 64 columns) and the binary32
-// outputs the drain stores from its staged boxes (box 32 x 32: y 2-D, partial tiles 3-D).
-enum TmapKind : uint32_t { kTmapF16Operand = 0, kTmapF32Out = 1, kTmapF32Planes = 2 };
+// The kinds of tensor map the GEMM uses, all [planes][rows][cols] with cols contiguous: the
+// binary16 operands (2-D, box box_rows x 64 columns, 128-byte swizzle), the int8 weight codes
+// (2-D, box box_rows x 64 bytes, unswizzled: the widening warps read them in row order), and
+// the binary32 outputs the drain stores from its staged boxes (box 32 x 32, 128-byte swizzle:
+// y 2-D, partial tiles 3-D).
+enum TmapKind : uint32_t { kTmapF16Operand = 0, kTmapF32Out = 1, kTmapF32Planes = 2, kTmapU8Operand = 3 };
 
 bool encode_tmap(CUtensorMap* map, TmapKind kind, const void* ptr, uint64_t planes, uint64_t rows,
                  uint64_t cols, uint32_t box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
-  const bool f16 = kind == kTmapF16Operand;
-  const uint64_t esz = f16 ? 2 : 4;
+  const bool operand = kind == kTmapF16Operand || kind == kTmapU8Operand;
+  const uint64_t esz = kind == kTmapU8Operand ? 1 : kind == kTmapF16Operand ? 2 : 4;
   const cuuint64_t dims[3] = {cols, rows, planes};
   const cuuint64_t strides[2] = {cols * esz, rows * cols * esz};
-  const cuuint32_t box[3] = {f16 ? static_cast<cuuint32_t>(BK) : 32u, box_rows, 1u};
+  const cuuint32_t box[3] = {operand ? static_cast<cuuint32_t>(BK) : 32u, box_rows, 1u};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-             kind == kTmapF32Planes ? 3 : 2, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUtensorMapDataType dt = kind == kTmapU8Operand    ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : kind == kTmapF16Operand ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  return enc(map, dt, kind == kTmapF32Planes ? 3 : 2, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             kind == kTmapU8Operand ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -776,20 +865,21 @@ __global__ void __launch_bounds__(256) reduce_sk_kernel(const float* __restrict_
   }
 }
 
-template <bool kBS, bool kFused = false, bool kSK = false>
+template <bool kBS, bool kFused = false, bool kSK = false, bool kConv = false>
 cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& yt,
                         const CUtensorMap& pt, const GemmParams& p, int grid, cudaStream_t stream,
                         int dev_id) {
-  auto fn = gemm_tc_kernel<kBS, kFused, kSK>;
+  auto fn = gemm_tc_kernel<kBS, kFused, kSK, kConv>;
+  constexpr size_t smem = kConv ? kSmemBytesConv : kSmemBytes;
   // setmaxnreg.inc waits until the registers exist: the split above is exact only if the
   // kernel was compiled for kLaunchRegs per thread.  Refuse to launch otherwise.
   int regs = 0;
   cudaError_t e = kernel_regs(reinterpret_cast<const void*>(fn), dev_id, &regs);
   if (e != cudaSuccess) return e;
   if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = ensure_smem(reinterpret_cast<const void*>(fn), kSmemBytes, dev_id);
+  e = ensure_smem(reinterpret_cast<const void*>(fn), smem, dev_id);
   if (e != cudaSuccess) return e;
-  fn<<<dim3(grid, p.splits), kThreads, kSmemBytes, stream>>>(a, b, yt, pt, p);
+  fn<<<dim3(grid, p.splits), kThreads, smem, stream>>>(a, b, yt, pt, p);
   return cudaGetLastError();
 }
 
@@ -844,15 +934,17 @@ size_t gemm_part_bytes(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
   return static_cast<size_t>(2) * sc.sk_ctas * BM * BN * 4;
 }
 
-cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float* xd,
+cudaError_t launch_gemm_tc(const uint16_t* A16, const void* B, bool b_int8, const float* xd,
                            const uint16_t* Wd, float* y, int32_t* isum, float* part, int splits,
                            int64_t M, int64_t N, int64_t K, const DeviceInfo& dev,
                            cudaStream_t stream, const Epilogue& epi) {
   if (M == 0 || N == 0) return cudaSuccess;
   if (K == 0) return cudaErrorInvalidValue;  // the API handles K == 0 without a launch
+  if (b_int8 && isum != nullptr) return cudaErrorInvalidValue;  // block sums: binary16 B only
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, kTmapF16Operand, A16, 1, static_cast<uint64_t>(M), static_cast<uint64_t>(K), BM) ||
-      !make_tmap(&tb, kTmapF16Operand, B16, 1, static_cast<uint64_t>(N), static_cast<uint64_t>(K), BN))
+      !make_tmap(&tb, b_int8 ? kTmapU8Operand : kTmapF16Operand, B, 1, static_cast<uint64_t>(N),
+                 static_cast<uint64_t>(K), BN))
     return cudaErrorInvalidValue;
   GemmParams p;
   p.xd = xd;
@@ -899,11 +991,15 @@ cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float
   const int grid = static_cast<int>(ctas);
   cudaError_t e;
   if (splits == 1 && !epi.plain())
-    e = sk ? launch_impl<false, true, true>(ta, tb, ty, tp, p, grid, stream, dev.device)
-           : launch_impl<false, true, false>(ta, tb, ty, tp, p, grid, stream, dev.device);
+    e = b_int8 ? (sk ? launch_impl<false, true, true, true>(ta, tb, ty, tp, p, grid, stream, dev.device)
+                     : launch_impl<false, true, false, true>(ta, tb, ty, tp, p, grid, stream, dev.device))
+               : (sk ? launch_impl<false, true, true>(ta, tb, ty, tp, p, grid, stream, dev.device)
+                     : launch_impl<false, true, false>(ta, tb, ty, tp, p, grid, stream, dev.device));
   else
-    e = sk ? launch_impl<false, false, true>(ta, tb, ty, tp, p, grid, stream, dev.device)
-           : launch_impl<false, false, false>(ta, tb, ty, tp, p, grid, stream, dev.device);
+    e = b_int8 ? (sk ? launch_impl<false, false, true, true>(ta, tb, ty, tp, p, grid, stream, dev.device)
+                     : launch_impl<false, false, false, true>(ta, tb, ty, tp, p, grid, stream, dev.device))
+               : (sk ? launch_impl<false, false, true>(ta, tb, ty, tp, p, grid, stream, dev.device)
+                     : launch_impl<false, false, false>(ta, tb, ty, tp, p, grid, stream, dev.device));
   if (e != cudaSuccess) return e;
   if (sk && sc.sk_ctas > 1) {
     reduce_sk_kernel<<<dim3(sc.sk_ctas - 1, BM / kFixRows), 256, 0, stream>>>(

@@ -131,8 +131,9 @@ int gemm_splits(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
 // runs' partial tiles), 0 if none.
 size_t gemm_part_bytes(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
 // With splits > 1, part [splits, M, N] f32 receives the partial outputs and a second kernel
-// adds them (in a fixed order) into y.
-cudaError_t launch_gemm_tc(const uint16_t* A16, const uint16_t* B16, const float* xd,
+// adds them (in a fixed order) into y.  B is the weight codes [N, K]: binary16 (B16), or with
+// b_int8 the int8 codes themselves (widened inside the GEMM; not with isum).
+cudaError_t launch_gemm_tc(const uint16_t* A16, const void* B, bool b_int8, const float* xd,
                            const uint16_t* Wd, float* y, int32_t* isum, float* part, int splits,
                            int64_t M, int64_t N, int64_t K, const DeviceInfo& dev,
                            cudaStream_t stream, const Epilogue& epi = Epilogue());

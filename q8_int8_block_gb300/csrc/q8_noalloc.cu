@@ -87,6 +87,6 @@ extern "C" q8_status q8_linear_noalloc(const void* x, q8_dtype xtype, const int8
                                               up256(static_cast<size_t>(M) * (K / kQK) * 4));
   e = launch_quantize(x, static_cast<int>(xtype), A16, true, xd, false, M, K, di, stream);
   if (e == cudaSuccess) e = launch_codes_to_f16(Wq, B16, N * K, di, stream);
-  if (e == cudaSuccess) e = launch_gemm_tc(A16, B16, xd, Wd, y, nullptr, nullptr, 1, M, N, K, di, stream);
+  if (e == cudaSuccess) e = launch_gemm_tc(A16, B16, false, xd, Wd, y, nullptr, nullptr, 1, M, N, K, di, stream);
   return e == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
 }

@@ -339,3 +339,26 @@ def test_tensor_path_stream_k(q8, M, N, K):
     assert torch.equal(y, y2)
     assert_close(y.cpu().numpy(), y_ref, f"tensor stream-K M={M} N={N} K={K}")
     assert q8.q8_device_error() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 544), (77, 1000, 544), (128, 4096, 4096),
+                                   (128, 19556, 1056), (100, 300, 512)])
+def test_tensor_path_int8_weights(q8, M, N, K):
+    """Up to 128 tokens the tensor path's GEMM reads the int8 weight codes by TMA and widens
+    them to binary16 in shared memory itself (no separate widening pass): the results are
+    the bits of the binary16 path on the same codes (the prepared-weights entry point) and
+    match the oracle.  Ragged N, K of 17 and 33 blocks (a last stage with one block), and
+    uniform split-K along K (4096 x 4096 and 19556 x 1056 at M = 128: 16 and 77 tiles)."""
+    rng = np.random.default_rng(M * 7 + N + K)
+    W = workloads.weights(rng, N, K)
+    x, _ = workloads.activations(rng, M, K, bf16=True, outlier_frac=0.02)
+    Wq_ref, Wd_ref = O.quantize_weights(W)
+    y_ref = O.linear(x, Wq_ref, Wd_ref, bf16=True)
+    Wq, Wd = q8.q8_quantize_weights(T(W))
+    xt = T(x)
+    y = q8.q8_linear_ex(xt, Wq, Wd, path="tensor")
+    yp = q8.q8_linear_prepared(xt, q8.q8_weights_to_f16(Wq), Wd)
+    torch.cuda.synchronize()
+    assert torch.equal(y, yp)
+    assert_close(y.cpu().numpy(), y_ref, f"tensor int8 weights M={M} N={N} K={K}")
+    assert q8.q8_device_error() == 0
