@@ -66,6 +66,14 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
                : "memory");
 }
 
+// Brings a whole 2-D box of the tensor towards L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -140,6 +148,8 @@ struct GemmParams {
   int32_t* isum;       // [M, N, nb] (block-sum mode)
   int M, N, K;
   int tma_y;           // whole-K tiles are stored through tmY (binary32 y, box 32 x 32)
+  int tma_aux;         // fused epilogue: tmP maps aux (box 128 rows x 256 columns), prefetched
+                       // to L2 while a whole tile's last window is loaded
   int tma_part;        // partial tiles are stored through tmP (binary32, 3-D, box 32 x 32 x 1):
                        // stream-K [2 sk_ctas][BM][BN] at (column, row, slot), split-K
                        // [splits][M][N] at (n, m, split)
@@ -353,6 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tile_origin(S.tile, mtiles, &m0, &n0);
           const int kb_end = (min(S.w1 * kWin, nb) + 1) / 2;
           for (int kb = S.w0 * (kWin / 2); kb < kb_end; ++kb) {
+            if constexpr (kFused) {
+              // the epilogue's aux tile, towards L2 a window ahead of its use
+              if (p.tma_aux && S.slot < 0 && kb == (S.w1 - 1) * (kWin / 2)) tma_prefetch_l2_2d(&tmP, n0, m0);
+            }
             const int s = issued % kStages;
             if (!mbar_wait(&empty_bar[s], ((issued / kStages) & 1) ^ 1, &abort_flag)) {
               report_error(p.err, kErrWaitTimeout, &abort_flag);
@@ -727,10 +741,12 @@ EncodeTiledFn get_encode_fn() {
 
 // The kinds of tensor map the GEMM uses, all [planes][rows][cols] with cols contiguous: the
 // binary16 operands (2-D, box box_rows x 64 columns, 128-byte swizzle), the int8 weight codes
-// (2-D, box box_rows x 64 bytes, unswizzled: the widening warps read them in row order), and
-// the binary32 outputs the drain stores from its staged boxes (box 32 x 32, 128-byte swizzle:
-// y 2-D, partial tiles 3-D).
-enum TmapKind : uint32_t { kTmapF16Operand = 0, kTmapF32Out = 1, kTmapF32Planes = 2, kTmapU8Operand = 3 };
+// (2-D, box box_rows x 64 bytes, unswizzled: the widening warps read them in row order), the
+// binary32 outputs the drain stores from its staged boxes (box 32 x 32, 128-byte swizzle:
+// y 2-D, partial tiles 3-D), and the fused epilogue's aux (2-D, a whole 128 x 256 tile,
+// unswizzled, only ever prefetched to L2).
+enum TmapKind : uint32_t { kTmapF16Operand = 0, kTmapF32Out = 1, kTmapF32Planes = 2, kTmapU8Operand = 3,
+                          kTmapF32Tile = 4 };
 
 bool encode_tmap(CUtensorMap* map, TmapKind kind, const void* ptr, uint64_t planes, uint64_t rows,
                  uint64_t cols, uint32_t box_rows) {
@@ -740,14 +756,16 @@ bool encode_tmap(CUtensorMap* map, TmapKind kind, const void* ptr, uint64_t plan
   const uint64_t esz = kind == kTmapU8Operand ? 1 : kind == kTmapF16Operand ? 2 : 4;
   const cuuint64_t dims[3] = {cols, rows, planes};
   const cuuint64_t strides[2] = {cols * esz, rows * cols * esz};
-  const cuuint32_t box[3] = {operand ? static_cast<cuuint32_t>(BK) : 32u, box_rows, 1u};
+  const cuuint32_t box[3] = {operand ? static_cast<cuuint32_t>(BK) : kind == kTmapF32Tile ? static_cast<cuuint32_t>(BN) : 32u,
+                             box_rows, 1u};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = kind == kTmapU8Operand    ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                  : kind == kTmapF16Operand ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   return enc(map, dt, kind == kTmapF32Planes ? 3 : 2, const_cast<void*>(ptr), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             kind == kTmapU8Operand ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+             (kind == kTmapU8Operand || kind == kTmapF32Tile) ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                                              : CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -978,7 +996,13 @@ cudaError_t launch_gemm_tc(const uint16_t* A16, const void* B, bool b_int8, cons
             (reinterpret_cast<uintptr_t>(y) % 16) == 0 &&
             make_tmap(&ty, kTmapF32Out, y, 1, static_cast<uint64_t>(M), static_cast<uint64_t>(N), 32);
   const bool part_ok = part != nullptr && (reinterpret_cast<uintptr_t>(part) % 16) == 0;
-  if (sk)
+  p.tma_aux = 0;
+  if (!epi.plain() && splits == 1 && isum == nullptr) {
+    // the fused kernel: tmP maps aux instead (its partial tiles are never stored by TMA)
+    p.tma_part = 0;
+    p.tma_aux = epi.aux != nullptr && rows16 && (reinterpret_cast<uintptr_t>(epi.aux) % 16) == 0 &&
+                make_tmap(&tp, kTmapF32Tile, epi.aux, 1, static_cast<uint64_t>(M), static_cast<uint64_t>(N), BM);
+  } else if (sk)
     p.tma_part = part_ok && make_tmap(&tp, kTmapF32Planes, part, 2 * static_cast<uint64_t>(sc.sk_ctas), BM, BN, 32);
   else
     p.tma_part = splits > 1 && part_ok && rows16 &&
