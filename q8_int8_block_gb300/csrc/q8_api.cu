@@ -91,7 +91,9 @@ q8_status resolve_path(int64_t M, int64_t N, int64_t K, q8_path req, const Devic
   const bool batch_ok = batch_supported(M < 1 ? 1 : M, N < 1 ? 1 : N, K, dev);
   switch (req) {
     case Q8_PATH_AUTO:
-      if (M <= 1 && decode_ok) *out = Q8_PATH_DECODE;
+      // the decode kernel (one dp4a per 4 MACs and token) streams faster than the batched
+      // mma.sync kernel up to 2 tokens (measured on the 9B and sweep shapes)
+      if (M <= 2 && decode_ok) *out = Q8_PATH_DECODE;
       else if (batch_ok) *out = Q8_PATH_BATCH;
       else if (decode_ok) *out = Q8_PATH_DECODE;
       else *out = Q8_PATH_TENSOR;
