@@ -18,10 +18,12 @@
 //
 // Design (one CTA per 16 * RG weight rows, 1 producer warp + 15 consumer warps, so that
 // 16 warps with up to 128 registers each fill an SM):
-//   * the CTA's weight rows stream through a ring of 256-wide K chunks: two TMA boxes of
-//     16 RG rows x 128 int8 codes with 128-byte swizzle (so ldmatrix reads them without
-//     bank conflicts), one box of the rows' 8 binary16 scales, and the chunk's activation
-//     codes and scales by bulk copies;
+//   * the CTA's weight rows stream through a ring of K chunks, 512 wide where K and the ring
+//     allow (else 256): one TMA box of 16 RG rows x 128 int8 codes per 4 blocks, with
+//     128-byte swizzle (so ldmatrix reads them without bank conflicts), one box of the
+//     rows' binary16 scales, and the chunk's activation codes and scales by bulk copies.
+//     A chunk costs the consumers a fixed latency besides its work (measured: ~0.5 us per
+//     256-wide chunk at M = 4), which the wider chunk spreads over twice the weights;
 //   * the activations arrive from quantize_batch_kernel in a fragment-ordered layout,
 //     xb[b][t][32] binary16 (for each 16-byte piece c: K 4c..4c+3 then K 16+4c..16+4c+3)
 //     and xbd[b][t] binary32, tokens padded with zeros to whole groups of 8, so each lane's
@@ -54,8 +56,12 @@
 namespace q8 {
 namespace {
 
-constexpr int kChunkK = 256;                 // K per stage
+// K per stage: 512 (16 Q8_0 blocks) where K allows, else 256.  A chunk costs the consumer
+// warps a fixed latency (their dependent chains of shared-memory loads, widening, MMAs and
+// rescale) besides its work, so the wider chunk halves that cost per weight byte.
+constexpr int kChunkK = 256;                 // the narrow chunk: K % 256 == 0 is required
 constexpr int kChunkBlocks = kChunkK / kQK;  // 8 Q8_0 blocks
+constexpr int kMaxChunkBlocks = 16;
 constexpr int kConsumerWarps = 15;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxRG = kConsumerWarps;       // every row group needs a warp (16 * RG <= 256 rows)
@@ -74,8 +80,9 @@ struct BatchParams {
   int RG;               // row groups of 16 per CTA
   int KPall;            // partial-sum layers (block splits) of the busiest row group
   int stages;
+  int cb;               // Q8_0 blocks per chunk (8 or 16)
   uint32_t stage_bytes;
-  uint32_t off_w1, off_wd, off_x, off_xd;  // offsets inside a stage
+  uint32_t off_w1, off_wd, off_x, off_xd;  // offsets inside a stage (off_w1: one 128-byte weight box)
   uint32_t* err;
   Epilogue epi;         // fused output step
 };
@@ -153,14 +160,16 @@ __global__ void __maxnreg__(kMaxRegs)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = p.M, N = p.N, K = p.K, RG = p.RG, S = p.stages;
   const int nb = K / kQK;
-  const int nchunks = K / kChunkK;
+  const int cbk = p.cb;           // blocks per chunk
+  const int nchunks = cbk > 0 ? K / (kQK * cbk) : 0;
   const int rows = 16 * RG;
   const int row0 = blockIdx.x * rows;
   const int TG = (M + 7) >> 3;
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw + 1023) & ~1023u) - raw);
 
-  if (S > kMaxStages || S < 2 || RG < 1 || RG > kMaxRG || M < 1 || M > kBatchMaxM) {
+  if (S > kMaxStages || S < 2 || RG < 1 || RG > kMaxRG || M < 1 || M > kBatchMaxM ||
+      (cbk != kChunkBlocks && cbk != kMaxChunkBlocks)) {
     if (threadIdx.x == 0) report_error(p.err, kErrBadLaunch, nullptr);  // the launcher never does this
     return;
   }
@@ -176,8 +185,8 @@ __global__ void __maxnreg__(kMaxRegs)
   }
   __syncthreads();
 
-  const uint32_t wbytes = static_cast<uint32_t>(rows) * (2 * 128 + kChunkBlocks * 2);
-  const uint32_t xbytes = static_cast<uint32_t>(kChunkBlocks * 8 * TG) * (64 + 4);
+  const uint32_t wbytes = static_cast<uint32_t>(rows) * (kQK * cbk + cbk * 2);
+  const uint32_t xbytes = static_cast<uint32_t>(cbk * 8 * TG) * (64 + 4);
 
   if (warp == 0) {
     // ---------------- producer ---------------------------------------------------------
@@ -185,16 +194,16 @@ __global__ void __maxnreg__(kMaxRegs)
       auto load_w = [&](int st) {
         uint8_t* stg = ring + static_cast<size_t>(st % S) * p.stage_bytes;
         uint64_t* bar = &full_bar[st % S];
-        tma_load_2d(stg, &tmW, bar, st * kChunkK, row0);
-        tma_load_2d(stg + p.off_w1, &tmW, bar, st * kChunkK + 128, row0);
-        tma_load_2d(stg + p.off_wd, &tmS, bar, st * kChunkBlocks, row0);
+        for (int bx = 0; bx < cbk / 4; ++bx)  // 128-byte boxes of 4 blocks
+          tma_load_2d(stg + bx * p.off_w1, &tmW, bar, st * kQK * cbk + 128 * bx, row0);
+        tma_load_2d(stg + p.off_wd, &tmS, bar, st * cbk, row0);
       };
       auto load_x = [&](int st) {
         uint8_t* stg = ring + static_cast<size_t>(st % S) * p.stage_bytes;
         uint64_t* bar = &full_bar[st % S];
-        const size_t blk0 = static_cast<size_t>(st) * kChunkBlocks * (8 * TG);
-        bulk_load(stg + p.off_x, p.xb + blk0 * 32, static_cast<uint32_t>(kChunkBlocks * 8 * TG) * 64, bar);
-        bulk_load(stg + p.off_xd, p.xbd + blk0, static_cast<uint32_t>(kChunkBlocks * 8 * TG) * 4, bar);
+        const size_t blk0 = static_cast<size_t>(st) * cbk * (8 * TG);
+        bulk_load(stg + p.off_x, p.xb + blk0 * 32, static_cast<uint32_t>(cbk * 8 * TG) * 64, bar);
+        bulk_load(stg + p.off_xd, p.xbd + blk0, static_cast<uint32_t>(cbk * 8 * TG) * 4, bar);
       };
       // weights of the first stages before waiting for the previous kernel, activations after
       const int pre = nchunks < S ? nchunks : S;
@@ -246,7 +255,7 @@ __global__ void __maxnreg__(kMaxRegs)
       ntg = (TG - idx + nw - 1) / nw;
     } else {
       KP = nw / TG;
-      if (KP > kChunkBlocks) KP = kChunkBlocks;
+      if (KP > cbk) KP = cbk;
       tg0 = idx % TG;
       tgstep = TG;
       kp = idx / TG;
@@ -271,7 +280,7 @@ __global__ void __maxnreg__(kMaxRegs)
     const uint32_t x_lane = static_cast<uint32_t>(p.off_x + g * 64 + 16 * c);
     const uint32_t x_block = static_cast<uint32_t>(TP * 64);
     const uint32_t dx_lane = static_cast<uint32_t>(p.off_xd + 8 * c);
-    const uint32_t wd_lane = static_cast<uint32_t>(p.off_wd + (16 * rg + g) * kChunkBlocks * 2);
+    const uint32_t wd_lane = static_cast<uint32_t>(p.off_wd + (16 * rg + g) * cbk * 2);
     int s = 0;
     uint32_t phase = 0;  // slot s and parity of stage st, kept without divisions
     for (int st = 0; st < nchunks && !failed; ++st, s = (s + 1 == S ? 0 : s + 1), phase ^= (s == 0)) {
@@ -288,7 +297,7 @@ __global__ void __maxnreg__(kMaxRegs)
       if (ntg > 0) {
         // this warp's blocks of the chunk: kp, kp + KP, ...; two at a time, so that the
         // shared-memory loads and MMAs of both are in flight together
-        const int nmine = (kChunkBlocks - kp + KP - 1) / KP;
+        const int nmine = (cbk - kp + KP - 1) / KP;
         // kGB of this warp's blocks at a time: all their shared-memory loads and MMAs are
         // issued before any result is used (the chains are long-latency: ldmatrix, MMA, FMA);
         // slots past the last block repeat it and are not accumulated
@@ -302,7 +311,7 @@ __global__ void __maxnreg__(kMaxRegs)
           for (int k = 0; k < kGB; ++k) {
             const int bp = bps[k];
             const uint32_t chunk = static_cast<uint32_t>(2 * (bp & 3) + (mi >> 1));
-            ldmatrix_x4(stg32 + ((bp >> 2) ? p.off_w1 : 0u) + a_lane + ((chunk ^ lr) << 4), wa[k][0],
+            ldmatrix_x4(stg32 + static_cast<uint32_t>(bp >> 2) * p.off_w1 + a_lane + ((chunk ^ lr) << 4), wa[k][0],
                         wa[k][1], wa[k][2], wa[k][3]);
           }
           float dw0[kGB], dw1[kGB];  // Wd of rows g and g + 8
@@ -312,7 +321,7 @@ __global__ void __maxnreg__(kMaxRegs)
             if constexpr (!kBlockSums) {
               const uint32_t wda = stg32 + wd_lane + 2 * bps[k];
               dw0[k] = lds_f16(wda);
-              dw1[k] = lds_f16(wda + 8 * kChunkBlocks * 2);
+              dw1[k] = lds_f16(wda + 8 * cbk * 2);
             }
           }
           {
@@ -346,7 +355,7 @@ __global__ void __maxnreg__(kMaxRegs)
                 for (int k = 0; k < kGB; ++k) {
                   if (j0 + k < nmine) {
                     if constexpr (kBlockSums) {
-                      const int b = st * kChunkBlocks + bps[k];
+                      const int b = st * cbk + bps[k];
                       const int n0 = row0 + 16 * rg + g;
                       const int t0 = 8 * tg + 2 * c;
 #pragma unroll
@@ -532,7 +541,7 @@ EncodeTiledFn encode_fn() {
 }
 
 struct BatchPlan {
-  int RG = 0, S = 0, grid = 0, KPall = 1;
+  int RG = 0, S = 0, grid = 0, KPall = 1, cb = kChunkBlocks;
   uint32_t stage = 0, off_w1 = 0, off_wd = 0, off_x = 0, off_xd = 0;
   size_t smem = 0;
 };
@@ -541,22 +550,24 @@ uint32_t up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 // The consumers' block split: a row group served by more warps than it has token groups
 // splits each chunk's blocks among them (kp layers).  Must match the kernel's mapping.
-int kp_layers(int RG, int TG) {
+int kp_layers(int RG, int TG, int cb) {
   int all = 1;
   for (int r = 0; r < RG; ++r) {
     const int nwr = (kConsumerWarps - 1 - r) / RG + 1;
     if (TG < nwr) {
       int k = nwr / TG;
-      if (k > kChunkBlocks) k = kChunkBlocks;
+      if (k > cb) k = cb;
       if (k > all) all = k;
     }
   }
   return all;
 }
 
-BatchPlan batch_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+// The plan for chunks of cb blocks (empty: the shape or the ring does not fit).
+BatchPlan batch_plan_cb(int64_t M, int64_t N, int64_t K, int cb_blocks, const DeviceInfo& dev) {
   BatchPlan pl;
-  if (M < 1 || M > kBatchMaxM || N < 1 || K < kChunkK || K % kChunkK != 0 || dev.sm_count < 1)
+  if (M < 1 || M > kBatchMaxM || N < 1 || K < kQK * cb_blocks || K % (kQK * cb_blocks) != 0 ||
+      dev.sm_count < 1)
     return pl;
   const int64_t groups = (N + 15) / 16;
   const int64_t RG = (groups + dev.sm_count - 1) / dev.sm_count;
@@ -565,13 +576,15 @@ BatchPlan batch_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
   const uint32_t m = static_cast<uint32_t>(M);
   pl.RG = static_cast<int>(RG);
   pl.grid = static_cast<int>((groups + RG - 1) / RG);
+  pl.cb = cb_blocks;
+  const uint32_t cb = static_cast<uint32_t>(cb_blocks);
   pl.off_w1 = rows * 128;                               // multiple of 2048: swizzle atoms aligned
-  pl.off_wd = 2 * rows * 128;
-  pl.off_x = pl.off_wd + rows * kChunkBlocks * 2;       // 16-byte aligned
+  pl.off_wd = cb / 4 * rows * 128;                      // after the chunk's 128-byte weight boxes
+  pl.off_x = pl.off_wd + rows * cb * 2;                 // 16-byte aligned
   const uint32_t tp = 8 * ((m + 7) / 8);  // tokens padded to whole groups of 8
-  pl.off_xd = pl.off_x + kChunkBlocks * tp * 64;
-  pl.stage = up(pl.off_xd + kChunkBlocks * tp * 4, 1024);
-  pl.KPall = kp_layers(pl.RG, static_cast<int>((M + 7) / 8));
+  pl.off_xd = pl.off_x + cb * tp * 64;
+  pl.stage = up(pl.off_xd + cb * tp * 4, 1024);
+  pl.KPall = kp_layers(pl.RG, static_cast<int>((M + 7) / 8), pl.cb);
   const size_t red = static_cast<size_t>(pl.KPall) * rows * tp * 4;  // partial-sum layers
   const size_t budget = static_cast<size_t>(dev.max_smem_optin) - 2048 - 1024;
   int S = static_cast<int>((kRingTarget + pl.stage - 1) / pl.stage);
@@ -585,6 +598,15 @@ BatchPlan batch_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
   pl.S = S;
   pl.smem = ring + 1024;
   return pl;
+}
+
+// Chunks of 16 blocks where K allows and the ring still holds 3 stages, else of 8.
+BatchPlan batch_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+  if (K % (kQK * kMaxChunkBlocks) == 0) {
+    const BatchPlan wide = batch_plan_cb(M, N, K, kMaxChunkBlocks, dev);
+    if (wide.smem != 0 && wide.S >= 3) return wide;
+  }
+  return batch_plan_cb(M, N, K, kChunkBlocks, dev);
 }
 
 template <bool kBS, int kNTG, bool kFused = false>
@@ -691,7 +713,7 @@ cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const in
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nb), static_cast<cuuint64_t>(N)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nb) * 2};
-    const cuuint32_t box[2] = {kChunkBlocks, rows};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(pl.cb), rows};
     const cuuint32_t es[2] = {1, 1};
     // block-sum mode reads no scales; the map still needs a valid address
     const void* base = bs ? static_cast<const void*>(Wq) : static_cast<const void*>(Wd);
@@ -711,6 +733,7 @@ cudaError_t launch_batch(const void* x, int xtype, const int8_t* xq_in, const in
   p.RG = pl.RG;
   p.KPall = pl.KPall;
   p.stages = pl.S;
+  p.cb = pl.cb;
   p.stage_bytes = pl.stage;
   p.off_w1 = pl.off_w1;
   p.off_wd = pl.off_wd;
