@@ -34,6 +34,10 @@ def test_widening_is_exact(q8):
     Wq = rng.integers(-127, 128, (300, 544), dtype=np.int64).astype(np.int8)
     B16 = q8.q8_weights_to_f16(T(Wq)).cpu().numpy().view(np.uint16)
     assert np.array_equal(B16, Wq.astype(np.float16).view(np.uint16))
+    # every byte value in every position of the 16-byte pieces the pass converts
+    allc = np.tile(np.arange(-128, 128, dtype=np.int64).astype(np.int8), 33).reshape(33, 256)
+    B16 = q8.q8_weights_to_f16(T(allc)).cpu().numpy().view(np.uint16)
+    assert np.array_equal(B16, allc.astype(np.float16).view(np.uint16))
 
 
 @pytest.mark.parametrize("M,N,K", [(130, 300, 96), (128, 256, 4096), (257, 513, 1056),
