@@ -506,11 +506,11 @@ def run_bsa(torch, q8, dev, steps, warmup, pk, pk_src):
                                      "frac": round(tf / pk["bf16_tflops"], 4),
                                      "peak_source": f"bf16_tflops (burst) of the {pk_src} peaks",
                                      "mma_sync_ceiling_tflops": round(mma_sync_peak, 1),
-                                     "kernel": "q8::bsa_kernel",
+                                     "kernel": "q8::bsa_tc_kernel",
                                      "traffic": recorded_traffic("bsa_32k")},
                         "steps": steps,
-                        "note": ("block-sparse causal attention (MInference-style), mma.sync "
-                                 "bf16 tensor cores, FlashAttention-2 online softmax")}}
+                        "note": ("block-sparse causal attention (MInference-style): tcgen05 "
+                                 "M=64 MMAs with S and O in TMEM, K/V by TMA, online softmax")}}
 
 
 def e2e_measure(torch, q8, dev, x_np, bf16, Wqs, Wds, M, N, K, steps, warmup, bytes_step, ops_step,

@@ -1,4 +1,5 @@
-// q8_bsa.cu -- block-sparse causal attention for long prefill (MInference-style).
+// q8_bsa.cu -- block-sparse causal attention for long prefill (MInference-style) on the
+// fifth-generation tensor cores.
 //
 // "CUDA inference engine for running Qwen3.5/3.6 hybrid models on mining cards
 // (CMP 100-210)" (news.hada.io topic 29953, feature list) speeds up long prefill with
@@ -8,17 +9,32 @@
 // key/value heads (head h reads h / (H / Hkv)); o_t = softmax(q_t . k / sqrt(d)) v over the
 // visible keys, d = 128; a query that sees no key gets 0.
 //
-// Design: one CTA of four warps per (head, query block); warp w owns query rows
-// 16 w .. 16 w + 15.  The Q tile stays in registers as mma.sync A fragments; each listed
-// key block's K and V tiles (64 x 128 bf16 each) are copied into shared memory with
-// cp.async, double-buffered, rows XOR-swizzled in 16-byte chunks so ldmatrix reads are
-// conflict-free.  Per key block: S = Q K^T (64 mma.sync m16n8k16 per warp, fp32), causal
-// mask on the diagonal block, online softmax in base 2 (running max and sum per row),
-// then O += P V with P rounded to bf16 (64 more mma.sync per warp).  Query blocks are
-// scheduled from the last (most key blocks) to the first.
+// Design (one CTA per head and query block, 64 query rows, two CTAs per SM):
+//  - warp 0 (one thread) loads the Q tile once and, per listed key block, the K and V
+//    tiles (64 x 128 bfloat16 each, two 64-column boxes with 128-byte swizzle) by TMA
+//    into two-stage K and V rings;
+//  - warp 1 (one thread) issues the tcgen05 MMAs: S_j = Q K_j^T (M = 64, N = 64, eight
+//    K = 16 steps) into one of two S buffers in TMEM, then O += P_{j-1} V_{j-1} (M = 64,
+//    N = 128, four K = 16 steps, V read in place as an MN-major operand) into the O
+//    accumulator in TMEM, so that the tensor pipe works on S_{j+1} and PV_{j-1} while the
+//    softmax warps work on S_j;
+//  - warps 2-5 (the four TMEM lane quarters; an M = 64 accumulator keeps rows 16q .. 16q+15
+//    in the first 16 lanes of quarter q) run the online softmax: each row is split over two
+//    threads (32 keys each), base-2 exponentials, P rounded to bfloat16 into a swizzled
+//    shared-memory tile that the PV MMA reads as its A operand.  The running maximum used
+//    as the exponent reference moves only when a row's maximum rises by more than 2^8 (then
+//    that warp waits for the previous PV product and rescales its rows of O in TMEM), so
+//    most blocks need no correction of O at all; the weights stay <= 2^8 and the final
+//    o = O / l is unchanged.
+// The grid runs key/value head by key/value head, and within one the query blocks from the
+// last (most key blocks) to the first, the heads of a group side by side: the K and V tiles
+// of the key/value head in flight (16 MB at 32K tokens) stay in L2 across the query blocks
+// and heads that list them.
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "q8_internal.h"
 #include "q8_ptx.cuh"
@@ -28,15 +44,22 @@ namespace {
 
 constexpr int kBlk = 64;     // tokens per query and key block
 constexpr int kD = 128;      // head dim
-constexpr int kRowBytes = kD * 2;
-constexpr int kTile = kBlk * kRowBytes;  // 16 KB
-constexpr int kThreads = 128;
+constexpr int kThreads = 192;
+constexpr uint32_t kTileBytes = kBlk * kD * 2;  // 16 KB: two 64 x 64 swizzled boxes
+constexpr uint32_t kBoxBytes = kTileBytes / 2;
+constexpr uint32_t kPBytes = kBlk * kBlk * 2;   // 8 KB
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kTileBytes;       // two stages
+constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;   // two stages
+constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;   // two buffers
+constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;  // barriers, 1024-byte alignment slack
+constexpr uint32_t kTmemCols = 256;  // S buffers at columns 0 and 64, O at 128
+constexpr uint32_t kColO = 128;
+constexpr float kRescaleLog2 = 8.0f;  // move the exponent reference when the max gains > 2^8
 constexpr uint32_t kErrBadBlock = 1u << 8;  // a listed key block outside [0, query block]
 
 struct BsaParams {
-  const uint16_t* q;   // [H][T][d]
-  const uint16_t* k;   // [Hkv][T][d]
-  const uint16_t* v;
   const int32_t* row_ptr;  // [H * nqb + 1]
   const int32_t* col_idx;  // [nnz]
   int64_t nnz;
@@ -47,44 +70,67 @@ struct BsaParams {
   uint32_t* err;
 };
 
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in a tile
-  return static_cast<uint32_t>(row * kRowBytes + ((chunk ^ (row & 7)) << 4));
+// tcgen05 instruction descriptor, kind::f16 with bfloat16 A and B, f32 D; A K-major, B
+// K-major or (b_mn) MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, uint32_t b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// Shared-memory descriptor of an MN-major operand with 128-byte swizzle: 64-element-wide
+// atoms of 8 K rows (1024 bytes); lbo = byte stride between atoms along MN, sbo = between
+// 8-row groups along K.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
 }
 
-// a 64 x 128 bf16 tile (rows of 256 bytes) into shared memory, swizzled
-__device__ __forceinline__ void load_tile(uint32_t smem, const uint16_t* g, int tid) {
-#pragma unroll
-  for (int i = 0; i < (kBlk * 16) / kThreads; ++i) {
-    const int idx = tid + kThreads * i;
-    const int row = idx >> 4, chunk = idx & 15;
-    cp_async16(smem + swz(row, chunk), g + row * kD + chunk * 8);
-  }
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+// 16 TMEM lanes x 32 columns, twice: thread i < 16 gets lane (base + i), columns
+// col .. col+31; thread i >= 16 gets lane (base + i - 16), columns col+kSplit .. +31.
+template <int kSplit>
+__device__ __forceinline__ void tmem_ld_16x32bx2_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+      "[%32], %33;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr), "n"(kSplit)
+      : "memory");
+}
+
+template <int kSplit>
+__device__ __forceinline__ void tmem_st_16x32bx2_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], %1, "
+      "{%2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, "
+      "%18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33};" ::"r"(taddr),
+      "n"(kSplit), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+      "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+      "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]),
+      "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 2^x on the special-function unit (hardware approximation, subnormals flushed; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -92,195 +138,361 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__global__ void __launch_bounds__(kThreads, 2) bsa_kernel(const BsaParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, tig = lane & 3;
-  const int nqb = p.T / kBlk;
-  const int qb = nqb - 1 - static_cast<int>(blockIdx.x / p.H);  // most key blocks first
-  const int h = static_cast<int>(blockIdx.x % p.H);
-  const int hk = h / (p.H / p.Hkv);
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sKV = sQ + kTile;  // [2][K tile, V tile]
+// the i-th listed key block of a row, or -1 if it lies outside [0, qb]
+__device__ __forceinline__ int listed_block(const int32_t* col_idx, int64_t e, int qb) {
+  const int kb = __ldg(col_idx + e);
+  return (kb >= 0 && kb <= qb) ? kb : -1;
+}
 
-  const int64_t e0 = p.row_ptr[static_cast<int64_t>(h) * nqb + qb];
-  int64_t e1 = p.row_ptr[static_cast<int64_t>(h) * nqb + qb + 1];
+// every lane of the warp waits; the warp leaves together if any lane's wait gave up
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag));
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    bsa_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const BsaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;   // [2] K tile j landed
+  uint64_t* v_full = bars + 3;   // [2] V tile j landed
+  uint64_t* qk_done = bars + 5;  // [2] S_j in TMEM; K stage free
+  uint64_t* pv_done = bars + 7;  // [2] P_j V_j added to O; V stage and P buffer free
+  uint64_t* s_free = bars + 9;   // [2] the softmax warps have read S_j (4 arrivals)
+  uint64_t* p_full = bars + 11;  // [2] P_j written, O rescaled if needed (4 arrivals)
+  uint64_t* end_bar = bars + 13;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  const int nqb = p.T / kBlk, G = p.H / p.Hkv;
+  const int per_kv = G * nqb;
+  const int bid = static_cast<int>(blockIdx.x);
+  const int hk = bid / per_kv, rem = bid - hk * per_kv;
+  const int qb = nqb - 1 - rem / G;
+  const int h = hk * G + rem % G;
+  const int64_t rowi = static_cast<int64_t>(h) * nqb + qb;
+  const int64_t e0 = p.row_ptr[rowi];
+  int64_t e1 = p.row_ptr[rowi + 1];
   if (e1 > p.nnz) e1 = p.nnz;
-  const int64_t nlist = e1 > e0 && e0 >= 0 ? e1 - e0 : 0;
+  const int64_t eend = (e1 > e0 && e0 >= 0) ? e1 : e0;  // a malformed row lists nothing
 
-  const uint16_t* kbase = p.k + static_cast<int64_t>(hk) * p.T * kD;
-  const uint16_t* vbase = p.v + static_cast<int64_t>(hk) * p.T * kD;
-  // the i-th listed key block, or -1 if the entry is outside [0, qb] (then skipped)
-  auto listed = [&](int64_t i) -> int {
-    const int kb = p.col_idx[e0 + i];
-    return (kb >= 0 && kb <= qb) ? kb : -1;
-  };
-
-  // Q tile -> shared -> A fragments (rows 16 warp .. +15, all of d)
-  load_tile(sQ, p.q + (static_cast<int64_t>(h) * p.T + static_cast<int64_t>(qb) * kBlk) * kD, tid);
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  if (nlist > 0) {
-    const int kb = listed(0);
-    if (kb >= 0) {
-      load_tile(sKV, kbase + static_cast<int64_t>(kb) * kBlk * kD, tid);
-      load_tile(sKV + kTile, vbase + static_cast<int64_t>(kb) * kBlk * kD, tid);
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&qk_done[i], 1);
+      mbar_init(&pv_done[i], 1);
+      mbar_init(&s_free[i], 4);
+      mbar_init(&p_full[i], 4);
     }
+    mbar_init(end_bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
   }
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  asm volatile("cp.async.wait_group 1;" ::: "memory");
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
-  uint32_t qa[8][4];
+  tc_fence_after();
+  const uint32_t tbase = tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const int32_t qrow = h * p.T + qb * kBlk;
+      mbar_arrive_expect_tx(q_full, kTileBytes);
+      tma_load_2d(sm + kOffQ, &tmQ, q_full, 0, qrow);
+      tma_load_2d(sm + kOffQ + kBoxBytes, &tmQ, q_full, 64, qrow);
+      int kpar[2] = {-1, -1}, vpar[2] = {-1, -1};
+      bool ok = true;
+      int j = 0;
+      for (int64_t e = e0; e < eend; ++e) {
+        const int kb = listed_block(p.col_idx, e, qb);
+        if (kb < 0) {
+          if (p.err != nullptr) atomicOr(p.err, kErrBadBlock);
+          continue;
+        }
+        const int st = j & 1;
+        const uint32_t par = (j >> 1) & 1;
+        const int32_t krow = hk * p.T + kb * kBlk;
+        uint8_t* sK = sm + kOffK + st * kTileBytes;
+        uint8_t* sV = sm + kOffV + st * kTileBytes;
+        if (!mbar_wait(&qk_done[st], par ^ 1, &abort_flag)) {  // S_{j-2} done with K stage
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&k_full[st], kTileBytes);
+        tma_load_2d(sK, &tmK, &k_full[st], 0, krow);
+        tma_load_2d(sK + kBoxBytes, &tmK, &k_full[st], 64, krow);
+        kpar[st] = static_cast<int>(par);
+        if (!mbar_wait(&pv_done[st], par ^ 1, &abort_flag)) {  // PV_{j-2} done with V stage
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&v_full[st], kTileBytes);
+        tma_load_2d(sV, &tmV, &v_full[st], 0, krow);
+        tma_load_2d(sV + kBoxBytes, &tmV, &v_full[st], 64, krow);
+        vpar[st] = static_cast<int>(par);
+        ++j;
+      }
+      if (!ok) report_error(p.err, kErrWaitTimeout, &abort_flag);
+      // no copy may still be landing in shared memory when the CTA ends
+      mbar_wait(q_full, 0, nullptr);
+      for (int st = 0; st < 2; ++st) {
+        if (kpar[st] >= 0) mbar_wait(&k_full[st], static_cast<uint32_t>(kpar[st]), nullptr);
+        if (vpar[st] >= 0) mbar_wait(&v_full[st], static_cast<uint32_t>(vpar[st]), nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int n = 0;
+      for (int64_t e = e0; e < eend; ++e) n += listed_block(p.col_idx, e, qb) >= 0 ? 1 : 0;
+      bool ok = n == 0 || mbar_wait(q_full, 0, &abort_flag);
+      tc_fence_after();
+      const uint32_t sQ = smem_u32(sm + kOffQ);
+      constexpr uint32_t idS = idesc_bf16(kBlk, kBlk, 0), idO = idesc_bf16(kBlk, kD, 1);
+      for (int j = 0; ok && n > 0 && j <= n; ++j) {
+        if (j < n) {  // S_j = Q K_j^T
+          const int st = j & 1;
+          const uint32_t par = (j >> 1) & 1;
+          if (!mbar_wait(&k_full[st], par, &abort_flag) ||
+              !mbar_wait(&s_free[st], par ^ 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sK = smem_u32(sm + kOffK + st * kTileBytes);
 #pragma unroll
-  for (int kc = 0; kc < 8; ++kc) {
-    const int row = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1);
-    const int chunk = 2 * kc + (lane >> 4);
-    ldsm_x4(sQ + swz(row, chunk), qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3]);
+          for (int s = 0; s < 8; ++s) {
+            const uint32_t off = static_cast<uint32_t>((s >> 2) * kBoxBytes + (s & 3) * 32);
+            mma_f16_ss(tbase + static_cast<uint32_t>(st * kBlk), sdesc_k_sw128(sQ + off),
+                       sdesc_k_sw128(sK + off), idS, s > 0 ? 1u : 0u);
+          }
+          mma_commit(&qk_done[st]);
+        }
+        if (j >= 1) {  // O += P_{j-1} V_{j-1}
+          const int jp = j - 1, st = jp & 1;
+          const uint32_t par = (jp >> 1) & 1;
+          if (!mbar_wait(&v_full[st], par, &abort_flag) || !mbar_wait(&p_full[st], par, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sP = smem_u32(sm + kOffP + st * kPBytes);
+          const uint32_t sV = smem_u32(sm + kOffV + st * kTileBytes);
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            mma_f16_ss(tbase + kColO, sdesc_k_sw128(sP + s * 32),
+                       sdesc_mn_sw128(sV + s * 2048, kBoxBytes, 1024), idO,
+                       (jp > 0 || s > 0) ? 1u : 0u);
+          mma_commit(&pv_done[st]);
+        }
+      }
+      if (!ok) report_error(p.err, kErrWaitTimeout, &abort_flag);
+      // every MMA issued has finished before the CTA frees TMEM and shared memory
+      mma_commit(end_bar);
+      mbar_wait(end_bar, 0, nullptr);
+    }
+  } else {
+    // ---------------- online softmax, O correction, output ----------------
+    const int qd = warp & 3;              // TMEM lane quarter this warp may access
+    const int hf = lane >> 4;             // keys 32 hf .. +31, output columns 64 hf .. +63
+    const int r = 16 * qd + (lane & 15);  // query row within the block
+    const uint32_t tl = tbase + (static_cast<uint32_t>(32 * qd) << 16);
+    const float sl2 = p.scale_log2;
+    float ref = -INFINITY, l = 0.0f;
+    bool ok = true;
+    int j = 0;
+    for (int64_t e = e0; e < eend; ++e) {
+      const int kb = listed_block(p.col_idx, e, qb);
+      if (kb < 0) continue;
+      const int sb = j & 1;
+      const uint32_t par = (j >> 1) & 1;
+      if (!warp_wait(&qk_done[sb], par, &abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[32];
+      tmem_ld_16x32bx2_x32<32>(tl + static_cast<uint32_t>(sb * kBlk), sr);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+      float x[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(sr[i]);
+      if (kb == qb) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (32 * hf + i > r) x[i] = -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int i = 1; i < 32; ++i) mx = fmaxf(mx, x[i]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+      const float mn = mx * sl2;
+      const bool resc = mn > ref + kRescaleLog2;  // always on a row's first block
+      float alpha = 1.0f;
+      if (resc) {
+        alpha = ex2(ref - mn);  // 0 on the first block
+        ref = mn;
+      }
+      float sum = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        x[i] = ex2(fmaf(x[i], sl2, -ref));
+        sum += x[i];
+      }
+      l = fmaf(l, alpha, sum);
+      // the P buffer is free again once PV_{j-2} is done
+      if (!warp_wait(&pv_done[sb], par ^ 1, &abort_flag)) {
+        ok = false;
+        break;
+      }
+      uint8_t* prow = sm + kOffP + sb * kPBytes + r * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int chunk = 4 * hf + c;
+        uint4 v;
+        v.x = pack_bf16(x[8 * c + 0], x[8 * c + 1]);
+        v.y = pack_bf16(x[8 * c + 2], x[8 * c + 3]);
+        v.z = pack_bf16(x[8 * c + 4], x[8 * c + 5]);
+        v.w = pack_bf16(x[8 * c + 6], x[8 * c + 7]);
+        *reinterpret_cast<uint4*>(prow + ((chunk ^ (r & 7)) << 4)) = v;
+      }
+      if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
+        // a row's reference moved: scale its O by alpha once PV_{j-1} is in
+        const int jp = j - 1;
+        if (!warp_wait(&pv_done[jp & 1], (jp >> 1) & 1, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_16x32bx2_x32<64>(tl + kColO + c0, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_16x32bx2_x32<64>(tl + kColO + c0, o);
+        }
+        tmem_st_wait();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[sb]);
+      ++j;
+    }
+    if (!ok) report_error(p.err, kErrWaitTimeout, &abort_flag);
+    const float lt = l + __shfl_xor_sync(0xFFFFFFFFu, l, 16);
+    bool have = false;
+    if (ok && j > 0) {
+      const int jl = j - 1;
+      have = warp_wait(&pv_done[jl & 1], (jl >> 1) & 1, &abort_flag);
+      if (!have) report_error(p.err, kErrWaitTimeout, &abort_flag);
+      tc_fence_after();
+    }
+    const float inv = (have && lt > 0.0f) ? 1.0f / lt : 0.0f;
+    const int64_t orow = static_cast<int64_t>(h) * p.T + static_cast<int64_t>(qb) * kBlk + r;
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t o[32];
+      if (have) {
+        tmem_ld_16x32bx2_x32<64>(tl + kColO + c0, o);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0u;  // no visible key (or an abandoned wait): 0
+      }
+      const int col = 64 * hf + c0;
+      if (p.otype == 1) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow * kD + col);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 v;
+          v.x = pack_bf16(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
+          v.y = pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
+          v.z = pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
+          v.w = pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
+          dst[c] = v;
+        }
+      } else {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * kD + col);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          dst[c] = make_float4(__uint_as_float(o[4 * c + 0]) * inv, __uint_as_float(o[4 * c + 1]) * inv,
+                               __uint_as_float(o[4 * c + 2]) * inv, __uint_as_float(o[4 * c + 3]) * inv);
+      }
+    }
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, kTmemCols);
+}
 
-  float o[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // rows g and g + 8
-  const int qrow0 = 16 * warp + g, qrow1 = qrow0 + 8;         // rows within the block
+// ---- host ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-  for (int64_t it = 0; it < nlist; ++it) {
-    const int buf = static_cast<int>(it & 1);
-    const int kb = listed(it);
-    if (it + 1 < nlist) {  // next block's tiles while this one is used
-      const int kn = listed(it + 1);
-      const uint32_t nb = sKV + static_cast<uint32_t>((buf ^ 1) * 2 * kTile);
-      if (kn >= 0) {
-        load_tile(nb, kbase + static_cast<int64_t>(kn) * kBlk * kD, tid);
-        load_tile(nb + kTile, vbase + static_cast<int64_t>(kn) * kBlk * kD, tid);
-      }
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
-    __syncthreads();
-    if (kb < 0) {
-      if (tid == 0 && p.err != nullptr) atomicOr(p.err, kErrBadBlock);
-      __syncthreads();
-      continue;
-    }
-    const uint32_t sK = sKV + static_cast<uint32_t>(buf * 2 * kTile), sV = sK + kTile;
+EncodeTiledFn bsa_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
 
-    // S = Q K^T: 8 key n-tiles of 8 keys, 8 d chunks of 16
-    float s[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int kc = 0; kc < 8; kc += 2) {
-        uint32_t b0, b1, b2, b3;  // d chunks kc and kc + 1 of keys 8 nt .. 8 nt + 7
-        ldsm_x4(sK + swz(8 * nt + (lane & 7), 2 * kc + (lane >> 3)), b0, b1, b2, b3);
-        mma_bf16(s[nt], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], b0, b1);
-        mma_bf16(s[nt], qa[kc + 1][0], qa[kc + 1][1], qa[kc + 1][2], qa[kc + 1][3], b2, b3);
-      }
-    }
-    // scale to base 2; causal mask on the diagonal block
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int key = 8 * nt + 2 * tig + j;
-        float a = s[nt][j] * p.scale_log2, b = s[nt][2 + j] * p.scale_log2;
-        if (kb == qb && key > qrow0) a = -INFINITY;
-        if (kb == qb && key > qrow1) b = -INFINITY;
-        s[nt][j] = a;
-        s[nt][2 + j] = b;
-        mx0 = fmaxf(mx0, a);
-        mx1 = fmaxf(mx1, b);
-      }
-    }
-#pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
-    }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    // rows that have seen no key yet keep a finite reference (their terms are all zero)
-    const float ref0 = mn0 == -INFINITY ? 0.0f : mn0, ref1 = mn1 == -INFINITY ? 0.0f : mn1;
-    const float al0 = exp2f(m0 - ref0), al1 = exp2f(m1 - ref1);  // exp2(-inf) = 0
-    m0 = mn0;
-    m1 = mn1;
-    float sum0 = 0.0f, sum1 = 0.0f;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      s[nt][0] = exp2f(s[nt][0] - ref0);
-      s[nt][1] = exp2f(s[nt][1] - ref0);
-      s[nt][2] = exp2f(s[nt][2] - ref1);
-      s[nt][3] = exp2f(s[nt][3] - ref1);
-      sum0 += s[nt][0] + s[nt][1];
-      sum1 += s[nt][2] + s[nt][3];
-    }
-#pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-      sum0 += __shfl_xor_sync(0xFFFFFFFFu, sum0, off);
-      sum1 += __shfl_xor_sync(0xFFFFFFFFu, sum1, off);
-    }
-    l0 = l0 * al0 + sum0;
-    l1 = l1 * al1 + sum1;
-#pragma unroll
-    for (int dn = 0; dn < 16; ++dn) {
-      o[dn][0] *= al0;
-      o[dn][1] *= al0;
-      o[dn][2] *= al1;
-      o[dn][3] *= al1;
-    }
-    // O += P V: 4 key chunks of 16, 16 d n-tiles of 8
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t a0 = pack_bf16(s[2 * j][0], s[2 * j][1]);
-      const uint32_t a1 = pack_bf16(s[2 * j][2], s[2 * j][3]);
-      const uint32_t a2 = pack_bf16(s[2 * j + 1][0], s[2 * j + 1][1]);
-      const uint32_t a3 = pack_bf16(s[2 * j + 1][2], s[2 * j + 1][3]);
-#pragma unroll
-      for (int dn = 0; dn < 16; dn += 2) {
-        uint32_t b0, b1, b2, b3;  // keys 16 j .. +15 of d n-tiles dn and dn + 1
-        const int row = 16 * j + (lane & 7) + 8 * ((lane >> 3) & 1);
-        ldsm_x4_t(sV + swz(row, dn + (lane >> 4)), b0, b1, b2, b3);
-        mma_bf16(o[dn], a0, a1, a2, a3, b0, b1);
-        mma_bf16(o[dn + 1], a0, a1, a2, a3, b2, b3);
-      }
-    }
-    __syncthreads();  // this buffer is refilled two iterations on
-  }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-
-  // O / l -> output (rows without any visible key stay 0)
-  const float inv0 = l0 > 0.0f ? 1.0f / l0 : 0.0f, inv1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
-  const int64_t t0 = static_cast<int64_t>(qb) * kBlk + qrow0, t1 = t0 + 8;
-  const int64_t base0 = (static_cast<int64_t>(h) * p.T + t0) * kD, base1 = (static_cast<int64_t>(h) * p.T + t1) * kD;
-#pragma unroll
-  for (int dn = 0; dn < 16; ++dn) {
-    const int col = 8 * dn + 2 * tig;
-    if (p.otype == 1) {
-      uint16_t* out = static_cast<uint16_t*>(p.o);
-      *reinterpret_cast<uint32_t*>(out + base0 + col) = pack_bf16(o[dn][0] * inv0, o[dn][1] * inv0);
-      *reinterpret_cast<uint32_t*>(out + base1 + col) = pack_bf16(o[dn][2] * inv1, o[dn][3] * inv1);
-    } else {
-      float* out = static_cast<float*>(p.o);
-      *reinterpret_cast<float2*>(out + base0 + col) = make_float2(o[dn][0] * inv0, o[dn][1] * inv0);
-      *reinterpret_cast<float2*>(out + base1 + col) = make_float2(o[dn][2] * inv1, o[dn][3] * inv1);
-    }
-  }
+// [rows][128] bfloat16, loaded as 64 x 64 boxes with 128-byte swizzle
+bool encode_head_rows(CUtensorMap* map, const void* ptr, uint64_t rows) {
+  EncodeTiledFn enc = bsa_encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlk)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
-
-size_t bsa_smem_bytes() { return static_cast<size_t>(kTile) * 5; }
 
 cudaError_t launch_bsa(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                        const int32_t* row_ptr, const int32_t* col_idx, int64_t nnz, void* o,
                        int otype, int64_t H, int64_t Hkv, int64_t T, const DeviceInfo& dev,
                        cudaStream_t stream) {
   if (H == 0 || T == 0) return cudaSuccess;
+  // TMA row coordinates are 32-bit
+  if (H * T > 0x7FFFFFFF || Hkv * T > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  CUtensorMap mq, mk, mv;
+  if (!encode_head_rows(&mq, q, static_cast<uint64_t>(H * T)) ||
+      !encode_head_rows(&mk, k, static_cast<uint64_t>(Hkv * T)) ||
+      !encode_head_rows(&mv, v, static_cast<uint64_t>(Hkv * T)))
+    return cudaErrorInvalidValue;
   BsaParams p;
-  p.q = q;
-  p.k = k;
-  p.v = v;
   p.row_ptr = row_ptr;
   p.col_idx = col_idx;
   p.nnz = nnz;
@@ -291,11 +503,10 @@ cudaError_t launch_bsa(const uint16_t* q, const uint16_t* k, const uint16_t* v,
   p.T = static_cast<int>(T);
   p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kD));
   p.err = dev.err_word;
-  const size_t smem = bsa_smem_bytes();
-  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(bsa_kernel), smem, dev.device);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(bsa_tc_kernel), kSmemBytes, dev.device);
   if (e != cudaSuccess) return e;
   const int64_t grid = H * (T / kBlk);
-  bsa_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
+  bsa_tc_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 

@@ -71,6 +71,31 @@ def test_dense_causal_and_scaled_queries(q8):
     _close(_run(q8, q, k, v, rp, ci).cpu().numpy(), OB.attention(q, k, v, rp, ci), "dense, sharp")
 
 
+@pytest.mark.parametrize("mask", ["dense", "sparse"])
+def test_running_max_rising_across_blocks(q8, mask):
+    """Keys scaled up block by block (3 + 3 kb, and random factors up to 24): each new block
+    raises a row's maximum score by more than 2^8 in base 2 on most blocks, so the kernel
+    moves its exponent reference and rescales O in the middle of the sweep; a row whose
+    maximum stays within 2^8 keeps its reference."""
+    rng = np.random.default_rng(21)
+    H, Hkv, Tn = 4, 2, 512
+    q, k, v = workloads.bsa_qkv(rng, H, Hkv, Tn)
+    nb = Tn // 64
+    kf = workloads.f32_from_bf16_bits(k).reshape(Hkv, nb, 64, 128)
+    if mask == "dense":
+        grow = (3.0 + 3.0 * np.arange(nb, dtype=np.float32))[None, :, None, None]
+        rp, ci = workloads.dense_causal_mask(H, Tn)
+    else:
+        grow = rng.uniform(0.5, 24.0, (Hkv, nb, 1, 1)).astype(np.float32)
+        rp, ci = workloads.bsa_mask(rng, H, Tn, 0.5)
+    k = workloads.bf16_bits_from_f32((kf * grow).reshape(Hkv, Tn, 128))
+    ref = OB.attention(q, k, v, rp, ci)
+    _close(_run(q8, q, k, v, rp, ci).cpu().numpy(), ref, f"rising maxima, {mask}")
+    _close(_run(q8, q, k, v, rp, ci, torch.bfloat16).float().cpu().numpy(), ref,
+           f"rising maxima, {mask}, bf16", k=2.0)
+    assert q8.q8_device_error() == 0
+
+
 def test_empty_rows_and_bad_blocks(q8):
     rng = np.random.default_rng(8)
     H, Tn = 2, 256
