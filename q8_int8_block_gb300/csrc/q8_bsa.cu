@@ -10,22 +10,23 @@
 // visible keys, d = 128; a query that sees no key gets 0.
 //
 // Design (one CTA per head and query block, 64 query rows, two CTAs per SM):
-//  - warp 0 (one thread) loads the Q tile once and, per listed key block, the K and V
-//    tiles (64 x 128 bfloat16 each, two 64-column boxes with 128-byte swizzle) by TMA
-//    into two-stage K and V rings;
+//  - warp 0 (one thread) loads the Q tile once and, per listed key block, the K tile
+//    (64 x 128 bfloat16, two 64-column boxes with 128-byte swizzle) by TMA into a
+//    three-stage ring; warp 6 (one thread) loads the V tiles into a two-stage ring;
 //  - warp 1 (one thread) issues the tcgen05 MMAs: S_j = Q K_j^T (M = 64, N = 64, eight
-//    K = 16 steps) into one of two S buffers in TMEM, then O += P_{j-1} V_{j-1} (M = 64,
-//    N = 128, four K = 16 steps, V read in place as an MN-major operand) into the O
-//    accumulator in TMEM, so that the tensor pipe works on S_{j+1} and PV_{j-1} while the
-//    softmax warps work on S_j;
+//    K = 16 steps) into one of two S buffers in TMEM, and O += P_j V_j (M = 64, N = 128,
+//    four K = 16 steps, V read in place as an MN-major operand) into the O accumulator in
+//    TMEM.  S_{j+2} is issued as soon as the softmax warps have read S_j, ahead of PV_j, so
+//    the tensor pipe (which runs its MMAs in order) never makes a score tile wait behind a
+//    PV product: the round trips of the MMAs stay off the per-block critical path;
 //  - warps 2-5 (the four TMEM lane quarters; an M = 64 accumulator keeps rows 16q .. 16q+15
 //    in the first 16 lanes of quarter q) run the online softmax: each row is split over two
 //    threads (32 keys each), base-2 exponentials, P rounded to bfloat16 into a swizzled
-//    shared-memory tile that the PV MMA reads as its A operand.  The running maximum used
-//    as the exponent reference moves only when a row's maximum rises by more than 2^8 (then
-//    that warp waits for the previous PV product and rescales its rows of O in TMEM), so
-//    most blocks need no correction of O at all; the weights stay <= 2^8 and the final
-//    o = O / l is unchanged.
+//    shared-memory tile that the PV MMA reads as its A operand (written once PV_{j-1} is
+//    done with it).  The running maximum used as the exponent reference moves only when a
+//    row's maximum rises by more than 2^8; then that warp rescales its rows of O in TMEM
+//    (PV_{j-1} is done by then), so most blocks need no correction of O at all; the weights
+//    stay <= 2^8 and the final o = O / l is unchanged.
 // The grid runs key/value head by key/value head, and within one the query blocks from the
 // last (most key blocks) to the first, the heads of a group side by side: the K and V tiles
 // of the key/value head in flight (16 MB at 32K tokens) stay in L2 across the query blocks
@@ -44,17 +45,21 @@ namespace {
 
 constexpr int kBlk = 64;     // tokens per query and key block
 constexpr int kD = 128;      // head dim
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;  // warps: 0 K/Q loads, 1 MMA, 2-5 softmax, 6 V loads
 constexpr uint32_t kTileBytes = kBlk * kD * 2;  // 16 KB: two 64 x 64 swizzled boxes
 constexpr uint32_t kBoxBytes = kTileBytes / 2;
 constexpr uint32_t kPBytes = kBlk * kBlk * 2;   // 8 KB
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;       // two stages
-constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;   // two stages
-constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;   // two buffers
+constexpr uint32_t kOffK = kOffQ + kTileBytes;
+constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;  // two stages each
+constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;  // two buffers
 constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;  // barriers, 1024-byte alignment slack
-constexpr uint32_t kTmemCols = 256;  // S buffers at columns 0 and 64, O at 128
+constexpr uint32_t kSmemBytes = kOffBar + 128;  // barriers, TMEM address, abort flag
+// two CTAs (and the runtime's 1 KB each) in the SM's 228 KB; the kernel checks that its
+// dynamic shared memory starts on a 1024-byte boundary (the 128-byte swizzle atoms of the
+// TMA tiles and MMA operands need it)
+static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
+constexpr uint32_t kTmemCols = 256;  // S buffers at columns 0 and 64, O at 128 .. 255
 constexpr uint32_t kColO = 128;
 constexpr float kRescaleLog2 = 8.0f;  // move the exponent reference when the max gains > 2^8
 constexpr uint32_t kErrBadBlock = 1u << 8;  // a listed key block outside [0, query block]
@@ -70,10 +75,11 @@ struct BsaParams {
   uint32_t* err;
 };
 
-// tcgen05 instruction descriptor, kind::f16 with bfloat16 A and B, f32 D; A K-major, B
-// K-major or (b_mn) MN-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, uint32_t b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+// tcgen05 instruction descriptor, kind::f16 with bfloat16 A and B, f32 D; A and B K-major,
+// or (a_mn, b_mn) MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) |
+         ((M >> 4) << 24);
 }
 
 // Shared-memory descriptor of an MN-major operand with 128-byte swizzle: 64-element-wide
@@ -152,20 +158,20 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 __global__ void __launch_bounds__(kThreads, 2)
     bsa_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const BsaParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t sm[];
+  if ((smem_u32(sm) & 1023u) != 0) {  // the whole CTA leaves before touching anything
+    if (threadIdx.x == 0 && p.err != nullptr) atomicOr(p.err, kErrBadLaunch);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;   // [2] K tile j landed
-  uint64_t* v_full = bars + 3;   // [2] V tile j landed
-  uint64_t* qk_done = bars + 5;  // [2] S_j in TMEM; K stage free
-  uint64_t* pv_done = bars + 7;  // [2] P_j V_j added to O; V stage and P buffer free
-  uint64_t* s_free = bars + 9;   // [2] the softmax warps have read S_j (4 arrivals)
-  uint64_t* p_full = bars + 11;  // [2] P_j written, O rescaled if needed (4 arrivals)
-  uint64_t* end_bar = bars + 13;
-  __shared__ uint32_t tmem_slot;
-  __shared__ int abort_flag;
+  uint64_t* k_full = bars + 1;   // [2] K tile landed
+  uint64_t* v_full = bars + 3;   // [2] V tile landed
+  uint64_t* grp = bars + 5;      // [2] MMA group c done (c = 0: S_0, S_1; c = j + 1: S_{j+2}, PV_j)
+  uint64_t* p_full = bars + 7;   // [2] P_j written (S_j read, O rescaled if needed): 4 arrivals
+  uint64_t* end_bar = bars + 9;
+  uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(sm + kOffBar + 96);
+  int& abort_flag = *reinterpret_cast<int*>(sm + kOffBar + 100);
 
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
   const int nqb = p.T / kBlk, G = p.H / p.Hkv;
@@ -185,9 +191,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&v_full[i], 1);
-      mbar_init(&qk_done[i], 1);
-      mbar_init(&pv_done[i], 1);
-      mbar_init(&s_free[i], 4);
+      mbar_init(&grp[i], 1);
       mbar_init(&p_full[i], 4);
     }
     mbar_init(end_bar, 1);
@@ -202,102 +206,101 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_slot;
+  // MMA group c completes grp[c % 2] for the (c / 2)-th time
+  auto grp_wait = [&](int c, bool warp_wide) -> bool {
+    uint64_t* b = &grp[c & 1];
+    const uint32_t par = static_cast<uint32_t>(c >> 1) & 1;
+    return warp_wide ? warp_wait(b, par, &abort_flag) : mbar_wait(b, par, &abort_flag);
+  };
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
+  if (warp == 0 || warp == 6) {
+    // ---------------- TMA producers: warp 0 Q and K, warp 6 V ----------------
     if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      const int32_t qrow = h * p.T + qb * kBlk;
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      tma_load_2d(sm + kOffQ, &tmQ, q_full, 0, qrow);
-      tma_load_2d(sm + kOffQ + kBoxBytes, &tmQ, q_full, 64, qrow);
-      int kpar[2] = {-1, -1}, vpar[2] = {-1, -1};
+      const bool isK = warp == 0;
+      const CUtensorMap* map = isK ? &tmK : &tmV;
+      uint64_t* full = isK ? k_full : v_full;
+      uint8_t* ring = sm + (isK ? kOffK : kOffV);
+      tma_prefetch_desc(map);
+      if (isK) {
+        tma_prefetch_desc(&tmQ);
+        const int32_t qrow = h * p.T + qb * kBlk;
+        mbar_arrive_expect_tx(q_full, kTileBytes);
+        tma_load_2d(sm + kOffQ, &tmQ, q_full, 0, qrow);
+        tma_load_2d(sm + kOffQ + kBoxBytes, &tmQ, q_full, 64, qrow);
+      }
+      int lastpar[2] = {-1, -1};
       bool ok = true;
       int j = 0;
       for (int64_t e = e0; e < eend; ++e) {
         const int kb = listed_block(p.col_idx, e, qb);
         if (kb < 0) {
-          if (p.err != nullptr) atomicOr(p.err, kErrBadBlock);
+          if (isK && p.err != nullptr) atomicOr(p.err, kErrBadBlock);
           continue;
         }
         const int st = j & 1;
-        const uint32_t par = (j >> 1) & 1;
+        // the stage's previous tile (j - 2) is used: S_{j-2} is in group max(j - 3, 0), PV_{j-2}
+        // in group j - 1
+        if (j >= 2 && !grp_wait(isK ? (j >= 4 ? j - 3 : 0) : j - 1, false)) {
+          ok = false;
+          break;
+        }
         const int32_t krow = hk * p.T + kb * kBlk;
-        uint8_t* sK = sm + kOffK + st * kTileBytes;
-        uint8_t* sV = sm + kOffV + st * kTileBytes;
-        if (!mbar_wait(&qk_done[st], par ^ 1, &abort_flag)) {  // S_{j-2} done with K stage
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&k_full[st], kTileBytes);
-        tma_load_2d(sK, &tmK, &k_full[st], 0, krow);
-        tma_load_2d(sK + kBoxBytes, &tmK, &k_full[st], 64, krow);
-        kpar[st] = static_cast<int>(par);
-        if (!mbar_wait(&pv_done[st], par ^ 1, &abort_flag)) {  // PV_{j-2} done with V stage
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&v_full[st], kTileBytes);
-        tma_load_2d(sV, &tmV, &v_full[st], 0, krow);
-        tma_load_2d(sV + kBoxBytes, &tmV, &v_full[st], 64, krow);
-        vpar[st] = static_cast<int>(par);
+        mbar_arrive_expect_tx(&full[st], kTileBytes);
+        tma_load_2d(ring + st * kTileBytes, map, &full[st], 0, krow);
+        tma_load_2d(ring + st * kTileBytes + kBoxBytes, map, &full[st], 64, krow);
+        lastpar[st] = (j >> 1) & 1;
         ++j;
       }
       if (!ok) report_error(p.err, kErrWaitTimeout, &abort_flag);
       // no copy may still be landing in shared memory when the CTA ends
-      mbar_wait(q_full, 0, nullptr);
-      for (int st = 0; st < 2; ++st) {
-        if (kpar[st] >= 0) mbar_wait(&k_full[st], static_cast<uint32_t>(kpar[st]), nullptr);
-        if (vpar[st] >= 0) mbar_wait(&v_full[st], static_cast<uint32_t>(vpar[st]), nullptr);
-      }
+      if (isK) mbar_wait(q_full, 0, nullptr);
+      for (int st = 0; st < 2; ++st)
+        if (lastpar[st] >= 0) mbar_wait(&full[st], static_cast<uint32_t>(lastpar[st]), nullptr);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       int n = 0;
       for (int64_t e = e0; e < eend; ++e) n += listed_block(p.col_idx, e, qb) >= 0 ? 1 : 0;
-      bool ok = n == 0 || mbar_wait(q_full, 0, &abort_flag);
-      tc_fence_after();
-      const uint32_t sQ = smem_u32(sm + kOffQ);
-      constexpr uint32_t idS = idesc_bf16(kBlk, kBlk, 0), idO = idesc_bf16(kBlk, kD, 1);
-      for (int j = 0; ok && n > 0 && j <= n; ++j) {
-        if (j < n) {  // S_j = Q K_j^T
-          const int st = j & 1;
-          const uint32_t par = (j >> 1) & 1;
-          if (!mbar_wait(&k_full[st], par, &abort_flag) ||
-              !mbar_wait(&s_free[st], par ^ 1, &abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sK = smem_u32(sm + kOffK + st * kTileBytes);
+      const uint32_t sQ = smem_u32(sm + kOffQ), sP = smem_u32(sm + kOffP);
+      // S = Q K^T: M = 64 queries, N = 64 keys.  O += P V: M = 64, N = 128 (head dim), V read
+      // in place as the MN-major B operand.
+      constexpr uint32_t idS = idesc_bf16(kBlk, kBlk, 0, 0), idO = idesc_bf16(kBlk, kD, 0, 1);
+      auto issue_s = [&](int i) -> bool {  // S_i into S buffer i % 2 (K_i in stage i % 2)
+        const int st = i & 1;
+        if (!mbar_wait(&k_full[st], static_cast<uint32_t>(i >> 1) & 1, &abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(sm + kOffK + st * kTileBytes);
 #pragma unroll
-          for (int s = 0; s < 8; ++s) {
-            const uint32_t off = static_cast<uint32_t>((s >> 2) * kBoxBytes + (s & 3) * 32);
-            mma_f16_ss(tbase + static_cast<uint32_t>(st * kBlk), sdesc_k_sw128(sQ + off),
-                       sdesc_k_sw128(sK + off), idS, s > 0 ? 1u : 0u);
-          }
-          mma_commit(&qk_done[st]);
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t off = static_cast<uint32_t>((s >> 2) * kBoxBytes + (s & 3) * 32);
+          mma_f16_ss(tbase + static_cast<uint32_t>(st * kBlk), sdesc_k_sw128(sQ + off),
+                     sdesc_k_sw128(sK + off), idS, s > 0 ? 1u : 0u);
         }
-        if (j >= 1) {  // O += P_{j-1} V_{j-1}
-          const int jp = j - 1, st = jp & 1;
-          const uint32_t par = (jp >> 1) & 1;
-          if (!mbar_wait(&v_full[st], par, &abort_flag) || !mbar_wait(&p_full[st], par, &abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sP = smem_u32(sm + kOffP + st * kPBytes);
-          const uint32_t sV = smem_u32(sm + kOffV + st * kTileBytes);
+        return true;
+      };
+      bool ok = true;
+      if (n > 0) {
+        ok = mbar_wait(q_full, 0, &abort_flag) && issue_s(0) && (n < 2 || issue_s(1));
+        if (ok) mma_commit(&grp[0]);  // group 0
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        // P_j is written, so S_j has been read: its buffer takes S_{j+2}
+        const int b = j & 1;
+        const uint32_t par = static_cast<uint32_t>(j >> 1) & 1;
+        if (!mbar_wait(&p_full[b], par, &abort_flag) || (j + 2 < n && !issue_s(j + 2)) ||
+            !mbar_wait(&v_full[b], par, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sV = smem_u32(sm + kOffV + b * kTileBytes);
+        const uint32_t sPj = sP + static_cast<uint32_t>(b) * kPBytes;
 #pragma unroll
-          for (int s = 0; s < 4; ++s)
-            mma_f16_ss(tbase + kColO, sdesc_k_sw128(sP + s * 32),
-                       sdesc_mn_sw128(sV + s * 2048, kBoxBytes, 1024), idO,
-                       (jp > 0 || s > 0) ? 1u : 0u);
-          mma_commit(&pv_done[st]);
-        }
+        for (int s = 0; s < 4; ++s)
+          mma_f16_ss(tbase + kColO, sdesc_k_sw128(sPj + s * 32),
+                     sdesc_mn_sw128(sV + s * 2048, kBoxBytes, 1024), idO, (j > 0 || s > 0) ? 1u : 0u);
+        mma_commit(&grp[(j + 1) & 1]);  // group j + 1
       }
       if (!ok) report_error(p.err, kErrWaitTimeout, &abort_flag);
       // every MMA issued has finished before the CTA frees TMEM and shared memory
@@ -318,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int kb = listed_block(p.col_idx, e, qb);
       if (kb < 0) continue;
       const int sb = j & 1;
-      const uint32_t par = (j >> 1) & 1;
-      if (!warp_wait(&qk_done[sb], par, &abort_flag)) {
+      // S_j is in group max(j - 1, 0), which also finished PV_{j-2} with P buffer j % 2
+      if (!grp_wait(j > 0 ? j - 1 : 0, true)) {
         ok = false;
         break;
       }
@@ -327,9 +330,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       uint32_t sr[32];
       tmem_ld_16x32bx2_x32<32>(tl + static_cast<uint32_t>(sb * kBlk), sr);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
       float x[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(sr[i]);
@@ -356,11 +356,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         sum += x[i];
       }
       l = fmaf(l, alpha, sum);
-      // the P buffer is free again once PV_{j-2} is done
-      if (!warp_wait(&pv_done[sb], par ^ 1, &abort_flag)) {
-        ok = false;
-        break;
-      }
       uint8_t* prow = sm + kOffP + sb * kPBytes + r * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -373,9 +368,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         *reinterpret_cast<uint4*>(prow + ((chunk ^ (r & 7)) << 4)) = v;
       }
       if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
-        // a row's reference moved: scale its O by alpha once PV_{j-1} is in
-        const int jp = j - 1;
-        if (!warp_wait(&pv_done[jp & 1], (jp >> 1) & 1, &abort_flag)) {
+        // a row's reference moved: once PV_{j-1} (group j) is in, scale its O by alpha (rows
+        // that kept theirs have alpha 1)
+        if (!grp_wait(j, true)) {
           ok = false;
           break;
         }
@@ -401,8 +396,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float lt = l + __shfl_xor_sync(0xFFFFFFFFu, l, 16);
     bool have = false;
     if (ok && j > 0) {
-      const int jl = j - 1;
-      have = warp_wait(&pv_done[jl & 1], (jl >> 1) & 1, &abort_flag);
+      have = grp_wait(j, true);  // group j holds the last PV
       if (!have) report_error(p.err, kErrWaitTimeout, &abort_flag);
       tc_fence_after();
     }
