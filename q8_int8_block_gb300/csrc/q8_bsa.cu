@@ -266,16 +266,21 @@ __global__ void __launch_bounds__(kThreads, 2)
       // S = Q K^T: M = 64 queries, N = 64 keys.  O += P V: M = 64, N = 128 (head dim), V read
       // in place as the MN-major B operand.
       constexpr uint32_t idS = idesc_bf16(kBlk, kBlk, 0, 0), idO = idesc_bf16(kBlk, kD, 0, 1);
+      // Operand descriptors are built once: a K step or another stage only moves the start
+      // address, which the descriptor holds in 16-byte units in its low bits (shared-memory
+      // addresses stay below 256 KB, so the sum never carries out of that field).
+      const uint64_t dQ = sdesc_k_sw128(sQ), dK0 = sdesc_k_sw128(smem_u32(sm + kOffK));
+      const uint64_t dP0 = sdesc_k_sw128(sP);
+      const uint64_t dV0 = sdesc_mn_sw128(smem_u32(sm + kOffV), kBoxBytes, 1024);
       auto issue_s = [&](int i) -> bool {  // S_i into S buffer i % 2 (K_i in stage i % 2)
         const int st = i & 1;
         if (!mbar_wait(&k_full[st], static_cast<uint32_t>(i >> 1) & 1, &abort_flag)) return false;
         tc_fence_after();
-        const uint32_t sK = smem_u32(sm + kOffK + st * kTileBytes);
+        const uint64_t dK = dK0 + static_cast<uint64_t>(st) * (kTileBytes >> 4);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          const uint32_t off = static_cast<uint32_t>((s >> 2) * kBoxBytes + (s & 3) * 32);
-          mma_f16_ss(tbase + static_cast<uint32_t>(st * kBlk), sdesc_k_sw128(sQ + off),
-                     sdesc_k_sw128(sK + off), idS, s > 0 ? 1u : 0u);
+          const uint64_t off = static_cast<uint64_t>(((s >> 2) * kBoxBytes + (s & 3) * 32) >> 4);
+          mma_f16_ss(tbase + static_cast<uint32_t>(st * kBlk), dQ + off, dK + off, idS, s > 0 ? 1u : 0u);
         }
         return true;
       };
@@ -294,12 +299,12 @@ __global__ void __launch_bounds__(kThreads, 2)
           break;
         }
         tc_fence_after();
-        const uint32_t sV = smem_u32(sm + kOffV + b * kTileBytes);
-        const uint32_t sPj = sP + static_cast<uint32_t>(b) * kPBytes;
+        const uint64_t dV = dV0 + static_cast<uint64_t>(b) * (kTileBytes >> 4);
+        const uint64_t dP = dP0 + static_cast<uint64_t>(b) * (kPBytes >> 4);
 #pragma unroll
-        for (int s = 0; s < 4; ++s)
-          mma_f16_ss(tbase + kColO, sdesc_k_sw128(sPj + s * 32),
-                     sdesc_mn_sw128(sV + s * 2048, kBoxBytes, 1024), idO, (j > 0 || s > 0) ? 1u : 0u);
+        for (int s = 0; s < 4; ++s)  // 16 keys per step: 32 bytes along a P row, 16 rows of V
+          mma_f16_ss(tbase + kColO, dP + static_cast<uint64_t>(s * 2), dV + static_cast<uint64_t>(s * 128), idO,
+                     (j > 0 || s > 0) ? 1u : 0u);
         mma_commit(&grp[(j + 1) & 1]);  // group j + 1
       }
       if (!ok) report_error(p.err, kErrWaitTimeout, &abort_flag);
