@@ -497,7 +497,13 @@ def run_bsa(torch, q8, dev, steps, warmup, pk, pk_src):
     fn()
     total, kern = time_graph_steps(torch, q8, [fn], steps, warmup, instrument=False)
     tf = flops / kern / 1e12
-    mma_sync_peak, _ = unit_peak(torch, pk, "hmma_mac_per_clk_sm", 2, 1024.0)
+    # the ceiling of this formulation: every MMA of the kernel is M = 64 (one query block), a
+    # shape the tensor pipe runs at half its rate; the recorded cycles per key block per CTA
+    # with two CTAs per SM (bench_rates.py) give two blocks of 4 d 64 64 flops per SM
+    rec = measured_rates() or {}
+    blk_cycles = rec.get("rates", {}).get("umma_attn_block_2cta_cycles")
+    m64_ceiling = (2 * 4 * cfg["d"] * 64 * 64 / blk_cycles * sm_count(torch) *
+                   pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12) if blk_cycles else None
     return {"bsa_32k": {"value": round(tf, 2), "unit": "TFLOP/s", "us_per_step": round(kern * 1e6, 2),
                         "algorithmic_flops_per_launch": flops, "visible_pairs": pairs,
                         "block_density": round(len(ci) / (cfg["H"] * nb * (nb + 1) / 2), 4),
@@ -505,7 +511,8 @@ def run_bsa(torch, q8, dev, steps, warmup, pk, pk_src):
                                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                                      "frac": round(tf / pk["bf16_tflops"], 4),
                                      "peak_source": f"bf16_tflops (burst) of the {pk_src} peaks",
-                                     "mma_sync_ceiling_tflops": round(mma_sync_peak, 1),
+                                     "m64_mma_ceiling_tflops": round(m64_ceiling, 1) if m64_ceiling else None,
+                                     "frac_of_m64_ceiling": round(tf / m64_ceiling, 4) if m64_ceiling else None,
                                      "kernel": "q8::bsa_tc_kernel",
                                      "traffic": recorded_traffic("bsa_32k")},
                         "steps": steps,

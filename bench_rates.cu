@@ -203,6 +203,76 @@ __global__ void __launch_bounds__(128, 1) umma_kernel(int iters, long long* cyc,
   }
 }
 
+// tcgen05 kind::f16 (bfloat16) chains of the block-sparse attention kernel's shapes.  One
+// thread per CTA issues dependent K=16 MMAs into one accumulator (commit + wait every 64).
+// kMix = 0: M x N MMAs only; kMix = 1: per "block" 8 x M64 N64 (S) + 4 x M64 N128 (O), the
+// attention kernel's per-key-block work.  Shared memory is sized for at most two CTAs per SM.
+template <int M, int N, int kMix>
+__global__ void __launch_bounds__(128) umma_chain_kernel(int iters, long long* cyc, uint32_t* err) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t tmem_slot;
+  __shared__ uint64_t bar;
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* base = smem_raw + (((raw + 1023) & ~1023u) - raw);
+  for (int i = threadIdx.x; i < 49152 / 4; i += blockDim.x)
+    reinterpret_cast<uint32_t*>(base)[i] = 0x3F803F80u;
+  fence_proxy_async_smem();
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_slot;
+  if (threadIdx.x == 32) {
+    const uint32_t a0 = smem_u32(base), b0 = smem_u32(base + 16384);
+    constexpr uint32_t kBf16 = (1u << 7) | (1u << 10);
+    int phase = 0;
+    const long long t0 = clock64();
+    for (int p = 0; p < iters; ++p) {
+      if (kMix == 0) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          mma_f16_ss(tmem_base, sdesc_k_sw128(a0 + (q & 3) * 32), sdesc_k_sw128(b0 + (q & 3) * 32),
+                     idesc_f16_f32(M, N) | kBf16, (p | q) ? 1u : 0u);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          mma_f16_ss(tmem_base + (p & 1) * 64, sdesc_k_sw128(a0 + (q & 3) * 32),
+                     sdesc_k_sw128(b0 + (q & 3) * 32), idesc_f16_f32(64, 64) | kBf16, q > 0 ? 1u : 0u);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          mma_f16_ss(tmem_base + 128, sdesc_k_sw128(a0 + (q & 3) * 32), sdesc_k_sw128(b0 + (q & 3) * 32),
+                     idesc_f16_f32(64, 128) | kBf16, 1u);
+      }
+      if ((p & 7) == 7) {
+        mma_commit(&bar);
+        if (!mbar_wait(&bar, phase & 1, nullptr)) {
+          atomicOr(err, 1u);
+          break;
+        }
+        ++phase;
+      }
+    }
+    // every MMA issued is finished before TMEM is freed
+    mma_commit(&bar);
+    if (!mbar_wait(&bar, phase & 1, nullptr)) atomicOr(err, 1u);
+    cyc[blockIdx.x] = (clock64() - t0) / iters;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 256);
+  }
+}
+
 double max_cycles(const long long* h, int n) {
   double m = 0;
   for (int i = 0; i < n; ++i) m = h[i] > m ? static_cast<double>(h[i]) : m;
@@ -263,6 +333,27 @@ extern "C" int q8_rates(int sms, double* res) {
   umma_kernel<1><<<sms, 128, smem>>>(2000, cyc, err);
   umma_kernel<1><<<sms, 128, smem>>>(2000, cyc, err);
   res[7] = get(sms);  // cycles per pair + commit + wait
+  // attention shapes: per-CTA cycles of the slowest CTA, two CTAs (or one) per SM
+  const int smem2 = 80 * 1024;  // at most two CTAs per SM (49 KB used)
+  cudaFuncSetAttribute(umma_chain_kernel<64, 64, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem2);
+  cudaFuncSetAttribute(umma_chain_kernel<128, 64, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem2);
+  cudaFuncSetAttribute(umma_chain_kernel<64, 64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem2);
+  clear();
+  umma_chain_kernel<64, 64, 0><<<sms, 128, smem2>>>(1024, cyc, err);
+  umma_chain_kernel<64, 64, 0><<<sms, 128, smem2>>>(1024, cyc, err);
+  res[8] = get(sms) / 8.0;  // cycles per M64 N64 MMA, one CTA per SM
+  clear();
+  umma_chain_kernel<64, 64, 0><<<2 * sms, 128, smem2>>>(1024, cyc, err);
+  umma_chain_kernel<64, 64, 0><<<2 * sms, 128, smem2>>>(1024, cyc, err);
+  res[9] = 2.0 * 8 * (64 * 64 * 16) / get(2 * sms);  // MACs per clock per SM
+  clear();
+  umma_chain_kernel<128, 64, 0><<<2 * sms, 128, smem2>>>(1024, cyc, err);
+  umma_chain_kernel<128, 64, 0><<<2 * sms, 128, smem2>>>(1024, cyc, err);
+  res[10] = 2.0 * 8 * (128 * 64 * 16) / get(2 * sms);  // MACs per clock per SM
+  clear();
+  umma_chain_kernel<64, 64, 1><<<2 * sms, 128, smem2>>>(1024, cyc, err);
+  umma_chain_kernel<64, 64, 1><<<2 * sms, 128, smem2>>>(1024, cyc, err);
+  res[11] = get(2 * sms);  // cycles per attention key block per CTA
   uint32_t e = 0;
   cudaMemcpy(&e, err, sizeof e, cudaMemcpyDeviceToHost);
   const cudaError_t st = cudaDeviceSynchronize();
@@ -270,5 +361,5 @@ extern "C" int q8_rates(int sms, double* res) {
   cudaFree(fout);
   cudaFree(cyc);
   cudaFree(err);
-  return (st == cudaSuccess && e == 0) ? 8 : -2;
+  return (st == cudaSuccess && e == 0) ? 12 : -2;
 }

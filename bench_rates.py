@@ -4,7 +4,8 @@
 These are the unit rates that the secondary rooflines of bench.py rest on (the dp4a GEMM's
 integer-ALU peak, the mma.sync ceiling of the batched and attention kernels) and that the
 analysis of the prefill GEMM uses (the FP32 rescale rate against the tcgen05 MMA rate, the
-broadcast shared-memory load rate of the rescale's column scales, the commit round trip).
+broadcast shared-memory load rate of the rescale's column scales, the commit round trip) and
+the block-sparse attention kernel's (the rates of its M = 64 MMA shapes).
 
     python bench_rates.py [--record profiles/rates_gb300.json]
 
@@ -32,6 +33,11 @@ NAMES = [
     ("lds_bcast_per_clk_sm", "warp-wide one-address LDS.128 per clock per SM"),
     ("umma_mac_per_clk_sm", "tcgen05.mma kind::f16 M128 N256 K16 MACs per clock per SM"),
     ("umma_pair_commit_rt_cycles", "cycles: 2 x M128 N256 K16, tcgen05.commit, mbarrier wait"),
+    ("umma_m64n64_1cta_cycles", "cycles per tcgen05.mma M64 N64 K16 in a dependent chain, one CTA per SM"),
+    ("umma_m64n64_2cta_mac_per_clk_sm", "tcgen05.mma M64 N64 K16 MACs per clock per SM, two CTAs per SM"),
+    ("umma_m128n64_2cta_mac_per_clk_sm", "tcgen05.mma M128 N64 K16 MACs per clock per SM, two CTAs per SM"),
+    ("umma_attn_block_2cta_cycles", "cycles per attention key block per CTA (8 x M64 N64 + 4 x M64 N128 K16), "
+                                    "two CTAs per SM"),
 ]
 
 
