@@ -123,6 +123,44 @@ def test_empty_rows_and_bad_blocks(q8):
     assert q8.q8_device_error() == 0
 
 
+def test_many_items_per_cta_with_empty_lists(q8):
+    """1024 (head, query block) items, more than the kernel's CTAs, so each CTA walks several
+    of them with two Q buffers in turn.  Empty block lists sit mid-walk (every fifth item of
+    head 1) and at the walk's end (the lowest query blocks of the last key/value group, which
+    the kernel takes last); their rows must be 0 and the others must match the oracle."""
+    rng = np.random.default_rng(31)
+    H, Hkv, Tn = 8, 2, 8192
+    nb = Tn // 64
+    q, k, v = workloads.bsa_qkv(rng, H, Hkv, Tn)
+    rp0, ci0 = workloads.bsa_mask(rng, H, Tn, 0.1)
+    empty = set()
+    for qb in range(0, nb, 5):
+        empty.add((1, qb))
+    for h in range(H - H // Hkv, H):
+        for qb in range(12):
+            empty.add((h, qb))
+    row_ptr, cols = [0], []
+    for h in range(H):
+        for qb in range(nb):
+            r = h * nb + qb
+            if (h, qb) not in empty:
+                cols.extend(ci0[rp0[r]:rp0[r + 1]].tolist())
+            row_ptr.append(len(cols))
+    rp, ci = np.array(row_ptr, np.int32), np.array(cols, np.int32)
+    o = _run(q8, q, k, v, rp, ci)
+    o_np = o.cpu().numpy()
+    for (h, qb) in empty:
+        assert not np.any(o_np[h, 64 * qb:64 * qb + 64]), (h, qb)
+    heads = np.concatenate([[0, H - 1, 1], rng.integers(0, H, 400)])
+    toks = np.concatenate([[Tn - 1, 64 * 12, 64 * 5 + 3], rng.integers(0, Tn, 400)])
+    keep = np.array([(int(h), int(t) // 64) not in empty for h, t in zip(heads, toks)])
+    heads, toks = heads[keep], toks[keep]
+    ref = OB.attention_at(q, k, v, rp, ci, heads, toks)
+    _close(o_np[heads, toks], ref, "many items per CTA")
+    assert np.array_equal(o_np, _run(q8, q, k, v, rp, ci).cpu().numpy())  # deterministic
+    assert q8.q8_device_error() == 0
+
+
 def test_binding_refuses_strided_block_lists(q8):
     """A strided int32 view of the block list would hand the kernel the wrong words: the
     binding refuses it before anything launches."""
