@@ -22,6 +22,11 @@
 // natural order (e bits, then t bits across lanes, then c bits), so every rounding is the
 // oracle's.  The 24 code bits of (c, t) sit at stream bits 96 c + 24 t: lanes t < 3 each
 // form one of the three words of block c from their chunk and the next lane's.
+// The butterflies, the sums and the threshold differences run on packed binary32 pairs
+// (add / fma .f32x2, one rounding per element as the scalar operations): element e of chunk c
+// shares a register pair with element e of chunk c + 2, so one instruction does two chunks';
+// a - b is fma(-1, b, a), whose product is exact.  Products that feed additions stay scalar
+// (__fmul_rn is never fused into an FMA; a packed product was measured being fused).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -43,42 +48,51 @@ __constant__ float kLevel[8] = {0.2451f,  0.7560f,  1.3440f,  2.1520f,
 
 constexpr int kE = 8;  // elements of a (c, t) chunk
 
-// Unnormalised WHT of a group held by four lanes (v[c][e] = element 32 c + 8 t + e).
-__device__ __forceinline__ void fwht_group(float (&v)[4][kE], int t) {
+// a - b with one rounding (the product with -1 is exact)
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  return __ffma2_rn(make_float2(-1.0f, -1.0f), b, a);
+}
+
+// Unnormalised WHT of a group held by four lanes: w[c][e] = (element 32 c + 8 t + e,
+// element 32 (c + 2) + 8 t + e), c = 0, 1.
+__device__ __forceinline__ void fwht_group(float2 (&w)[2][kE], int t) {
 #pragma unroll
   for (int h = 1; h < kE; h <<= 1)  // h = 1, 2, 4: inside a chunk
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
       for (int e = 0; e < kE; ++e)
         if ((e & h) == 0) {
-          const float a = v[c][e], b = v[c][e + h];
-          v[c][e] = __fadd_rn(a, b);
-          v[c][e + h] = __fsub_rn(a, b);
+          const float2 a = w[c][e], b = w[c][e + h];
+          w[c][e] = __fadd2_rn(a, b);
+          w[c][e + h] = sub2(a, b);
         }
 #pragma unroll
   for (int o = 1; o < 4; o <<= 1) {  // h = 8, 16: the lane t ^ o; the upper lane takes a - b
     // q + (+-1) v in one rounding: the product with +-1 is exact, so this is q +- v
     const float sg = (t & o) ? -1.0f : 1.0f;
+    const float2 sg2 = make_float2(sg, sg);
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
       for (int e = 0; e < kE; ++e) {
-        const float q = __shfl_xor_sync(kFull, v[c][e], o);
-        v[c][e] = __fmaf_rn(sg, v[c][e], q);
+        const float2 q = make_float2(__shfl_xor_sync(kFull, w[c][e].x, o), __shfl_xor_sync(kFull, w[c][e].y, o));
+        w[c][e] = __ffma2_rn(sg2, w[c][e], q);
       }
   }
 #pragma unroll
-  for (int hc = 1; hc < 4; hc <<= 1)  // h = 32, 64: across chunks of the lane
+  for (int e = 0; e < kE; ++e) {  // h = 32: chunk 0 with 1 and 2 with 3, i.e. w[0] with w[1]
+    const float2 a = w[0][e], b = w[1][e];
+    w[0][e] = __fadd2_rn(a, b);
+    w[1][e] = sub2(a, b);
+  }
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if ((c & hc) == 0)
+  for (int c = 0; c < 2; ++c)  // h = 64: chunk c with c + 2, the two halves of a pair
 #pragma unroll
-        for (int e = 0; e < kE; ++e) {
-          const float a = v[c][e], b = v[c + hc][e];
-          v[c][e] = __fadd_rn(a, b);
-          v[c + hc][e] = __fsub_rn(a, b);
-        }
+    for (int e = 0; e < kE; ++e) {
+      const float a = w[c][e].x, b = w[c][e].y;
+      w[c][e] = make_float2(__fadd_rn(a, b), __fsub_rn(a, b));
+    }
 }
 
 struct Kv3Params {
@@ -93,29 +107,37 @@ struct Kv3Params {
   int64_t n;
 };
 
-// the lane's four 8-element chunks of group g (zeros past the end)
+// the lane's four 8-element chunks of group g (zeros past the end), paired chunk c with c + 2
 template <int kXType>
 __device__ __forceinline__ void load_group(const void* x, int64_t g, int64_t n, int t,
-                                           float (&v)[4][kE]) {
+                                           float2 (&w)[2][kE]) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int64_t off = g * kD + 32 * c + 8 * t;
+    float v[kE];
     if (g >= n) {
 #pragma unroll
-      for (int e = 0; e < kE; ++e) v[c][e] = 0.0f;
+      for (int e = 0; e < kE; ++e) v[e] = 0.0f;
     } else if constexpr (kXType == 1) {
-      const uint4 w = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off));
-      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+      const uint4 u4 = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off));
+      const uint32_t u[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        v[c][2 * i] = __uint_as_float(u[i] << 16);
-        v[c][2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+        v[2 * i] = __uint_as_float(u[i] << 16);
+        v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
       }
     } else {
       const float4* f = reinterpret_cast<const float4*>(static_cast<const float*>(x) + off);
       const float4 a = __ldcs(f), b = __ldcs(f + 1);
-      v[c][0] = a.x; v[c][1] = a.y; v[c][2] = a.z; v[c][3] = a.w;
-      v[c][4] = b.x; v[c][5] = b.y; v[c][6] = b.z; v[c][7] = b.w;
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+#pragma unroll
+    for (int e = 0; e < kE; ++e) {
+      if (c < 2)
+        w[c][e].x = v[e];
+      else
+        w[c - 2][e].y = v[e];
     }
   }
 }
@@ -128,28 +150,32 @@ __global__ void __launch_bounds__(256) kv3_encode_kernel(const Kv3Params p) {
   const int64_t rounds = (p.n + nteams - 1) / nteams;  // the same for every lane of the grid
   for (int64_t it = 0; it < rounds; ++it) {
     const int64_t g = it * nteams + team;
-    float v[4][kE];
-    load_group<kXType>(p.x, g, p.n, t, v);
-    fwht_group(v, t);
+    float2 w[2][kE];
+    load_group<kXType>(p.x, g, p.n, t, w);
+    fwht_group(w, t);
     // pairwise sum of the squares: e levels in the lane, t levels across lanes, then c
-    float sc[4];
+    float2 sc[2];  // (chunk c, chunk c + 2)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float q[kE];
+    for (int c = 0; c < 2; ++c) {
+      float2 q[kE];
 #pragma unroll
-      for (int e = 0; e < kE; ++e) q[e] = __fmul_rn(v[c][e], v[c][e]);
-      sc[c] = __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
-                        __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
+      for (int e = 0; e < kE; ++e)  // scalar products: a packed one may be fused into the adds
+        q[e] = make_float2(__fmul_rn(w[c][e].x, w[c][e].x), __fmul_rn(w[c][e].y, w[c][e].y));
+      sc[c] = __fadd2_rn(__fadd2_rn(__fadd2_rn(q[0], q[1]), __fadd2_rn(q[2], q[3])),
+                         __fadd2_rn(__fadd2_rn(q[4], q[5]), __fadd2_rn(q[6], q[7])));
 #pragma unroll
-      for (int o = 1; o < 4; o <<= 1) sc[c] = __fadd_rn(sc[c], __shfl_xor_sync(kFull, sc[c], o));
+      for (int o = 1; o < 4; o <<= 1)
+        sc[c] = __fadd2_rn(sc[c], make_float2(__shfl_xor_sync(kFull, sc[c].x, o), __shfl_xor_sync(kFull, sc[c].y, o)));
     }
-    const float ss = __fadd_rn(__fadd_rn(sc[0], sc[1]), __fadd_rn(sc[2], sc[3]));
+    const float2 s01 = __fadd2_rn(sc[0], sc[1]);  // (chunks 0 + 1, chunks 2 + 3)
+    const float ss = __fadd_rn(s01.x, s01.y);
     const float s = __fsqrt_rn(__fmul_rn(ss, 0.0078125f));  // ss / 128, exact
     const float t0 = __fmul_rn(0.5006f, s), t1 = __fmul_rn(1.0500f, s), t2 = __fmul_rn(1.7480f, s);
+    const float2 t02 = make_float2(t0, t0), t12 = make_float2(t1, t1), t22 = make_float2(t2, t2);
     uint32_t chunk[4];  // 24 code bits of (c, t): element 32 c + 8 t + e at bit 3 e
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t bits = 0;
+    for (int c = 0; c < 2; ++c) {
+      uint32_t lo = 0, hi = 0;  // chunks c and c + 2
 #pragma unroll
       for (int e = kE - 1; e >= 0; --e) {
         // the three bits of the code from sign bits, each shifted in at the bottom (element
@@ -157,16 +183,18 @@ __global__ void __launch_bounds__(256) kv3_encode_kernel(const Kv3Params p) {
         // and the parity of the signs of a - t0, a - t1, a - t2 (the thresholds not passed;
         // a - t is +0 when they are equal, so a >= t is a clear sign bit).  m counts the
         // thresholds passed, so its bits are the complements of the last two: inverted below.
-        const float a = fabsf(v[c][e]);
-        const uint32_t sg = __float_as_uint(__fadd_rn(v[c][e], 0.0f));
-        const uint32_t d0 = __float_as_uint(__fsub_rn(a, t0));
-        const uint32_t d1 = __float_as_uint(__fsub_rn(a, t1));
-        const uint32_t d2 = __float_as_uint(__fsub_rn(a, t2));
-        bits = __funnelshift_l(sg, bits, 1);
-        bits = __funnelshift_l(d1, bits, 1);
-        bits = __funnelshift_l(d0 ^ d1 ^ d2, bits, 1);
+        const float2 a = make_float2(fabsf(w[c][e].x), fabsf(w[c][e].y));
+        const float2 sg = __fadd2_rn(w[c][e], make_float2(0.0f, 0.0f));
+        const float2 d0 = sub2(a, t02), d1 = sub2(a, t12), d2 = sub2(a, t22);
+        lo = __funnelshift_l(__float_as_uint(sg.x), lo, 1);
+        lo = __funnelshift_l(__float_as_uint(d1.x), lo, 1);
+        lo = __funnelshift_l(__float_as_uint(d0.x) ^ __float_as_uint(d1.x) ^ __float_as_uint(d2.x), lo, 1);
+        hi = __funnelshift_l(__float_as_uint(sg.y), hi, 1);
+        hi = __funnelshift_l(__float_as_uint(d1.y), hi, 1);
+        hi = __funnelshift_l(__float_as_uint(d0.y) ^ __float_as_uint(d1.y) ^ __float_as_uint(d2.y), hi, 1);
       }
-      chunk[c] = s == 0.0f ? 0u : bits ^ 0x6DB6DBu;  // bits 3 e and 3 e + 1 of each code
+      chunk[c] = s == 0.0f ? 0u : lo ^ 0x6DB6DBu;  // bits 3 e and 3 e + 1 of each code
+      chunk[c + 2] = s == 0.0f ? 0u : hi ^ 0x6DB6DBu;
     }
     // stream bits 96 c + 24 t: lane t < 3 forms word 3 c + t from its chunk and lane t + 1's
     const int next = (lane & ~3) | ((t + 1) & 3);
@@ -218,20 +246,30 @@ __global__ void __launch_bounds__(256) kv3_decode_kernel(const Kv3Params p) {
     uint32_t nlo[4], nhi[4];
     load_chunks(p.codes_in, gn, p.n, t, nlo, nhi);
     const float ns = gn < p.n ? __ldg(p.scales_in + gn) : 0.0f;
-    float v[4][kE];
+    float2 w[2][kE];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t chunk = ((lo[c] >> off) | (off > 8 ? hi[c] << (32 - off) : 0u)) & 0xFFFFFFu;
+    for (int c = 0; c < 2; ++c) {
+      const uint32_t ca = ((lo[c] >> off) | (off > 8 ? hi[c] << (32 - off) : 0u)) & 0xFFFFFFu;
+      const uint32_t cb = ((lo[c + 2] >> off) | (off > 8 ? hi[c + 2] << (32 - off) : 0u)) & 0xFFFFFFu;
 #pragma unroll
-      for (int e = 0; e < kE; ++e) v[c][e] = __fmul_rn(s, level[(chunk >> (3 * e)) & 7u]);
+      for (int e = 0; e < kE; ++e)  // scalar products: a packed one may be fused into the adds
+        w[c][e] = make_float2(__fmul_rn(s, level[(ca >> (3 * e)) & 7u]), __fmul_rn(s, level[(cb >> (3 * e)) & 7u]));
     }
-    fwht_group(v, t);
+    fwht_group(w, t);
     if (g < p.n) {
+      const float2 inv2 = make_float2(0.0078125f, 0.0078125f);  // / 128, exact
+      float out[4][kE];
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int e = 0; e < kE; ++e) {
+          const float2 pr = __fmul2_rn(w[c][e], inv2);
+          out[c][e] = pr.x;
+          out[c + 2][e] = pr.y;
+        }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        float o[kE];
-#pragma unroll
-        for (int e = 0; e < kE; ++e) o[e] = __fmul_rn(v[c][e], 0.0078125f);  // / 128, exact
+        const float* o = out[c];
         const int64_t eo = g * kD + 32 * c + 8 * t;
         if constexpr (kOType == 1) {
           uint32_t u[4];
