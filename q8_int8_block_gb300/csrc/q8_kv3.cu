@@ -107,7 +107,8 @@ struct Kv3Params {
   int64_t n;
 };
 
-// the lane's four 8-element chunks of group g (zeros past the end), paired chunk c with c + 2
+// binary32 input: the lane's four 8-element chunks of group g (zeros past the end), paired
+// chunk c with c + 2
 template <int kXType>
 __device__ __forceinline__ void load_group(const void* x, int64_t g, int64_t n, int t,
                                            float2 (&w)[2][kE]) {
@@ -118,14 +119,6 @@ __device__ __forceinline__ void load_group(const void* x, int64_t g, int64_t n, 
     if (g >= n) {
 #pragma unroll
       for (int e = 0; e < kE; ++e) v[e] = 0.0f;
-    } else if constexpr (kXType == 1) {
-      const uint4 u4 = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off));
-      const uint32_t u[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __uint_as_float(u[i] << 16);
-        v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
-      }
     } else {
       const float4* f = reinterpret_cast<const float4*>(static_cast<const float*>(x) + off);
       const float4 a = __ldcs(f), b = __ldcs(f + 1);
@@ -142,16 +135,50 @@ __device__ __forceinline__ void load_group(const void* x, int64_t g, int64_t n, 
   }
 }
 
+// bfloat16 input: the lane's four 16-byte pieces of group g (zeros past the end), and their
+// values paired chunk c with c + 2
+__device__ __forceinline__ void load_raw_bf16(const void* x, int64_t g, int64_t n, int t, uint4 (&raw)[4]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    raw[c] = g < n ? __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + g * kD + 32 * c + 8 * t))
+                   : make_uint4(0u, 0u, 0u, 0u);
+}
+__device__ __forceinline__ void unpack_bf16(const uint4 (&raw)[4], float2 (&w)[2][kE]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = __uint_as_float(u[i] << 16), hi = __uint_as_float(u[i] & 0xFFFF0000u);
+      if (c < 2) {
+        w[c][2 * i].x = lo;
+        w[c][2 * i + 1].x = hi;
+      } else {
+        w[c - 2][2 * i].y = lo;
+        w[c - 2][2 * i + 1].y = hi;
+      }
+    }
+  }
+}
+
 template <int kXType>
 __global__ void __launch_bounds__(256) kv3_encode_kernel(const Kv3Params p) {
   const int lane = threadIdx.x & 31, t = lane & 3;
   const int64_t team = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 2;
   const int64_t nteams = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 2;
   const int64_t rounds = (p.n + nteams - 1) / nteams;  // the same for every lane of the grid
+  // bfloat16 input: the next group's bytes are in flight while this one is encoded
+  uint4 raw[4];
+  if constexpr (kXType == 1) load_raw_bf16(p.x, team, p.n, t, raw);
   for (int64_t it = 0; it < rounds; ++it) {
     const int64_t g = it * nteams + team;
     float2 w[2][kE];
-    load_group<kXType>(p.x, g, p.n, t, w);
+    if constexpr (kXType == 1) {
+      unpack_bf16(raw, w);
+      load_raw_bf16(p.x, g + nteams, p.n, t, raw);
+    } else {
+      load_group<kXType>(p.x, g, p.n, t, w);
+    }
     fwht_group(w, t);
     // pairwise sum of the squares: e levels in the lane, t levels across lanes, then c
     float2 sc[2];  // (chunk c, chunk c + 2)
