@@ -201,7 +201,8 @@ q8_status q8_kv3_decode(const uint32_t* codes, const float* scales, void* out, q
  * blocks listed for its 64-token query block; H query heads share Hkv key/value heads
  * (head h reads h / (H / Hkv)); o_t = softmax(q_t . k_j / sqrt(d)) weighted sum of v_j; a
  * query that sees no key gets 0.
- *   q [H][T][d], k and v [Hkv][T][d]: bfloat16 bits; d = 128; T a multiple of 64.
+ *   q [H][T][d], k and v [Hkv][T][d]: bfloat16 bits; d = 128; T a multiple of 64;
+ *     H * T below 2^31 (else Q8_ERR_SHAPE).
  *   row_ptr [H * T/64 + 1], col_idx [nnz]: int32 CSR over (head, query block) rows; the
  *     key blocks of a row ascending, each in [0, query block] (others are skipped and set
  *     bit 8 of the device error word).

@@ -461,7 +461,7 @@ q8_status q8_bsa_attention(const uint16_t* q, const uint16_t* k, const uint16_t*
   if (otype != Q8_F32 && otype != Q8_BF16) return Q8_ERR_DTYPE;
   if (d != 128 || H < 0 || Hkv <= 0 || T < 0 || T % 64 != 0 || nnz < 0 || H % Hkv != 0 ||
       H > 0x7FFFFFFF || T > 0x7FFFFFFF || static_cast<double>(H) * T * d * 4 > 281474976710656.0 ||
-      static_cast<double>(H) * (T / 64) >= 2147483647.0)
+      static_cast<double>(H) * T > 2147483647.0)  // the tiles' row coordinates are 32-bit
     return Q8_ERR_SHAPE;
   if (H * T > 0 && (q == nullptr || k == nullptr || v == nullptr || o == nullptr || row_ptr == nullptr ||
                     (nnz > 0 && col_idx == nullptr)))

@@ -11,22 +11,22 @@
 //
 // Design (one CTA per head and query block, 64 query rows, two CTAs per SM):
 //  - warp 0 (one thread) loads the Q tile once and, per listed key block, the K tile
-//    (64 x 128 bfloat16, two 64-column boxes with 128-byte swizzle) by TMA into a
-//    three-stage ring; warp 6 (one thread) loads the V tiles into a two-stage ring;
+//    (64 x 128 bfloat16, two 64-column boxes with 128-byte swizzle) by TMA into a two-stage
+//    ring; warp 6 (one thread) loads the V tiles into another two-stage ring;
 //  - warp 1 (one thread) issues the tcgen05 MMAs: S_j = Q K_j^T (M = 64, N = 64, eight
 //    K = 16 steps) into one of two S buffers in TMEM, and O += P_j V_j (M = 64, N = 128,
 //    four K = 16 steps, V read in place as an MN-major operand) into the O accumulator in
-//    TMEM.  S_{j+2} is issued as soon as the softmax warps have read S_j, ahead of PV_j, so
-//    the tensor pipe (which runs its MMAs in order) never makes a score tile wait behind a
-//    PV product: the round trips of the MMAs stay off the per-block critical path;
+//    TMEM.  One group per key block: once the softmax warps have written P_j (so they have
+//    read S_j), S_{j+2} (into S_j's buffer) and PV_j are issued together and committed to one
+//    of two alternating barriers; S_{j+2} is then ready a whole block ahead of its use;
 //  - warps 2-5 (the four TMEM lane quarters; an M = 64 accumulator keeps rows 16q .. 16q+15
-//    in the first 16 lanes of quarter q) run the online softmax: each row is split over two
-//    threads (32 keys each), base-2 exponentials, P rounded to bfloat16 into a swizzled
-//    shared-memory tile that the PV MMA reads as its A operand (written once PV_{j-1} is
-//    done with it).  The running maximum used as the exponent reference moves only when a
-//    row's maximum rises by more than 2^8; then that warp rescales its rows of O in TMEM
-//    (PV_{j-1} is done by then), so most blocks need no correction of O at all; the weights
-//    stay <= 2^8 and the final o = O / l is unchanged.
+//    in the first 16 lanes of quarter q) run the online softmax, waiting once per block: each
+//    row is split over two threads (32 keys each), base-2 exponentials, P rounded to bfloat16
+//    into one of two swizzled shared-memory tiles that the PV MMA reads as its A operand.
+//    The running maximum used as the exponent reference moves only when a row's maximum
+//    rises by more than 2^8; then that warp waits for the previous PV and rescales its rows
+//    of O in TMEM, so most blocks need no correction of O at all; the weights stay <= 2^8
+//    and the final o = O / l is unchanged.
 // The grid runs key/value head by key/value head, and within one the query blocks from the
 // last (most key blocks) to the first, the heads of a group side by side: the K and V tiles
 // of the key/value head in flight (16 MB at 32K tokens) stay in L2 across the query blocks

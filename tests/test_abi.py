@@ -178,6 +178,9 @@ def test_bsa_entry_rejects_bad_arguments(L):
     assert call(11, 64) == 2          # head dim other than 128
     assert call(10, 100) == 2         # T not a multiple of 64
     assert call(9, 3) == 2            # H not a multiple of Hkv
+    a = list(ok)
+    a[8], a[10] = 1 << 22, 1 << 10    # H * T = 2^32: beyond the tiles' 32-bit row coordinates
+    assert F(*a) == 2
     assert call(0, None) == 1
     assert call(4, None) == 1         # nnz > 0 without col_idx
     assert call(1, P(FAKE + 2)) == 3
