@@ -119,8 +119,15 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+# the current stream's handle without building a torch Stream object (a few microseconds per
+# call otherwise); torch has long provided the query, the fallback covers a build without it
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream):
     if stream is None:
+        if _RAW_STREAM is not None:
+            return ctypes.c_void_p(_RAW_STREAM(torch.cuda.current_device()))
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
 
